@@ -1,0 +1,353 @@
+"""Benchmark of the GPT-2 forward pass on GB300: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2-124m-b16] [--precision bf16]
+
+A step is one gpt2_forward over a batch of B sequences of T tokens of
+seeded synthetic input (random-init GPT-2 weights, uniform token ids), with
+the logits and the softmax probabilities written.  `value` is tokens/s of
+the whole job (all ranks), timed with CUDA events around exactly K steps
+bracketed by a barrier and a device synchronisation, max over ranks.  The
+working set (logits plus probabilities alone are 6.6 GB at B=16) is far
+larger than the 129 MB L2, so no L2 flush runs between steps.
+
+Several GPUs run independent replicas (the forward pass of one batch needs
+no exchange between GPUs): each rank processes its own batch, no collective
+touches the data path, and scaling is weak.
+
+--impl reference times the CPU oracle (the plain double-precision C
+implementation) on the host cores, on a bounded sample of the same workload
+per step; rank 0 alone runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gpt_transformer_forward_gb300 import inputs  # noqa: E402
+
+METRIC = "GPT-2 124M forward tokens/s (B=16,T=1024) on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------- algorithmic cost
+def stage_costs(cfg, B, T, act_bytes=2):
+    """Algorithmic FLOPs and bytes of each stage of one forward pass (every
+    layer summed): bytes count each input read once and each output written
+    once, with operand buffers of act_bytes (2 for bf16), the residual
+    stream, logits and probabilities fp32, weights bf16, and the causal
+    attention FLOPs only (j <= t)."""
+    C, L, NH, Vp = cfg.channels, cfg.num_layers, cfg.num_heads, cfg.padded_vocab_size
+    hs = C // NH
+    N = B * T
+    a, w = act_bytes, 2
+    ln_bytes = N * C * 4 + N * C * a + 2 * C * 4
+    pairs = T * (T + 1) // 2
+    return {
+        "encoder": (0, 4 * N + N * C * 4 + T * C * 4 + N * C * 4),
+        "ln1": (0, L * ln_bytes),
+        "qkv": (L * 2 * N * C * 3 * C, L * (N * C * a + 3 * C * C * w + 3 * C * 4 + N * 3 * C * a)),
+        "attention": (L * B * NH * 4 * hs * pairs, L * (N * 3 * C * a + N * C * a)),
+        "attproj": (L * 2 * N * C * C, L * (N * C * a + C * C * w + C * 4 + 2 * N * C * 4)),
+        "ln2": (0, L * ln_bytes),
+        "fc": (L * 2 * N * C * 4 * C, L * (N * C * a + 4 * C * C * w + 4 * C * 4 + N * 4 * C * a)),
+        "fcproj": (L * 2 * N * 4 * C * C, L * (N * 4 * C * a + 4 * C * C * w + C * 4 + 2 * N * C * 4)),
+        "lnf": (0, ln_bytes),
+        "lm_head": (2 * N * C * Vp, N * C * a + Vp * C * w + N * Vp * 4),
+        "softmax": (0, 2 * N * Vp * 4),
+    }
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_sample_run(w, params, tok, T_s):
+    """One oracle forward pass over sequence 0's first T_s tokens (logits and
+    probabilities, every column); returns seconds."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.forward(w.cfg, params, tok[:1, :T_s])
+    return time.perf_counter() - t0
+
+
+def oracle_threads():
+    return int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+
+def cpu_baseline(w, params, tok, target_s=15.0):
+    """The oracle timed on a bounded sample (about target_s seconds)."""
+    t8 = oracle_sample_run(w, params, tok, 8)
+    T_s = int(max(8, min(w.T, 8 * target_s / max(t8, 1e-3))))
+    dt = oracle_sample_run(w, params, tok, T_s)
+    return {"value": T_s / dt, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+            "sample": f"1 sequence x {T_s} tokens of {w.name} (double precision, logits and probs), {dt:.1f} s"}
+
+
+# ------------------------------------------------------------------- arms
+def dist_setup(n_gpus):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        pg = dist
+    return rank, world, local, pg
+
+
+def run_reference(args):
+    rank, world, _, pg = dist_setup(args.gpus)
+    if rank != 0:
+        if pg is not None:
+            pg.barrier()
+        return
+    w = inputs.WORKLOADS[args.workload]
+    params, tok = inputs.workload_inputs(w)
+    # size one step's sample so that warm-up plus timed steps take ~2 minutes
+    t8 = oracle_sample_run(w, params, tok, 8)
+    per_step = 120.0 / (args.steps + args.warmup)
+    T_s = int(max(1, min(w.T, 8 * per_step / max(t8, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_run(w, params, tok, T_s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample_run(w, params, tok, T_s)
+    dt = time.perf_counter() - t0
+    value = args.steps * T_s / dt
+    sample = f"per step: 1 sequence x {T_s} tokens of {w.name} (double precision, logits and probs)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.barrier()
+
+
+def run_ours(args):
+    import torch
+    from gpt_transformer_forward_gb300 import binding as ab
+    from gpt_transformer_forward_gb300.runner import GPT2Model
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev_index = torch.cuda.current_device()
+    w = inputs.WORKLOADS[args.workload]
+    precision = ab.PRECISIONS[args.precision]
+    params, tok = inputs.workload_inputs(w)
+    if rank > 0:  # replicas: each rank its own batch of token ids
+        tok = inputs.make_tokens(w.token_seed + 7919 * rank, w.B, w.T, w.cfg.vocab_size)
+    model = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    logits, probs = model.new_outputs(w.B, w.T)
+    tok_d = torch.from_numpy(tok).cuda()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(args.warmup):
+        model.forward(tok_d, logits, probs)
+    torch.cuda.synchronize()
+    assert ab.gpt2_get_error() == 0
+
+    # ---- device-resident timed region
+    clocks = ClockSampler(dev_index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        model.forward(tok_d, logits, probs)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if pg is not None:
+        t = torch.tensor([ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    err = ab.gpt2_get_error()
+
+    # ---- end to end: pinned host tokens in, logits and probabilities out
+    tok_h = torch.from_numpy(tok).pin_memory()
+    logits_h = torch.empty(logits.shape, dtype=torch.float32, pin_memory=True)
+    probs_h = torch.empty(probs.shape, dtype=torch.float32, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        tok_d.copy_(tok_h, non_blocking=True)
+        model.forward(tok_d, logits, probs)
+        logits_h.copy_(logits, non_blocking=True)
+        probs_h.copy_(probs, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if pg is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    # ---- per-stage times (CUDA events between stages) and the roofline
+    prof_runs = 5
+    stage_ms = {k: 0.0 for k in ab.STAGES}
+    for _ in range(prof_runs):
+        for k, v in model.forward_profile(tok_d, logits, probs).items():
+            stage_ms[k] += v / prof_runs
+    peaks, peak_src = load_peaks()
+    costs = stage_costs(w.cfg, w.B, w.T, act_bytes=2 if precision == ab.GPT2_BF16 else 4)
+    hbm = peaks["hbm_gbs"] * 1e9
+    tensor = peaks["bf16_tflops_sustained"] * 1e12
+    stages, roof_ms = {}, 0.0
+    for k, (flops, nbytes) in costs.items():
+        t_roof = max(flops / tensor, nbytes / hbm) * 1e3
+        roof_ms += t_roof
+        stages[k] = {"ms": round(stage_ms[k], 4), "roofline_ms": round(t_roof, 4),
+                     "bound": "tensor" if flops / tensor > nbytes / hbm else "hbm"}
+    dom = max(stage_ms, key=stage_ms.get)
+    flops, nbytes = costs[dom]
+    launches = w.cfg.num_layers if dom not in ("encoder", "lnf", "lm_head", "softmax") else 1
+    per_launch_ms = stage_ms[dom] / launches
+    if flops / tensor > nbytes / hbm:
+        achieved = flops / launches / (per_launch_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    else:
+        achieved = nbytes / launches / (per_launch_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = peak_src
+
+    tokens = w.B * w.T
+    value = world * tokens / (ms * 1e-3)
+    launches_per_step = 1 + 7 * w.cfg.num_layers + 3
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, params, tok)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": args.precision, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "layers": w.cfg.num_layers,
+                   "channels": w.cfg.channels, "heads": w.cfg.num_heads, "vocab": w.cfg.vocab_size,
+                   "padded_vocab": w.cfg.padded_vocab_size, "outputs": "logits+probs",
+                   "l2": "no flush: working set > 7 GB, L2 129 MB", "parallelism": f"replicas{world}"},
+        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": int(tok.nbytes), "d2h_bytes_per_step": int(logits.numel() * 4 * 2)},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof,
+        "pass_roofline": {"roofline_ms": roof_ms, "measured_ms": ms, "frac": roof_ms / ms,
+                          "peaks": "hbm_gbs, bf16_tflops_sustained of " + peak_src},
+        "stages": stages,
+        "clocks": clk,
+        "device_error_word": err,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "tf32", "fp32"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

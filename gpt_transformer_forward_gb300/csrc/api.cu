@@ -1,0 +1,561 @@
+// api.cu -- the C ABI (declared in include/gpt2fwd.h): argument checks,
+// workspace and weight-packing layouts, and the orchestration of the
+// forward pass and of the decode step on the caller's stream.
+//
+// Forward pass order (pre-LayerNorm GPT-2 blocks; the ECE408 GPT-2 project
+// page names the kernels, llm.c's profile splits the step into encoder,
+// forward blocks and classifier):
+//   encoder -> L x [LN1 -> QKV GEMM(+bias) -> attention -> attn-proj GEMM
+//   (+bias, +residual in place) -> LN2 -> FC GEMM(+bias, GELU) -> FC-proj
+//   GEMM(+bias, +residual in place)] -> LN_f -> LM-head GEMM (tied wte) ->
+//   softmax.
+// In GPT2_BF16 mode LayerNorm, attention and the GELU epilogue write bf16
+// directly, because that is the only form in which the next GEMM consumes
+// them; the residual stream x stays fp32.
+#include <stdio.h>
+
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kernels.cuh"
+
+namespace gpt2 {
+
+int num_sms() {
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+thread_local std::string g_last_cuda_error;
+
+int check_launch() {
+  const cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) {
+    g_last_cuda_error = cudaGetErrorString(e);
+    cudaGetLastError();
+    return GPT2_ERR_CUDA;
+  }
+  return GPT2_OK;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+#define RETURN_IF(cond, code) \
+  do {                        \
+    if (cond) return (code);  \
+  } while (0)
+
+#define TRY(expr)                   \
+  do {                              \
+    const int _rc = (expr);         \
+    if (_rc != GPT2_OK) return _rc; \
+  } while (0)
+
+bool valid_precision(int p) { return p == GPT2_FP32 || p == GPT2_TF32 || p == GPT2_BF16; }
+
+int check_config(const GPT2Config* c) {
+  RETURN_IF(c == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(c->max_seq_len <= 0 || c->vocab_size <= 0 || c->padded_vocab_size < c->vocab_size ||
+                c->num_layers <= 0 || c->num_heads <= 0 || c->channels <= 0,
+            GPT2_ERR_ARG);
+  RETURN_IF(c->channels % c->num_heads != 0, GPT2_ERR_SHAPE);
+  RETURN_IF(c->channels % 8 != 0 || c->padded_vocab_size % 4 != 0, GPT2_ERR_SHAPE);
+  return GPT2_OK;
+}
+
+// every attention kernel (tensor-core, fp32 and decode) handles head sizes 16, 32, 64
+int check_attention_shape(int C, int NH) {
+  const int hs = C / NH;
+  return (hs == 16 || hs == 32 || hs == 64) ? GPT2_OK : GPT2_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------ parameter tensor offsets
+struct ParamOffsets {
+  size_t wte, wpe, ln1w, ln1b, qkvw, qkvb, attprojw, attprojb, ln2w, ln2b, fcw, fcb, fcprojw, fcprojb, lnfw, lnfb,
+      total;
+};
+
+ParamOffsets param_offsets(const GPT2Config* c) {
+  const size_t C = c->channels, L = c->num_layers, Vp = c->padded_vocab_size, maxT = c->max_seq_len;
+  ParamOffsets o;
+  size_t p = 0;
+  o.wte = p; p += Vp * C;
+  o.wpe = p; p += maxT * C;
+  o.ln1w = p; p += L * C;
+  o.ln1b = p; p += L * C;
+  o.qkvw = p; p += L * 3 * C * C;
+  o.qkvb = p; p += L * 3 * C;
+  o.attprojw = p; p += L * C * C;
+  o.attprojb = p; p += L * C;
+  o.ln2w = p; p += L * C;
+  o.ln2b = p; p += L * C;
+  o.fcw = p; p += L * 4 * C * C;
+  o.fcb = p; p += L * 4 * C;
+  o.fcprojw = p; p += L * 4 * C * C;
+  o.fcprojb = p; p += L * C;
+  o.lnfw = p; p += C;
+  o.lnfb = p; p += C;
+  o.total = p;
+  return o;
+}
+
+// bf16 copies of the five weight matrices, each 256-byte aligned
+struct PackedOffsets {
+  size_t wte, qkvw, attprojw, fcw, fcprojw, total;  // byte offsets
+};
+
+PackedOffsets packed_offsets(const GPT2Config* c) {
+  const size_t C = c->channels, L = c->num_layers, Vp = c->padded_vocab_size;
+  PackedOffsets o;
+  size_t p = 0;
+  o.wte = p; p = round_up(p + Vp * C * 2, 256);
+  o.qkvw = p; p = round_up(p + L * 3 * C * C * 2, 256);
+  o.attprojw = p; p = round_up(p + L * C * C * 2, 256);
+  o.fcw = p; p = round_up(p + L * 4 * C * C * 2, 256);
+  o.fcprojw = p; p = round_up(p + L * 4 * C * C * 2, 256);
+  o.total = p;
+  return o;
+}
+
+// ---------------------------------------------------------- workspace
+struct Workspace {
+  size_t x, ln, qkv, qkv16, att, fch, dec, total;  // byte offsets
+};
+
+Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
+  const size_t N = static_cast<size_t>(B) * T, C = c->channels;
+  const size_t act = (precision == GPT2_BF16) ? 2 : 4;  // operand buffers
+  Workspace w;
+  size_t p = 0;
+  w.x = p; p = round_up(p + N * C * 4, 256);
+  w.ln = p; p = round_up(p + N * C * act, 256);
+  w.qkv = p; p = round_up(p + N * 3 * C * act, 256);
+  w.qkv16 = p;
+  if (precision == GPT2_TF32) p = round_up(p + N * 3 * C * 2, 256);  // bf16 copy for the attention kernel
+  w.att = p; p = round_up(p + N * C * act, 256);
+  w.fch = p; p = round_up(p + N * 4 * C * act, 256);
+  w.dec = p; p = round_up(p + decode_attention_scratch_floats(B, c->channels, c->num_heads, c->max_seq_len) * 4, 256);
+  w.total = p;
+  return w;
+}
+
+size_t kv_elem_bytes(int precision) { return precision == GPT2_BF16 ? 2 : 4; }
+
+// elements of one layer's cache slab [2][B][NH][maxT][hs]
+size_t kv_layer_elems(const GPT2Config* c, int B) {
+  return 2ull * B * c->num_heads * c->max_seq_len * (c->channels / c->num_heads);
+}
+
+// One GEMM site: picks the kernel for the precision mode.
+int gemm(int precision, void* out, const void* A, const void* W, const float* bias, int M, int N, int K, int epi,
+         cudaStream_t s) {
+  if (precision == GPT2_FP32) {
+    launch_gemm_simt(static_cast<float*>(out), static_cast<const float*>(A), static_cast<const float*>(W), bias, M,
+                     N, K, epi, s);
+    return check_launch();
+  }
+  if (precision == GPT2_TF32 && epi == kEpiGeluBF16) {
+    // tf32 operands with an fp32 GELU output: GEMM then the GELU kernel
+    TRY(launch_gemm_tc(out, A, W, bias, M, N, K, kEpiF32, false, s));
+    launch_gelu(static_cast<float*>(out), static_cast<const float*>(out), M * N, s);
+    return check_launch();
+  }
+  return launch_gemm_tc(out, A, W, bias, M, N, K, epi, precision == GPT2_BF16, s);
+}
+
+// Records a CUDA event on the stream after each stage of the forward pass;
+// stage_ms[k] accumulates the time between the event before and after each
+// occurrence of stage k.
+struct StageProfiler {
+  cudaStream_t stream;
+  std::vector<cudaEvent_t> events;
+  std::vector<int> stages;  // stage of the interval ending at events[i + 1]
+  int begin() {
+    return record(-1);
+  }
+  int record(int stage) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return GPT2_ERR_CUDA;
+    events.push_back(e);
+    if (stage >= 0) stages.push_back(stage);
+    return cudaEventRecord(e, stream) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  }
+  int finish(float* stage_ms, int n_stages) {
+    int rc = cudaEventSynchronize(events.back()) == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+    for (size_t i = 0; rc == GPT2_OK && i + 1 < events.size(); ++i) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, events[i], events[i + 1]) != cudaSuccess) rc = GPT2_ERR_CUDA;
+      if (stages[i] < n_stages) stage_ms[stages[i]] += ms;
+    }
+    for (cudaEvent_t e : events) cudaEventDestroy(e);
+    events.clear();
+    return rc;
+  }
+};
+
+}  // namespace
+}  // namespace gpt2
+
+using namespace gpt2;
+
+// ====================================================================== ABI
+extern "C" {
+
+int encoder_forward(float* out, const int* tok, const float* wte, const float* wpe, int B, int T, int C, int V,
+                    void* stream) {
+  RETURN_IF(!out || !tok || !wte || !wpe, GPT2_ERR_ARG);
+  RETURN_IF(B < 0 || T < 0 || C <= 0 || V <= 0, GPT2_ERR_ARG);
+  RETURN_IF(C % 4 != 0, GPT2_ERR_SHAPE);
+  RETURN_IF(!aligned16(out) || !aligned16(wte) || !aligned16(wpe), GPT2_ERR_ALIGN);
+  if (B == 0 || T == 0) return GPT2_OK;
+  launch_encoder(out, tok, wte, wpe, B * T, T, C, V, as_stream(stream));
+  return check_launch();
+}
+
+int layernorm_forward(float* out, float* mean, float* rstd, const float* inp, const float* w, const float* b, int N,
+                      int C, void* stream) {
+  RETURN_IF(!out || !inp || !w || !b, GPT2_ERR_ARG);
+  RETURN_IF(N < 0 || C <= 0, GPT2_ERR_ARG);
+  RETURN_IF(C % 4 != 0, GPT2_ERR_SHAPE);
+  RETURN_IF(!aligned16(out) || !aligned16(inp) || !aligned16(w) || !aligned16(b), GPT2_ERR_ALIGN);
+  if (N == 0) return GPT2_OK;
+  launch_layernorm_f32(out, mean, rstd, inp, w, b, N, C, as_stream(stream));
+  return check_launch();
+}
+
+size_t matmul_workspace_size(int N, int C, int OC, int precision) {
+  if (precision != GPT2_BF16 || N <= 0 || C <= 0 || OC <= 0) return 0;
+  return round_up(static_cast<size_t>(N) * C * 2, 256) + round_up(static_cast<size_t>(OC) * C * 2, 256);
+}
+
+int matmul_forward(float* out, const float* inp, const float* W, const float* bias, int N, int C, int OC,
+                   int precision, void* workspace, size_t ws_bytes, void* stream) {
+  RETURN_IF(!out || !inp || !W, GPT2_ERR_ARG);
+  RETURN_IF(N < 0 || C <= 0 || OC <= 0 || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(out) || !aligned16(inp) || !aligned16(W) || (bias && !aligned16(bias)), GPT2_ERR_ALIGN);
+  if (N == 0) return GPT2_OK;
+  cudaStream_t s = as_stream(stream);
+  if (precision == GPT2_FP32) return gemm(precision, out, inp, W, bias, N, OC, C, kEpiF32, s);
+  RETURN_IF(C % 8 != 0 || OC % 4 != 0, GPT2_ERR_SHAPE);
+  if (precision == GPT2_TF32) return launch_gemm_tc(out, inp, W, bias, N, OC, C, kEpiF32, false, s);
+  const size_t need = matmul_workspace_size(N, C, OC, precision);
+  RETURN_IF(workspace == nullptr || ws_bytes < need, GPT2_ERR_WORKSPACE);
+  RETURN_IF((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0, GPT2_ERR_ALIGN);
+  __nv_bfloat16* a16 = static_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* w16 =
+      reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + round_up(static_cast<size_t>(N) * C * 2, 256));
+  launch_f32_to_bf16(a16, inp, static_cast<long long>(N) * C, s);
+  launch_f32_to_bf16(w16, W, static_cast<long long>(OC) * C, s);
+  TRY(check_launch());
+  return launch_gemm_tc(out, a16, w16, bias, N, OC, C, kEpiF32, true, s);
+}
+
+size_t attention_workspace_size(int B, int T, int C, int precision) {
+  if (precision == GPT2_FP32 || B <= 0 || T <= 0 || C <= 0) return 0;
+  return round_up(static_cast<size_t>(B) * T * 3 * C * 2, 256);
+}
+
+int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH, int precision, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  RETURN_IF(!out || !qkv, GPT2_ERR_ARG);
+  RETURN_IF(B < 0 || T < 0 || C <= 0 || NH <= 0 || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(C % NH != 0, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(C, NH));
+  RETURN_IF(!aligned16(out) || !aligned16(qkv), GPT2_ERR_ALIGN);
+  if (B == 0 || T == 0) return GPT2_OK;
+  cudaStream_t s = as_stream(stream);
+  if (precision == GPT2_FP32) {
+    TRY(launch_attention_f32(out, qkv, B, T, C, NH, s));
+    return check_launch();
+  }
+  RETURN_IF(workspace == nullptr || ws_bytes < attention_workspace_size(B, T, C, precision), GPT2_ERR_WORKSPACE);
+  RETURN_IF(!aligned16(workspace), GPT2_ERR_ALIGN);
+  __nv_bfloat16* q16 = static_cast<__nv_bfloat16*>(workspace);
+  launch_f32_to_bf16(q16, qkv, static_cast<long long>(B) * T * 3 * C, s);
+  TRY(launch_attention_bf16(out, false, q16, B, T, C, NH, s));
+  return check_launch();
+}
+
+int gelu_forward(float* out, const float* inp, int n, void* stream) {
+  RETURN_IF(!out || !inp || n < 0, GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(out) || !aligned16(inp), GPT2_ERR_ALIGN);
+  if (n == 0) return GPT2_OK;
+  launch_gelu(out, inp, n, as_stream(stream));
+  return check_launch();
+}
+
+int residual_forward(float* out, const float* a, const float* b, int n, void* stream) {
+  RETURN_IF(!out || !a || !b || n < 0, GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(out) || !aligned16(a) || !aligned16(b), GPT2_ERR_ALIGN);
+  if (n == 0) return GPT2_OK;
+  launch_residual(out, a, b, n, as_stream(stream));
+  return check_launch();
+}
+
+int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, void* stream) {
+  RETURN_IF(!probs || !logits || N < 0 || V <= 0 || Vp < V, GPT2_ERR_ARG);
+  RETURN_IF(Vp % 4 != 0, GPT2_ERR_SHAPE);
+  RETURN_IF(!aligned16(probs) || !aligned16(logits), GPT2_ERR_ALIGN);
+  if (N == 0) return GPT2_OK;
+  launch_softmax(probs, logits, N, V, Vp, as_stream(stream));
+  return check_launch();
+}
+
+int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, void* stream) {
+  RETURN_IF(!next || !logits || B < 0 || V <= 0 || Vp < V, GPT2_ERR_ARG);
+  if (B == 0) return GPT2_OK;
+  launch_argmax(next, logits, B, V, Vp, as_stream(stream));
+  return check_launch();
+}
+
+size_t gpt2_num_parameters(const GPT2Config* cfg) {
+  if (check_config(cfg) != GPT2_OK) return 0;
+  return param_offsets(cfg).total;
+}
+
+size_t gpt2_packed_weights_size(const GPT2Config* cfg, int precision) {
+  if (check_config(cfg) != GPT2_OK || precision != GPT2_BF16) return 0;
+  return packed_offsets(cfg).total;
+}
+
+int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, void* packed, size_t bytes, int precision,
+                         void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !valid_precision(precision), GPT2_ERR_ARG);
+  if (precision != GPT2_BF16) return GPT2_OK;
+  RETURN_IF(!packed, GPT2_ERR_ARG);
+  RETURN_IF(bytes < gpt2_packed_weights_size(cfg, precision), GPT2_ERR_WORKSPACE);
+  RETURN_IF(!aligned16(params) || (reinterpret_cast<uintptr_t>(packed) & 255u) != 0, GPT2_ERR_ALIGN);
+  const ParamOffsets po = param_offsets(cfg);
+  const PackedOffsets ko = packed_offsets(cfg);
+  const size_t C = cfg->channels, L = cfg->num_layers, Vp = cfg->padded_vocab_size;
+  uint8_t* base = static_cast<uint8_t*>(packed);
+  cudaStream_t s = as_stream(stream);
+  auto conv = [&](size_t dst_off, size_t src_off, size_t n) {
+    launch_f32_to_bf16(reinterpret_cast<__nv_bfloat16*>(base + dst_off), params + src_off,
+                       static_cast<long long>(n), s);
+  };
+  conv(ko.wte, po.wte, Vp * C);
+  conv(ko.qkvw, po.qkvw, L * 3 * C * C);
+  conv(ko.attprojw, po.attprojw, L * C * C);
+  conv(ko.fcw, po.fcw, L * 4 * C * C);
+  conv(ko.fcprojw, po.fcprojw, L * 4 * C * C);
+  return check_launch();
+}
+
+size_t gpt2_workspace_size(const GPT2Config* cfg, int B, int T, int precision) {
+  if (check_config(cfg) != GPT2_OK || B <= 0 || T <= 0 || !valid_precision(precision)) return 0;
+  return workspace_layout(cfg, B, T, precision).total;
+}
+
+size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision) {
+  if (check_config(cfg) != GPT2_OK || B <= 0 || !valid_precision(precision)) return 0;
+  return static_cast<size_t>(cfg->num_layers) * kv_layer_elems(cfg, B) * kv_elem_bytes(precision);
+}
+
+// The body shared by the full forward pass and the decode step.  decode_pos
+// < 0: rows are B sequences x T tokens at positions 0..T-1; otherwise rows
+// are the B sequences' tokens at position decode_pos (T == 1).
+static int run_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                       int decode_pos, float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes,
+                       int precision, cudaStream_t s, StageProfiler* prof = nullptr) {
+  auto mark = [&](int stage) { return prof ? prof->record(stage) : GPT2_OK; };
+  const int C = cfg->channels, L = cfg->num_layers, NH = cfg->num_heads, V = cfg->vocab_size;
+  const int Vp = cfg->padded_vocab_size, maxT = cfg->max_seq_len;
+  const int N = B * T;
+  const ParamOffsets po = param_offsets(cfg);
+  const Workspace wl = workspace_layout(cfg, B, T, precision);
+  RETURN_IF(ws_bytes < wl.total, GPT2_ERR_WORKSPACE);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* x = reinterpret_cast<float*>(ws + wl.x);
+  void* ln = ws + wl.ln;
+  void* qkv = ws + wl.qkv;
+  void* att = ws + wl.att;
+  void* fch = ws + wl.fch;
+  float* dec_scratch = reinterpret_cast<float*>(ws + wl.dec);
+  const bool bf16 = precision == GPT2_BF16;
+  const PackedOffsets ko = packed_offsets(cfg);
+  const uint8_t* pk = static_cast<const uint8_t*>(packed);
+  const size_t kv_slab = kv_layer_elems(cfg, B);
+  const size_t kv_half = kv_slab / 2;
+
+  // weight matrix of a GEMM site for layer l
+  auto wmat = [&](size_t f32_off, size_t bf16_off, size_t per_layer, int l) -> const void* {
+    if (bf16) return pk + bf16_off + static_cast<size_t>(l) * per_layer * 2;
+    return params + f32_off + static_cast<size_t>(l) * per_layer;
+  };
+  auto layernorm = [&](void* out, const float* in, size_t w_off, size_t b_off) {
+    if (bf16)
+      launch_layernorm_bf16(static_cast<__nv_bfloat16*>(out), in, params + w_off, params + b_off, N, C, s);
+    else
+      launch_layernorm_f32(static_cast<float*>(out), nullptr, nullptr, in, params + w_off, params + b_off, N, C, s);
+  };
+
+  if (decode_pos < 0)
+    launch_encoder(x, tok, params + po.wte, params + po.wpe, N, T, C, V, s);
+  else
+    launch_encoder_pos(x, tok, params + po.wte, params + po.wpe, B, decode_pos, C, V, s);
+  TRY(check_launch());
+  TRY(mark(GPT2_STAGE_ENCODER));
+
+  for (int l = 0; l < L; ++l) {
+    const size_t CC = static_cast<size_t>(C) * C;
+    layernorm(ln, x, po.ln1w + static_cast<size_t>(l) * C, po.ln1b + static_cast<size_t>(l) * C);
+    TRY(mark(GPT2_STAGE_LN1));
+    TRY(gemm(precision, qkv, ln, wmat(po.qkvw, ko.qkvw, 3 * CC, l), params + po.qkvb + static_cast<size_t>(l) * 3 * C,
+             N, 3 * C, C, bf16 ? kEpiBF16 : kEpiF32, s));
+    if (kvcache != nullptr) {
+      const int pos0 = decode_pos < 0 ? 0 : decode_pos;
+      if (bf16)
+        launch_kv_store_bf16(static_cast<__nv_bfloat16*>(kvcache) + l * kv_slab,
+                             static_cast<const __nv_bfloat16*>(qkv), B, T, C, NH, maxT, pos0, s);
+      else
+        launch_kv_store_f32(static_cast<float*>(kvcache) + l * kv_slab, static_cast<const float*>(qkv), B, T, C, NH,
+                            maxT, pos0, s);
+    }
+    TRY(mark(GPT2_STAGE_QKV));
+    if (decode_pos < 0) {
+      if (precision == GPT2_FP32) {
+        TRY(launch_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), B, T, C, NH, s));
+      } else if (precision == GPT2_TF32) {
+        __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(ws + wl.qkv16);
+        launch_f32_to_bf16(q16, static_cast<const float*>(qkv), static_cast<long long>(N) * 3 * C, s);
+        TRY(launch_attention_bf16(att, false, q16, B, T, C, NH, s));
+      } else {
+        TRY(launch_attention_bf16(att, true, static_cast<const __nv_bfloat16*>(qkv), B, T, C, NH, s));
+      }
+    } else {
+      if (bf16) {
+        const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(kvcache) + l * kv_slab;
+        launch_decode_attention_bf16(att, true, static_cast<const __nv_bfloat16*>(qkv), kc, kc + kv_half, B, C, NH,
+                                     maxT, decode_pos, dec_scratch, s);
+      } else {
+        const float* kc = static_cast<const float*>(kvcache) + l * kv_slab;
+        launch_decode_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), kc, kc + kv_half, B, C,
+                                    NH, maxT, decode_pos, dec_scratch, s);
+      }
+    }
+    TRY(check_launch());
+    TRY(mark(GPT2_STAGE_ATTENTION));
+    TRY(gemm(precision, x, att, wmat(po.attprojw, ko.attprojw, CC, l), params + po.attprojb + static_cast<size_t>(l) * C,
+             N, C, C, kEpiResidF32, s));
+    TRY(mark(GPT2_STAGE_ATTPROJ));
+    layernorm(ln, x, po.ln2w + static_cast<size_t>(l) * C, po.ln2b + static_cast<size_t>(l) * C);
+    TRY(mark(GPT2_STAGE_LN2));
+    TRY(gemm(precision, fch, ln, wmat(po.fcw, ko.fcw, 4 * CC, l), params + po.fcb + static_cast<size_t>(l) * 4 * C, N,
+             4 * C, C, kEpiGeluBF16, s));
+    TRY(mark(GPT2_STAGE_FC));
+    TRY(gemm(precision, x, fch, wmat(po.fcprojw, ko.fcprojw, 4 * CC, l),
+             params + po.fcprojb + static_cast<size_t>(l) * C, N, C, 4 * C, kEpiResidF32, s));
+    TRY(mark(GPT2_STAGE_FCPROJ));
+  }
+  layernorm(ln, x, po.lnfw, po.lnfb);
+  TRY(mark(GPT2_STAGE_LNF));
+  const void* wte = bf16 ? static_cast<const void*>(pk + ko.wte) : static_cast<const void*>(params + po.wte);
+  TRY(gemm(precision, logits, ln, wte, nullptr, N, Vp, C, kEpiF32, s));
+  TRY(mark(GPT2_STAGE_LMHEAD));
+  if (probs != nullptr) launch_softmax(probs, logits, N, V, Vp, s);
+  TRY(check_launch());
+  TRY(mark(GPT2_STAGE_SOFTMAX));
+  return GPT2_OK;
+}
+
+int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                 float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
+                 void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !tok || !logits || !workspace || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(B <= 0 || T <= 0, GPT2_ERR_ARG);
+  RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
+                (kvcache && !aligned16(kvcache)) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
+            GPT2_ERR_ALIGN);
+  return run_forward(cfg, params, packed, tok, B, T, -1, logits, probs, kvcache, workspace, ws_bytes, precision,
+                     as_stream(stream));
+}
+
+int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                         float* logits, float* probs, void* workspace, size_t ws_bytes, int precision, void* stream,
+                         float* stage_ms, int n_stages) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !tok || !logits || !workspace || !stage_ms || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(B <= 0 || T <= 0 || n_stages <= 0, GPT2_ERR_ARG);
+  RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
+                (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
+            GPT2_ERR_ALIGN);
+  StageProfiler prof{as_stream(stream), {}, {}};
+  int rc = prof.begin();
+  if (rc == GPT2_OK)
+    rc = run_forward(cfg, params, packed, tok, B, T, -1, logits, probs, nullptr, workspace, ws_bytes, precision,
+                     as_stream(stream), &prof);
+  const int rc2 = prof.finish(stage_ms, n_stages);
+  return rc != GPT2_OK ? rc : rc2;
+}
+
+int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* packed, void* kvcache, const int* tok,
+                     int B, int pos, float* logits, float* probs, void* workspace, size_t ws_bytes, int precision,
+                     void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !tok || !logits || !workspace || !kvcache || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(B <= 0, GPT2_ERR_ARG);
+  RETURN_IF(pos < 0 || pos >= cfg->max_seq_len, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) || !aligned16(kvcache) ||
+                (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
+            GPT2_ERR_ALIGN);
+  return run_forward(cfg, params, packed, tok, B, 1, pos, logits, probs, kvcache, workspace, ws_bytes, precision,
+                     as_stream(stream));
+}
+
+int gpt2_get_error(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
+    g_last_cuda_error = cudaGetErrorString(cudaGetLastError());
+    return GPT2_ERR_CUDA;
+  }
+  unsigned int w = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(w)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) {
+    g_last_cuda_error = cudaGetErrorString(cudaGetLastError());
+    return GPT2_ERR_CUDA;
+  }
+  return static_cast<int>(w);
+}
+
+const char* gpt2_strerror(int code) {
+  switch (code) {
+    case GPT2_OK: return "ok";
+    case GPT2_ERR_ARG: return "invalid argument";
+    case GPT2_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case GPT2_ERR_ALIGN: return "pointer not aligned";
+    case GPT2_ERR_WORKSPACE: return "workspace or buffer too small";
+    case GPT2_ERR_CUDA: return "CUDA error";
+    case GPT2_ERR_DEVICE: return "device-detected fault";
+    case GPT2_ERR_UNSUPPORTED: return "unsupported configuration";
+  }
+  return "unknown error";
+}
+
+const char* gpt2_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+}  // extern "C"

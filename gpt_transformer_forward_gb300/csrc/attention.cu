@@ -1,0 +1,459 @@
+// attention.cu -- causal multi-head attention of the GPT-2 forward pass.
+//
+// The result is FlashAttention's Algorithm 0 (scores, causal mask, softmax,
+// times V); it is computed the Algorithm 1 way: key/value tiles stream
+// through shared memory while each query row keeps a running maximum, a
+// running sum and an unnormalised output, so the T x T score matrix never
+// exists.  Key tiles wholly after a query tile are never visited (causal
+// tile skipping); only the diagonal tile is masked.  Heads are read in place
+// from the fused QKV buffer [B, T, 3C] (query, key, value column blocks, head
+// h = columns h*hs .. h*hs+hs-1 of each), and the output is written straight
+// into [B, T, C]: no permute or unpermute pass.
+//
+//   attn_bf16_kernel    bf16 tensor cores (mma.sync m16n8k16, fp32
+//                       accumulate), head size 16, 32 or 64, 64 query rows
+//                       per block;
+//   attn_f32_kernel     fp32 CUDA cores, reference-grade (GPT2_FP32 mode);
+//   decode kernels      one query per sequence against the KV cache, split
+//                       over positions, then a combine pass.
+#include "kernels.cuh"
+
+namespace gpt2 {
+namespace {
+
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// d += a * b, m16n8k16, bf16 inputs, fp32 accumulators
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ----------------------------------------------- bf16 tensor-core kernel
+constexpr int kBQ = 64;    // query rows per block (16 per warp)
+constexpr int kBKV = 64;   // keys per tile
+constexpr int kAttnThreads = 128;
+
+// A tile is 64 rows of HS bf16 (HS * 2 bytes, HS / 8 chunks of 16 bytes);
+// chunk c of row r is stored at chunk (c ^ (r mod chunks)) so that the eight
+// row addresses of an ldmatrix fall in distinct banks.
+template <int HS>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  constexpr int kChunks = HS / 8;
+  return static_cast<uint32_t>(row * (HS * 2) + ((chunk ^ (row & (kChunks - 1))) << 4));
+}
+
+// Loads rows [row0, row0+64) (row index = token t of sequence b) of the
+// HS-wide column block starting at `col` of qkv into a swizzled tile; rows
+// at or beyond T are zero-filled.
+template <int HS>
+__device__ __forceinline__ void load_tile(uint8_t* tile, const __nv_bfloat16* qkv, int b, int T, int C3, int col,
+                                          int row0) {
+  constexpr int kChunks = HS / 8;
+  for (int idx = threadIdx.x; idx < kBKV * kChunks; idx += kAttnThreads) {
+    const int r = idx / kChunks, c = idx % kChunks;
+    const int t = row0 + r;
+    const bool valid = t < T;
+    const __nv_bfloat16* src = qkv + (static_cast<size_t>(b) * T + (valid ? t : 0)) * C3 + col + c * 8;
+    cp_async16(tile + swz<HS>(r, c), src, valid);
+  }
+}
+
+template <int HS, bool kOutBF16>
+__global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(void* __restrict__ out,
+                                                                 const __nv_bfloat16* __restrict__ qkv, int T, int C,
+                                                                 float scale_log2) {
+  constexpr int kKS = HS / 16;  // k-steps of Q K^T over the head dimension
+  constexpr int kDT = HS / 8;   // 8-wide output column tiles
+  __shared__ __align__(128) uint8_t q_s[kBQ * HS * 2];
+  __shared__ __align__(128) uint8_t k_s[2][kBKV * HS * 2];
+  __shared__ __align__(128) uint8_t v_s[2][kBKV * HS * 2];
+
+  const int n_qt = gridDim.x;
+  const int qt = n_qt - 1 - blockIdx.x;  // longest rows first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int C3 = 3 * C;
+  const int q0 = qt * kBQ;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+
+  load_tile<HS>(q_s, qkv, b, T, C3, h * HS, q0);
+  load_tile<HS>(k_s[0], qkv, b, T, C3, C + h * HS, 0);
+  load_tile<HS>(v_s[0], qkv, b, T, C3, 2 * C + h * HS, 0);
+  cp_async_commit();
+
+  float o[kDT][4];
+#pragma unroll
+  for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY};
+  float l_r[2] = {0.f, 0.f};
+  uint32_t qf[kKS][4];
+
+  const int row_w = warp * 16;  // this warp's first query row in the tile
+  for (int j = 0; j <= qt; ++j) {
+    const int buf = j & 1;
+    if (j < qt) {  // prefetch the next key/value tile
+      load_tile<HS>(k_s[buf ^ 1], qkv, b, T, C3, C + h * HS, (j + 1) * kBKV);
+      load_tile<HS>(v_s[buf ^ 1], qkv, b, T, C3, 2 * C + h * HS, (j + 1) * kBKV);
+    }
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (j == 0) {
+#pragma unroll
+      for (int ks = 0; ks < kKS; ++ks) {
+        const int r = row_w + (lane & 15);
+        const int c = ks * 2 + (lane >> 4);
+        ldsm_x4(smem_u32(q_s) + swz<HS>(r, c), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+      }
+    }
+    // S = Q K^T for this warp's 16 rows and the tile's 64 keys
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    const uint32_t kb = smem_u32(k_s[buf]);
+#pragma unroll
+    for (int ks = 0; ks < kKS; ++ks) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int key = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int c = ks * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + swz<HS>(key, c), b0, b1, b2, b3);
+        mma_bf16(s[2 * np], qf[ks], b0, b1);
+        mma_bf16(s[2 * np + 1], qf[ks], b2, b3);
+      }
+    }
+    // scale into log2 units and mask the diagonal tile
+    const bool diag = (j == qt);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float x = s[nt][e] * scale_log2;
+        if (diag) {
+          const int key = j * kBKV + nt * 8 + 2 * tig + (e & 1);
+          const int qrow = q0 + row_w + g + ((e >> 1) << 3);
+          if (key > qrow || key >= T) x = -INFINITY;
+        }
+        s[nt][e] = x;
+      }
+    }
+    // online softmax: rows g (e = 0, 1) and g + 8 (e = 2, 3)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) mx = fmaxf(mx, fmaxf(s[nt][2 * r], s[nt][2 * r + 1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_r[r], mx);
+      const float alpha = exp2_fast(m_r[r] - m_new);  // 0 on the first tile (m = -inf)
+      m_r[r] = m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float p0 = exp2_fast(s[nt][2 * r] - m_new);
+        const float p1 = exp2_fast(s[nt][2 * r + 1] - m_new);
+        s[nt][2 * r] = p0;
+        s[nt][2 * r + 1] = p1;
+        sum += p0 + p1;
+      }
+      l_r[r] = l_r[r] * alpha + sum;
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt) {
+        o[dt][2 * r] *= alpha;
+        o[dt][2 * r + 1] *= alpha;
+      }
+    }
+    // O += P V: P's accumulator layout is the A-operand layout of k-steps
+    const uint32_t vb = smem_u32(v_s[buf]);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
+      pa[1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
+      pa[2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      pa[3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < kDT / 2; ++dp) {
+        const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int c = dp * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + swz<HS>(key, c), b0, b1, b2, b3);
+        mma_bf16(o[2 * dp], pa, b0, b1);
+        mma_bf16(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    __syncthreads();  // this buffer is refilled by the next iteration's prefetch
+  }
+  // normalise and store rows g and g + 8
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float l = l_r[r];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    const float inv = 1.0f / l;
+    const int t = q0 + row_w + g + 8 * r;
+    if (t >= T) continue;
+    const size_t base = (static_cast<size_t>(b) * T + t) * C + h * HS;
+#pragma unroll
+    for (int dt = 0; dt < kDT; ++dt) {
+      const int d = dt * 8 + 2 * tig;
+      const float x0 = o[dt][2 * r] * inv, x1 = o[dt][2 * r + 1] * inv;
+      if constexpr (kOutBF16) {
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out) + base + d) = pack_bf16x2(x0, x1);
+      } else {
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(out) + base + d) = make_float2(x0, x1);
+      }
+    }
+  }
+}
+
+// -------------------------------------------------- fp32 reference kernel
+// One thread per query row, 64 rows per block; key/value tiles of 64 rows
+// in shared memory; exact expf; one key at a time with the running max.
+template <int HS>
+__global__ void __launch_bounds__(64) attn_f32_kernel(float* __restrict__ out, const float* __restrict__ qkv, int T,
+                                                      int C, float scale) {
+  __shared__ float k_s[64][HS];
+  __shared__ float v_s[64][HS];
+  const int qt = gridDim.x - 1 - blockIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int C3 = 3 * C;
+  const int t = qt * 64 + threadIdx.x;
+  const bool active = t < T;
+  float q[HS], o[HS];
+  const float* qrow = qkv + (static_cast<size_t>(b) * T + (active ? t : 0)) * C3 + h * HS;
+#pragma unroll
+  for (int d = 0; d < HS; ++d) {
+    q[d] = qrow[d];
+    o[d] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int j0 = 0; j0 <= qt * 64; j0 += 64) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 64 * HS; i += 64) {
+      const int r = i / HS, d = i % HS;
+      const int key = j0 + r;
+      const size_t base = (static_cast<size_t>(b) * T + (key < T ? key : 0)) * C3 + h * HS + d;
+      k_s[r][d] = key < T ? qkv[base + C] : 0.f;
+      v_s[r][d] = key < T ? qkv[base + 2 * C] : 0.f;
+    }
+    __syncthreads();
+    for (int r = 0; r < 64; ++r) {
+      const int key = j0 + r;
+      if (key > t || key >= T) break;
+      float dot = 0.f;
+#pragma unroll
+      for (int d = 0; d < HS; ++d) dot = fmaf(q[d], k_s[r][d], dot);
+      const float sc = dot * scale;
+      if (sc > m) {
+        const float a = expf(m - sc);  // 0 when m = -inf
+        l = l * a + 1.f;
+#pragma unroll
+        for (int d = 0; d < HS; ++d) o[d] = o[d] * a + v_s[r][d];
+        m = sc;
+      } else {
+        const float p = expf(sc - m);
+        l += p;
+#pragma unroll
+        for (int d = 0; d < HS; ++d) o[d] = fmaf(p, v_s[r][d], o[d]);
+      }
+    }
+  }
+  if (!active) return;
+  const float inv = 1.f / l;
+  float* orow = out + (static_cast<size_t>(b) * T + t) * C + h * HS;
+#pragma unroll
+  for (int d = 0; d < HS; ++d) orow[d] = o[d] * inv;
+}
+
+// ------------------------------------------------------------- decode
+// Phase 1: block (split, h, b) with 4 warps covers 128 cache positions of
+// one (sequence, head); each warp takes 32 of them.  Scores with one lane
+// per position, then the value sum with one lane per pair of dimensions.
+// Each warp leaves (max, sum, o[hs]) in scratch; phase 2 combines them.
+constexpr int kDecPos = 32;   // positions per warp
+constexpr int kDecWarps = 4;  // warps per block
+
+template <typename E, int HS>
+__global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __restrict__ scratch,
+                                                                     const E* __restrict__ qkv,
+                                                                     const E* __restrict__ kcache,
+                                                                     const E* __restrict__ vcache, int B, int C,
+                                                                     int NH, int maxT, int pos, float scale) {
+  __shared__ float q_s[HS];
+  __shared__ float p_s[kDecWarps][kDecPos];
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int d = threadIdx.x; d < HS; d += blockDim.x)
+    q_s[d] = static_cast<float>(qkv[static_cast<size_t>(b) * 3 * C + h * HS + d]);
+  __syncthreads();
+  const int chunk = split * kDecWarps + warp;
+  const int j = chunk * kDecPos + lane;
+  const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
+  float sc = -INFINITY;
+  if (j <= pos) {
+    const E* krow = kcache + (head + j) * HS;
+    float dot = 0.f;
+#pragma unroll
+    for (int d = 0; d < HS; ++d) dot = fmaf(q_s[d], static_cast<float>(krow[d]), dot);
+    sc = dot * scale;
+  }
+  const float mx = warp_max(sc);
+  const float p = (j <= pos) ? __expf(sc - mx) : 0.f;
+  const float sum = warp_sum(p);
+  p_s[warp][lane] = p;
+  __syncwarp();
+  const int nchunks = gridDim.x * kDecWarps;
+  float* part = scratch + ((static_cast<size_t>(b) * NH + h) * nchunks + chunk) * (HS + 2);
+  const int jmax = min(kDecPos, pos + 1 - chunk * kDecPos);  // valid positions in this chunk (may be <= 0)
+  for (int d = lane; d < HS; d += 32) {
+    float acc = 0.f;
+    for (int r = 0; r < jmax; ++r)
+      acc = fmaf(p_s[warp][r], static_cast<float>(vcache[(head + chunk * kDecPos + r) * HS + d]), acc);
+    part[2 + d] = acc;
+  }
+  if (lane == 0) {
+    part[0] = (jmax > 0) ? mx : -INFINITY;
+    part[1] = sum;
+  }
+}
+
+template <typename OutT, int HS>
+__global__ void decode_combine_kernel(OutT* __restrict__ out, const float* __restrict__ scratch, int C, int NH,
+                                      int nchunks) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const float* part = scratch + (static_cast<size_t>(b) * NH + h) * nchunks * (HS + 2);
+  float M = -INFINITY;
+  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, part[c * (HS + 2)]);
+  for (int d = threadIdx.x; d < HS; d += blockDim.x) {
+    float L = 0.f, acc = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+      const float m = part[c * (HS + 2)];
+      if (m == -INFINITY) continue;
+      const float w = __expf(m - M);
+      L += part[c * (HS + 2) + 1] * w;
+      acc += part[c * (HS + 2) + 2 + d] * w;
+    }
+    const float v = acc / L;
+    if constexpr (sizeof(OutT) == 2)
+      out[static_cast<size_t>(b) * C + h * HS + d] = __float2bfloat16_rn(v);
+    else
+      out[static_cast<size_t>(b) * C + h * HS + d] = v;
+  }
+}
+
+}  // namespace
+
+template <int HS>
+static void attention_bf16_hs(void* out, bool out_bf16, const __nv_bfloat16* qkv, int B, int T, int C, int NH,
+                              cudaStream_t s) {
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
+  dim3 grid((T + kBQ - 1) / kBQ, NH, B);
+  if (out_bf16)
+    attn_bf16_kernel<HS, true><<<grid, kAttnThreads, 0, s>>>(out, qkv, T, C, scale_log2);
+  else
+    attn_bf16_kernel<HS, false><<<grid, kAttnThreads, 0, s>>>(out, qkv, T, C, scale_log2);
+}
+
+int launch_attention_bf16(void* out, bool out_bf16, const __nv_bfloat16* qkv, int B, int T, int C, int NH,
+                          cudaStream_t s) {
+  switch (C / NH) {
+    case 16: attention_bf16_hs<16>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
+    case 32: attention_bf16_hs<32>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
+    case 64: attention_bf16_hs<64>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
+  }
+  return GPT2_ERR_UNSUPPORTED;
+}
+
+int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s) {
+  const int hs = C / NH;
+  const float scale = 1.0f / sqrtf(static_cast<float>(hs));
+  dim3 grid((T + 63) / 64, NH, B);
+  switch (hs) {
+    case 16: attn_f32_kernel<16><<<grid, 64, 0, s>>>(out, qkv, T, C, scale); return GPT2_OK;
+    case 32: attn_f32_kernel<32><<<grid, 64, 0, s>>>(out, qkv, T, C, scale); return GPT2_OK;
+    case 64: attn_f32_kernel<64><<<grid, 64, 0, s>>>(out, qkv, T, C, scale); return GPT2_OK;
+  }
+  return GPT2_ERR_UNSUPPORTED;
+}
+
+size_t decode_attention_scratch_floats(int B, int C, int NH, int maxT) {
+  const int hs = C / NH;
+  const int nsplit = (maxT + kDecPos * kDecWarps - 1) / (kDecPos * kDecWarps);
+  return static_cast<size_t>(B) * NH * nsplit * kDecWarps * (hs + 2);
+}
+
+template <typename E, typename OutT, int HS>
+static void decode_typed(OutT* out, const E* qkv, const E* kc, const E* vc, int B, int C, int NH, int maxT, int pos,
+                         float* scratch, cudaStream_t s) {
+  const int nsplit = (pos + 1 + kDecPos * kDecWarps - 1) / (kDecPos * kDecWarps);
+  const float scale = 1.0f / sqrtf(static_cast<float>(HS));
+  decode_attn_kernel<E, HS><<<dim3(nsplit, NH, B), 32 * kDecWarps, 0, s>>>(scratch, qkv, kc, vc, B, C, NH, maxT,
+                                                                           pos, scale);
+  decode_combine_kernel<OutT, HS><<<dim3(NH, B), 64, 0, s>>>(out, scratch, C, NH, nsplit * kDecWarps);
+}
+
+void launch_decode_attention_bf16(void* out, bool out_bf16, const __nv_bfloat16* qkv, const __nv_bfloat16* kcache,
+                                  const __nv_bfloat16* vcache, int B, int C, int NH, int maxT, int pos,
+                                  float* scratch, cudaStream_t s) {
+  using bf = __nv_bfloat16;
+  bf* o16 = reinterpret_cast<bf*>(out);
+  float* o32 = reinterpret_cast<float*>(out);
+  switch (C / NH) {
+    case 16:
+      if (out_bf16) decode_typed<bf, bf, 16>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<bf, float, 16>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      break;
+    case 32:
+      if (out_bf16) decode_typed<bf, bf, 32>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<bf, float, 32>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      break;
+    default:
+      if (out_bf16) decode_typed<bf, bf, 64>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<bf, float, 64>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      break;
+  }
+}
+
+void launch_decode_attention_f32(float* out, const float* qkv, const float* kcache, const float* vcache, int B,
+                                 int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+  switch (C / NH) {
+    case 16: decode_typed<float, float, 16>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
+    case 32: decode_typed<float, float, 32>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
+    default: decode_typed<float, float, 64>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
+  }
+}
+
+}  // namespace gpt2

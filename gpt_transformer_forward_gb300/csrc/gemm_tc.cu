@@ -1,0 +1,412 @@
+// gemm_tc.cu -- the five GEMM sites of the GPT-2 forward pass (QKV, attention
+// projection, MLP up-projection, MLP down-projection, tied LM head) on the
+// sm_103a tensor cores.
+//
+//   D[M, N] = A[M, K] * B[N, K]^T   (A: activations, B: a Linear weight
+//                                     stored [out, in], both K-major)
+//
+// Design (persistent, warp-specialised, one CTA per SM):
+//   warp 0      TMA producer: 128 x 128-byte A and 256 x 128-byte B boxes
+//               (128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns, and one lane issues tcgen05.mma
+//               (128 x 256 x 16 bf16 or 128 x 256 x 8 tf32 per instruction)
+//               into one of two 128 x 256 fp32 TMEM accumulators;
+//   warps 2-5   epilogue: tcgen05.ld 32 columns of their 32 TMEM lanes,
+//               add bias, apply GELU or add the residual (TMA-loaded), stage
+//               the tile in swizzled shared memory and TMA-store it.
+// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
+// i+1.  Tiles are walked M-fastest so that concurrently running CTAs share
+// one weight tile (B) while the activation matrix (A) stays in L2.
+// Every wait is bounded (about one second); on a timeout the CTA records
+// GPT2_DEVERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace gpt2 {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+constexpr int kRowBytes = 128;  // one swizzle atom row: 64 bf16 or 32 fp32 of K
+constexpr int kAStageBytes = kBM * kRowBytes;
+constexpr int kBStageBytes = kBN * kRowBytes;
+constexpr int kEpiWarps = 4;
+constexpr int kStageBufBytes = 32 * 128;  // 32 rows x 128 bytes
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTmemCols = 512;
+
+struct SmemLayout {
+  static constexpr int a_off = 0;
+  static constexpr int b_off = a_off + kStages * kAStageBytes;
+  static constexpr int stg_off = b_off + kStages * kBStageBytes;
+  static constexpr int bar_off = stg_off + kEpiWarps * 2 * kStageBufBytes;
+  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], res[kEpiWarps*2], drain
+  static constexpr int n_bars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
+  static constexpr int misc_off = bar_off + n_bars * 8;
+  static constexpr int total = misc_off + 16;
+  static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
+};
+static_assert(SmemLayout::alloc <= 232448, "shared memory budget");
+
+template <int kEpi, bool kTF32>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
+                   int K, int tiles_m, int num_tiles) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bar_off);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tmem_full = bars + 2 * kStages;
+  uint64_t* tmem_empty = tmem_full + 2;
+  uint64_t* res_bar = tmem_empty + 2;
+  uint64_t* drain_bar = res_bar + 2 * kEpiWarps;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kElemBytes = kTF32 ? 4 : 2;
+  constexpr int kBKElems = kRowBytes / kElemBytes;  // K elements per stage
+  constexpr int kMmaK = 32 / kElemBytes;            // K per instruction (32 bytes)
+  constexpr uint32_t kIdesc = make_idesc(kTF32 ? 2u : 1u, kBM, kBN);
+  const int num_kb = (K + kBKElems - 1) / kBKElems;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], kEpiWarps);
+    }
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&res_bar[i], 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_a);
+    tma_prefetch_desc(&tmap_b);
+    tma_prefetch_desc(&tmap_out);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_a = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled, parity of its last fill
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+        const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kAStageBytes + kBStageBytes);
+          tma_load_2d_hint(smem + SmemLayout::a_off + stage * kAStageBytes, &tmap_a, &full[stage], kb * kBKElems,
+                           m_blk * kBM, pol_a);
+          tma_load_2d(smem + SmemLayout::b_off + stage * kBStageBytes, &tmap_b, &full[stage], kb * kBKElems,
+                      n_blk * kBN);
+          filled |= 1u << stage;
+          fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+      // Only this thread arms the full barriers, so the phase of a stage's
+      // last fill completes exactly when its bytes have landed: wait for
+      // every such phase before the CTA may exit (immediate when the MMA
+      // warp has consumed them, which is the normal case).
+      for (int s = 0; s < kStages; ++s)
+        if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + SmemLayout::a_off + stage * kAStageBytes);
+          const uint32_t b_addr = smem_u32(smem + SmemLayout::b_off + stage * kBStageBytes);
+#pragma unroll
+          for (int k = 0; k < kBKElems / kMmaK; ++k) {
+            tc_mma<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                          (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);  // frees the smem slot once these MMAs have read it
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_commit(&tmem_full[acc]);  // accumulator ready for the epilogue
+      }
+      // every MMA issued above has completed once this commit arrives
+      tc_commit(drain_bar);
+      mbar_wait(drain_bar, 0);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int ew = warp - 2;            // epilogue warp index 0..3
+    const int quad = warp & 3;          // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32;  // tile rows [row_in_tile, row_in_tile + 32)
+    uint8_t* stg0 = smem + SmemLayout::stg_off + ew * 2 * kStageBufBytes;
+    uint32_t res_phase = 0;  // bit b: parity of the next residual load into buffer b
+    uint32_t chunk_ctr = 0;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+      const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      // every lane waits; the outcome is made warp-uniform so that the
+      // .sync.aligned tcgen05 instructions below never run divergent
+      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase))) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int m0 = m_blk * kBM + row_in_tile;
+      const int n0 = n_blk * kBN;
+      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
+      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32);
+      constexpr int kChunkCols = kOutF32 ? 32 : 64;  // 128 bytes of output per row
+      bool ok = true;
+#pragma unroll 1
+      for (int ch = 0; ch < kBN / kChunkCols; ++ch) {
+        const int buf = chunk_ctr & 1;
+        uint8_t* stg = stg0 + buf * kStageBufBytes;
+        const int col0 = n0 + ch * kChunkCols;
+        if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done
+        __syncwarp();
+        if constexpr (kEpi == kEpiResidF32) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&res_bar[ew * 2 + buf], kStageBufBytes);
+            tma_load_2d(stg, &tmap_out, &res_bar[ew * 2 + buf], col0, m0);
+          }
+        }
+        float v[kChunkCols];
+        {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_base + ch * kChunkCols, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+          if constexpr (kChunkCols == 64) {
+            tmem_ld_32x32b_x32(t_base + ch * kChunkCols + 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[32 + j] = __uint_as_float(r[j]);
+          }
+        }
+        if (bias != nullptr) {
+          if (col0 + kChunkCols <= N) {
+            const float4* b4 = reinterpret_cast<const float4*>(bias + col0);
+#pragma unroll
+            for (int j = 0; j < kChunkCols / 4; ++j) {
+              const float4 bb = __ldg(b4 + j);
+              v[4 * j] += bb.x;
+              v[4 * j + 1] += bb.y;
+              v[4 * j + 2] += bb.z;
+              v[4 * j + 3] += bb.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kChunkCols; ++j)
+              if (col0 + j < N) v[j] += __ldg(bias + col0 + j);
+          }
+        }
+        const int sw = lane & 7;
+        uint8_t* my_row = stg + lane * 128;
+        if constexpr (kOutF32) {
+          if constexpr (kEpi == kEpiResidF32) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&res_bar[ew * 2 + buf], (res_phase >> buf) & 1u));
+            res_phase ^= 1u << buf;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 old = *reinterpret_cast<const float4*>(my_row + ((j ^ sw) << 4));
+              v[4 * j] += old.x;
+              v[4 * j + 1] += old.y;
+              v[4 * j + 2] += old.z;
+              v[4 * j + 3] += old.w;
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(my_row + ((j ^ sw) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float a[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              a[e] = v[8 * j + e];
+              if constexpr (kEpi == kEpiGeluBF16) a[e] = gelu_fast(a[e]);
+            }
+            uint4 p;
+            p.x = pack_bf16x2(a[0], a[1]);
+            p.y = pack_bf16x2(a[2], a[3]);
+            p.z = pack_bf16x2(a[4], a[5]);
+            p.w = pack_bf16x2(a[6], a[7]);
+            *reinterpret_cast<uint4*>(my_row + ((j ^ sw) << 4)) = p;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmap_out, stg, col0, m0);
+          bulk_commit_group();
+        }
+        ++chunk_ctr;
+        if (!ok) break;
+      }
+      // this warp is done reading the accumulator
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major [rows, cols] matrix with a box of
+// box_cols x box_rows and the 128-byte swizzle (box_cols * elem = 128).
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int rows, int cols,
+              int box_cols, int box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int kEpi, bool kTF32>
+int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s) {
+  CUtensorMap ta, tb, to;
+  const CUtensorMapDataType dt_in = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int eb = kTF32 ? 4 : 2;
+  const int bk = kRowBytes / eb;
+  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32);
+  if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
+  if (!make_map(&tb, B, dt_in, eb, N, K, bk, kBN)) return GPT2_ERR_CUDA;
+  if (kOutF32) {
+    if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 32, 32)) return GPT2_ERR_CUDA;
+  } else {
+    if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, 64, 32)) return GPT2_ERR_CUDA;
+  }
+  const int tiles_m = (M + kBM - 1) / kBM;
+  const int tiles_n = (N + kBN - 1) / kBN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int grid = num_tiles < num_sms() ? num_tiles : num_sms();
+  auto kern = gemm_tc_kernel<kEpi, kTF32>;
+  static bool attr_set[kMaxDevices] = {};  // per template instance and device
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc) != cudaSuccess)
+      return GPT2_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  kern<<<grid, kThreads, SmemLayout::alloc, s>>>(ta, tb, to, bias, M, N, K, tiles_m, num_tiles);
+  return cudaPeekAtLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi,
+                   bool ab_bf16, cudaStream_t s) {
+  if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
+  if (ab_bf16) {
+    switch (epi) {
+      case kEpiF32: return launch_typed<kEpiF32, false>(out, A, B, bias, M, N, K, s);
+      case kEpiBF16: return launch_typed<kEpiBF16, false>(out, A, B, bias, M, N, K, s);
+      case kEpiGeluBF16: return launch_typed<kEpiGeluBF16, false>(out, A, B, bias, M, N, K, s);
+      case kEpiResidF32: return launch_typed<kEpiResidF32, false>(out, A, B, bias, M, N, K, s);
+    }
+  } else {
+    switch (epi) {
+      case kEpiF32: return launch_typed<kEpiF32, true>(out, A, B, bias, M, N, K, s);
+      case kEpiResidF32: return launch_typed<kEpiResidF32, true>(out, A, B, bias, M, N, K, s);
+    }
+  }
+  return GPT2_ERR_UNSUPPORTED;
+}
+
+}  // namespace gpt2

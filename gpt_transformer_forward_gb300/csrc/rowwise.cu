@@ -1,0 +1,419 @@
+// rowwise.cu -- the HBM-bound steps of the GPT-2 forward pass: encoder,
+// LayerNorm, GELU, residual add, vocabulary softmax, argmax, plus the fp32
+// to bf16 conversions and the KV-cache writes the forward pass needs.
+//
+// Every kernel streams its rows with 128-bit loads and stores where the
+// layout allows; row reductions are warp-shuffle (LayerNorm: one warp per
+// row, the row held in registers) or block-wide (softmax: one block per
+// row).
+#include "kernels.cuh"
+
+namespace gpt2 {
+
+__device__ unsigned int g_error_word = 0;
+
+// ---------------------------------------------------------------- encoder
+// out[n, :] = wte[tok[n], :] + wpe[n % T, :], one float4 per thread.
+__global__ void encoder_kernel(float4* __restrict__ out, const int* __restrict__ tok,
+                               const float4* __restrict__ wte, const float4* __restrict__ wpe, int N, int T,
+                               int C4, int V) {
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<long long>(N) * C4) return;
+  const int n = static_cast<int>(idx / C4);
+  const int c = static_cast<int>(idx % C4);
+  int ix = __ldg(tok + n);
+  if (ix < 0 || ix >= V) {
+    if (c == 0) set_error(GPT2_DEVERR_TOKEN);
+    ix = 0;
+  }
+  const int t = n % T;
+  const float4 a = __ldg(wte + static_cast<size_t>(ix) * C4 + c);
+  const float4 b = __ldg(wpe + static_cast<size_t>(t) * C4 + c);
+  out[idx] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+// Decode-step encoder: row b is token tok[b] at position pos.
+__global__ void encoder_pos_kernel(float4* __restrict__ out, const int* __restrict__ tok,
+                                   const float4* __restrict__ wte, const float4* __restrict__ wpe, int B, int pos,
+                                   int C4, int V) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= B * C4) return;
+  const int b = idx / C4, c = idx % C4;
+  int ix = __ldg(tok + b);
+  if (ix < 0 || ix >= V) {
+    if (c == 0) set_error(GPT2_DEVERR_TOKEN);
+    ix = 0;
+  }
+  const float4 a = __ldg(wte + static_cast<size_t>(ix) * C4 + c);
+  const float4 p = __ldg(wpe + static_cast<size_t>(pos) * C4 + c);
+  out[idx] = make_float4(a.x + p.x, a.y + p.y, a.z + p.z, a.w + p.w);
+}
+
+void launch_encoder(float* out, const int* tok, const float* wte, const float* wpe, int N, int T, int C, int V,
+                    cudaStream_t s) {
+  const int C4 = C / 4;
+  const long long total = static_cast<long long>(N) * C4;
+  const int threads = 256;
+  const unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
+  encoder_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<float4*>(out), tok,
+                                            reinterpret_cast<const float4*>(wte),
+                                            reinterpret_cast<const float4*>(wpe), N, T, C4, V);
+}
+
+void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos, int C, int V,
+                        cudaStream_t s) {
+  const int C4 = C / 4;
+  const int threads = 256;
+  encoder_pos_kernel<<<(B * C4 + threads - 1) / threads, threads, 0, s>>>(
+      reinterpret_cast<float4*>(out), tok, reinterpret_cast<const float4*>(wte),
+      reinterpret_cast<const float4*>(wpe), B, pos, C4, V);
+}
+
+// -------------------------------------------------------------- LayerNorm
+// One warp per row; the row's C = 128 * kVec floats sit in registers (kVec
+// float4 per lane), so the mean and the variance of the centred values are
+// two register passes over a single read.  Output fp32 or bf16.
+template <int kVec, typename OutT>
+__global__ void __launch_bounds__(256) layernorm_warp_kernel(OutT* __restrict__ out, float* __restrict__ mean_out,
+                                                             float* __restrict__ rstd_out,
+                                                             const float* __restrict__ inp,
+                                                             const float* __restrict__ w,
+                                                             const float* __restrict__ b, int N) {
+  constexpr int C = 128 * kVec;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= N) return;
+  const float4* x4 = reinterpret_cast<const float4*>(inp + static_cast<size_t>(row) * C);
+  float4 v[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) v[i] = __ldcs(x4 + lane + 32 * i);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  const float mean = warp_sum(s) * (1.0f / C);
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float dx = v[i].x - mean, dy = v[i].y - mean, dz = v[i].z - mean, dw = v[i].w - mean;
+    q += (dx * dx + dy * dy) + (dz * dz + dw * dw);
+  }
+  const float var = warp_sum(q) * (1.0f / C);
+  const float rstd = rsqrtf(var + 1e-5f);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  const float4* b4 = reinterpret_cast<const float4*>(b);
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const int c4 = lane + 32 * i;
+    const float4 ww = __ldg(w4 + c4), bb = __ldg(b4 + c4);
+    const float y0 = (v[i].x - mean) * rstd * ww.x + bb.x;
+    const float y1 = (v[i].y - mean) * rstd * ww.y + bb.y;
+    const float y2 = (v[i].z - mean) * rstd * ww.z + bb.z;
+    const float y3 = (v[i].w - mean) * rstd * ww.w + bb.w;
+    if constexpr (sizeof(OutT) == 4) {
+      reinterpret_cast<float4*>(out + static_cast<size_t>(row) * C)[c4] = make_float4(y0, y1, y2, y3);
+    } else {
+      uint2 p;
+      p.x = pack_bf16x2(y0, y1);
+      p.y = pack_bf16x2(y2, y3);
+      reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * C)[c4] = p;
+    }
+  }
+  if (lane == 0) {
+    if (mean_out) mean_out[row] = mean;
+    if (rstd_out) rstd_out[row] = rstd;
+  }
+}
+
+// Any C with C % 4 == 0: one block per row, three passes over the row
+// (sum, centred sum of squares, output); the re-reads hit L1/L2.
+template <typename OutT>
+__global__ void __launch_bounds__(256) layernorm_block_kernel(OutT* __restrict__ out, float* __restrict__ mean_out,
+                                                              float* __restrict__ rstd_out,
+                                                              const float* __restrict__ inp,
+                                                              const float* __restrict__ w,
+                                                              const float* __restrict__ b, int C) {
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const float* x = inp + static_cast<size_t>(row) * C;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  auto block_sum = [&](float v) {
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[wid] = v;
+    __syncthreads();
+    float t = (lane < nw) ? red[lane] : 0.f;
+    return warp_sum(t);
+  };
+  float s = 0.f;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) s += x[c];
+  const float mean = block_sum(s) / C;
+  float q = 0.f;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const float d = x[c] - mean;
+    q += d * d;
+  }
+  const float rstd = rsqrtf(block_sum(q) / C + 1e-5f);
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const float y = (x[c] - mean) * rstd * w[c] + b[c];
+    if constexpr (sizeof(OutT) == 4)
+      out[static_cast<size_t>(row) * C + c] = y;
+    else
+      out[static_cast<size_t>(row) * C + c] = __float2bfloat16_rn(y);
+  }
+  if (threadIdx.x == 0) {
+    if (mean_out) mean_out[row] = mean;
+    if (rstd_out) rstd_out[row] = rstd;
+  }
+}
+
+template <typename OutT>
+static void layernorm_dispatch(OutT* out, float* mean, float* rstd, const float* inp, const float* w, const float* b,
+                               int N, int C, cudaStream_t s) {
+  const int rows_per_block = 8;
+  const unsigned grid = static_cast<unsigned>((N + rows_per_block - 1) / rows_per_block);
+  switch (C) {
+    case 256: layernorm_warp_kernel<2, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 512: layernorm_warp_kernel<4, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 768: layernorm_warp_kernel<6, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 1024: layernorm_warp_kernel<8, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 1280: layernorm_warp_kernel<10, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 1536: layernorm_warp_kernel<12, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    default: layernorm_block_kernel<OutT><<<N, 256, 0, s>>>(out, mean, rstd, inp, w, b, C); return;
+  }
+}
+
+void launch_layernorm_f32(float* out, float* mean, float* rstd, const float* inp, const float* w, const float* b,
+                          int N, int C, cudaStream_t s) {
+  layernorm_dispatch<float>(out, mean, rstd, inp, w, b, N, C, s);
+}
+
+void launch_layernorm_bf16(__nv_bfloat16* out, const float* inp, const float* w, const float* b, int N, int C,
+                           cudaStream_t s) {
+  layernorm_dispatch<__nv_bfloat16>(out, nullptr, nullptr, inp, w, b, N, C, s);
+}
+
+// ------------------------------------------------------- GELU and residual
+__global__ void gelu_kernel(float4* __restrict__ out, const float4* __restrict__ inp, long long n4) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 x = inp[i];
+    out[i] = make_float4(gelu_exact(x.x), gelu_exact(x.y), gelu_exact(x.z), gelu_exact(x.w));
+  }
+}
+
+__global__ void gelu_tail_kernel(float* __restrict__ out, const float* __restrict__ inp, int start, int n) {
+  const int i = start + blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = gelu_exact(inp[i]);
+}
+
+__global__ void residual_kernel(float4* out, const float4* a, const float4* b, long long n4) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 x = a[i], y = b[i];
+    out[i] = make_float4(x.x + y.x, x.y + y.y, x.z + y.z, x.w + y.w);
+  }
+}
+
+__global__ void residual_tail_kernel(float* out, const float* a, const float* b, int start, int n) {
+  const int i = start + blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = a[i] + b[i];
+}
+
+static unsigned stream_grid(long long n4, int threads) {
+  int sms = num_sms();
+  long long want = (n4 + threads - 1) / threads;
+  long long cap = static_cast<long long>(sms) * 8;
+  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+void launch_gelu(float* out, const float* inp, int n, cudaStream_t s) {
+  const long long n4 = n / 4;
+  if (n4 > 0) gelu_kernel<<<stream_grid(n4, 256), 256, 0, s>>>(reinterpret_cast<float4*>(out),
+                                                                reinterpret_cast<const float4*>(inp), n4);
+  const int rem = n - static_cast<int>(n4 * 4);
+  if (rem > 0) gelu_tail_kernel<<<1, 32, 0, s>>>(out, inp, static_cast<int>(n4 * 4), n);
+}
+
+void launch_residual(float* out, const float* a, const float* b, int n, cudaStream_t s) {
+  const long long n4 = n / 4;
+  if (n4 > 0)
+    residual_kernel<<<stream_grid(n4, 256), 256, 0, s>>>(reinterpret_cast<float4*>(out),
+                                                          reinterpret_cast<const float4*>(a),
+                                                          reinterpret_cast<const float4*>(b), n4);
+  const int rem = n - static_cast<int>(n4 * 4);
+  if (rem > 0) residual_tail_kernel<<<1, 32, 0, s>>>(out, a, b, static_cast<int>(n4 * 4), n);
+}
+
+// ---------------------------------------------------------------- softmax
+constexpr int kSoftmaxThreads = 1024;
+
+// One block per row: an online max/sum pass over the row, then the
+// normalised write pass.
+__global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float* __restrict__ probs,
+                                                                        const float* __restrict__ logits, int V,
+                                                                        int Vp) {
+  __shared__ float red_m[32], red_s[32];
+  __shared__ float bm, bs;
+  const size_t row = blockIdx.x;
+  const float* lrow = logits + row * Vp;
+  float* prow = probs + row * Vp;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  float m = -INFINITY, s = 0.f;
+  for (int c = tid; c < V; c += blockDim.x) {
+    const float x = lrow[c];
+    if (x > m) {
+      s = s * __expf(m - x) + 1.f;
+      m = x;
+    } else {
+      s += __expf(x - m);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    const float mm = fmaxf(m, m2);
+    s = (mm == -INFINITY) ? 0.f : s * __expf(m - mm) + s2 * __expf(m2 - mm);
+    m = mm;
+  }
+  if (lane == 0) {
+    red_m[wid] = m;
+    red_s[wid] = s;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    m = red_m[lane];
+    s = red_s[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      const float mm = fmaxf(m, m2);
+      s = (mm == -INFINITY) ? 0.f : s * __expf(m - mm) + s2 * __expf(m2 - mm);
+      m = mm;
+    }
+    if (lane == 0) {
+      bm = m;
+      bs = s;
+    }
+  }
+  __syncthreads();
+  const float mx = bm, inv = 1.0f / bs;
+  for (int c = tid; c < Vp; c += blockDim.x) prow[c] = (c < V) ? __expf(lrow[c] - mx) * inv : 0.f;
+}
+
+void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s) {
+  // The second pass re-reads a row the same block has just read; with one
+  // row per block the rows in flight (a few MB) stay in L2, so HBM sees one
+  // read and one write per element.
+  softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(probs, logits, V, Vp);
+}
+
+// ----------------------------------------------------------------- argmax
+// One block per row; ties go to the smallest index.
+__global__ void __launch_bounds__(512) argmax_kernel(int* __restrict__ next, const float* __restrict__ logits, int V,
+                                                     int Vp) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float* row = logits + static_cast<size_t>(blockIdx.x) * Vp;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int c = threadIdx.x; c < V; c += blockDim.x) {
+    const float x = row[c];
+    if (x > best) {  // strictly greater: within a thread indices increase
+      best = x;
+      bi = c;
+    }
+  }
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+    const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (b2 > best || (b2 == best && i2 < bi)) {
+      best = b2;
+      bi = i2;
+    }
+  }
+  if (lane == 0) {
+    sv[wid] = best;
+    si[wid] = bi;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    best = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float b2 = __shfl_xor_sync(0xffffffffu, best, o);
+      const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (b2 > best || (b2 == best && i2 < bi)) {
+        best = b2;
+        bi = i2;
+      }
+    }
+    if (lane == 0) next[blockIdx.x] = (bi == 0x7fffffff) ? 0 : bi;
+  }
+}
+
+void launch_argmax(int* next, const float* logits, int B, int V, int Vp, cudaStream_t s) {
+  argmax_kernel<<<B, 512, 0, s>>>(next, logits, V, Vp);
+}
+
+// ------------------------------------------------------------ conversions
+__global__ void f32_to_bf16_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ in, long long n) {
+  const long long n4 = n / 4;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float4 x = reinterpret_cast<const float4*>(in)[i];
+    uint2 p;
+    p.x = pack_bf16x2(x.x, x.y);
+    p.y = pack_bf16x2(x.z, x.w);
+    reinterpret_cast<uint2*>(out)[i] = p;
+  }
+  const long long i = n4 * 4 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (blockIdx.x == 0 && i < n) out[i] = __float2bfloat16_rn(in[i]);
+}
+
+void launch_f32_to_bf16(__nv_bfloat16* out, const float* in, long long n, cudaStream_t s) {
+  f32_to_bf16_kernel<<<stream_grid(n / 4 + 1, 256), 256, 0, s>>>(out, in, n);
+}
+
+// ----------------------------------------------------------- KV cache
+// Copies keys and values of rows [0, T) of each sequence from the QKV buffer
+// ([B*T, 3C], element type T_) into a layer's cache slab
+// [2][B][NH][maxT][hs] at positions [pos0, pos0 + T).  One thread per 16
+// bytes of a head row.
+template <typename E>
+__global__ void kv_store_kernel(E* __restrict__ cache, const E* __restrict__ qkv, int B, int T, int C, int NH,
+                                int maxT, int pos0) {
+  constexpr int kPer = 16 / sizeof(E);
+  const int hs = C / NH;
+  const int chunks = hs / kPer;
+  const long long total = 2LL * B * T * NH * chunks;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    long long r = i;
+    const int ch = static_cast<int>(r % chunks); r /= chunks;
+    const int h = static_cast<int>(r % NH); r /= NH;
+    const int t = static_cast<int>(r % T); r /= T;
+    const int b = static_cast<int>(r % B); r /= B;
+    const int kv = static_cast<int>(r);  // 0 = keys, 1 = values
+    const E* src = qkv + (static_cast<size_t>(b) * T + t) * 3 * C + (kv + 1) * C + h * hs + ch * kPer;
+    E* dst = cache + ((((static_cast<size_t>(kv) * B + b) * NH + h) * maxT) + pos0 + t) * hs + ch * kPer;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  }
+}
+
+void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, int NH, int maxT, int pos0,
+                         cudaStream_t s) {
+  const long long total = 2LL * B * T * C / 4;
+  kv_store_kernel<float><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
+}
+
+void launch_kv_store_bf16(__nv_bfloat16* cache, const __nv_bfloat16* qkv, int B, int T, int C, int NH, int maxT,
+                          int pos0, cudaStream_t s) {
+  const long long total = 2LL * B * T * C / 8;
+  kv_store_kernel<__nv_bfloat16><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
+}
+
+}  // namespace gpt2

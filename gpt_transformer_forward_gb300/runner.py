@@ -1,0 +1,63 @@
+"""Device buffers around the C ABI: a GPT-2 model ready to run forward passes
+and decode steps on one GPU.
+
+PyTorch only provides device memory and the stream here; every kernel that
+touches the data is the CUDA library's, reached through `binding`.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as ab
+
+
+class GPT2Model:
+    """Parameters (fp32, plus the packed bf16 weights in GPT2_BF16 mode) and a
+    workspace sized for batches of up to B sequences of up to T tokens."""
+
+    def __init__(self, cfg, params, B: int, T: int, precision: int = ab.GPT2_BF16, device="cuda"):
+        ab.load()
+        self.cfg = cfg
+        self.precision = precision
+        self.device = torch.device(device)
+        p = torch.as_tensor(params)
+        n = ab.gpt2_num_parameters(cfg)
+        if p.numel() != n:
+            raise ValueError(f"parameter buffer has {p.numel()} values, the config needs {n}")
+        self.params = p.to(self.device, dtype=torch.float32).contiguous()
+        nbytes = ab.gpt2_packed_weights_size(cfg, precision)
+        self.packed = torch.empty(nbytes, dtype=torch.uint8, device=self.device) if nbytes else None
+        if self.packed is not None:
+            ab.gpt2_prepare_weights(cfg, self.params, self.packed, nbytes, precision)
+        self.B, self.T = B, T
+        self.ws_bytes = max(ab.gpt2_workspace_size(cfg, B, T, precision),
+                            ab.gpt2_workspace_size(cfg, B, 1, precision))
+        self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
+
+    # ---------------------------------------------------------------- buffers
+    def new_outputs(self, B: int, T: int, probs: bool = True):
+        Vp = self.cfg.padded_vocab_size
+        shape = (B, T, Vp) if T is not None else (B, Vp)
+        logits = torch.empty(shape, dtype=torch.float32, device=self.device)
+        pr = torch.empty(shape, dtype=torch.float32, device=self.device) if probs else None
+        return logits, pr
+
+    def new_kvcache(self, B: int):
+        nbytes = ab.gpt2_kvcache_size(self.cfg, B, self.precision)
+        return torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+
+    # ----------------------------------------------------------------- calls
+    def forward(self, tok, logits, probs=None, kvcache=None, stream=None):
+        B, T = tok.shape
+        ab.gpt2_forward(self.cfg, self.params, self.packed, tok, B, T, logits, probs, kvcache, self.workspace,
+                        self.ws_bytes, self.precision, stream)
+
+    def forward_profile(self, tok, logits, probs=None, stream=None) -> dict:
+        B, T = tok.shape
+        return ab.gpt2_forward_profile(self.cfg, self.params, self.packed, tok, B, T, logits, probs,
+                                       self.workspace, self.ws_bytes, self.precision, stream)
+
+    def decode_step(self, kvcache, tok, pos: int, logits, probs=None, stream=None):
+        B = tok.shape[0]
+        ab.gpt2_decode_step(self.cfg, self.params, self.packed, kvcache, tok, B, pos, logits, probs,
+                            self.workspace, self.ws_bytes, self.precision, stream)

@@ -1,0 +1,253 @@
+/*
+ * gpt2fwd.h -- C ABI of the GPT-2 forward-pass library for one NVIDIA GB300
+ * (sm_103a).  Library file: libgpt2fwd.so.
+ *
+ * Sources of the operations (web pages the method is taken from):
+ *   [ECE408]  "ECE408 Final Project - GPT-2", Milestone 1 README: section
+ *             "Milestone Requirements" (host functions `xxxx_forward()` only
+ *             launch kernels; the caller allocates and copies memory; their
+ *             signatures are fixed, the kernels are free) and the grade table
+ *             of "Code Submission and Grading" (the forward-pass kernels:
+ *             Attention including Softmax, Encoder, LayerNorm, MatMul,
+ *             Residual, GELU).
+ *   [llm.c]   "State of the Union [April 22, 2024]" (llm.c discussion #224):
+ *             the per-kernel table naming the forward kernels
+ *             (encoder_forward, layernorm_forward, the attention softmax,
+ *             gelu_forward, residual_forward, the classifier) and the GEMMs.
+ *   [NTU]     NTU optdl2025 project list: "Understanding and Improving GPT-2
+ *             Implementations in NanoGPT" (fused QKV projection, heads split
+ *             as column blocks, KV caching for autoregressive prediction) and
+ *             "Understand FlashAttention (I)" (Algorithms 0 and 1: exact
+ *             attention with a tiled online softmax).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     the argument says "host".  No call allocates, frees or copies memory
+ *     between host and device.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on it and return without synchronising.
+ *   - Floating-point tensors are IEEE fp32, row-major, unless a precision
+ *     mode below says otherwise for an internal buffer.
+ *   - Return value: GPT2_OK (0) or a negative GPT2_ERR_* code.  Arguments are
+ *     checked on the host before anything is enqueued; on error nothing is
+ *     enqueued.  Faults found on the device (a token id outside [0, V), a
+ *     pipeline wait that gave up) never trap: they set a device error word
+ *     read by gpt2_get_error().
+ *   - Pointers must be 16-byte aligned (128-bit vector accesses).
+ */
+#ifndef GPT2FWD_H
+#define GPT2FWD_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define GPT2_API __attribute__((visibility("default")))
+#else
+#define GPT2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Model hyper-parameters (GPT-2 names maxT, V, Vp, L, NH, C). */
+typedef struct {
+  int max_seq_len;       /* maxT: longest sequence, size of the position table */
+  int vocab_size;        /* V: number of real tokens */
+  int padded_vocab_size; /* Vp >= V: rows of the token embedding and logits columns */
+  int num_layers;        /* L */
+  int num_heads;         /* NH; head size hs = C / NH */
+  int channels;          /* C */
+} GPT2Config;
+
+/* Operand precision of the matrix products (GEMMs and attention).
+ *   GPT2_FP32: fp32 CUDA-core arithmetic throughout (reference-grade mode).
+ *   GPT2_TF32: tensor cores (tcgen05 kind::tf32) on fp32 operands.
+ *   GPT2_BF16: tensor cores (tcgen05 kind::f16) on bf16 operands; operand
+ *              buffers internal to gpt2_forward are stored as bf16 (the
+ *              tensor cores would round them to bf16 anyway); the residual
+ *              stream, logits and probabilities stay fp32.
+ * Accumulation is fp32 in every mode. */
+typedef enum { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2 } GPT2Precision;
+
+enum {
+  GPT2_OK = 0,
+  GPT2_ERR_ARG = -1,       /* null pointer or nonsensical argument */
+  GPT2_ERR_SHAPE = -2,     /* T > maxT, C % NH, pos >= maxT, unsupported shape */
+  GPT2_ERR_ALIGN = -3,     /* pointer not 16-byte aligned */
+  GPT2_ERR_WORKSPACE = -4, /* workspace or buffer too small */
+  GPT2_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed */
+  GPT2_ERR_DEVICE = -6,    /* device-detected fault (see gpt2_get_error) */
+  GPT2_ERR_UNSUPPORTED = -7
+};
+
+/* Device error word bits returned by gpt2_get_error (as -GPT2_ERR_DEVICE
+ * combined into a positive bit set, see below). */
+#define GPT2_DEVERR_TOKEN_BIT 1    /* token id outside [0, V); the read was clamped */
+#define GPT2_DEVERR_TIMEOUT_BIT 2  /* a pipeline wait gave up after ~1 s */
+#define GPT2_DEVERR_POSITION_BIT 4 /* a decode position outside [0, maxT) */
+
+/* ----------------------------------------------------------- single steps */
+
+/* Encoder [ECE408 grade table "Encoder"; llm.c table encoder_forward]:
+ *   out[b,t,c] = wte[tok[b,t], c] + wpe[t, c]
+ * out [B,T,C] fp32, tok [B,T] int32, wte [V',C] (any V' >= V rows), wpe
+ * [>=T, C].  A token outside [0, V) is clamped to 0 for the read and flags
+ * GPT2_DEVERR_TOKEN_BIT.  Requires C % 4 == 0. */
+GPT2_API int encoder_forward(float* out, const int* tok, const float* wte, const float* wpe, int B, int T, int C, int V,
+                    void* stream);
+
+/* LayerNorm [ECE408 "LayerNorm"; llm.c layernorm_forward]: per row of C
+ *   mean = sum x / C, var = sum (x - mean)^2 / C, rstd = 1/sqrt(var + 1e-5),
+ *   out = (x - mean) * rstd * w + b.
+ * out, inp [N,C]; w, b [C]; mean and rstd [N] are written when non-null.
+ * Requires C % 4 == 0.  out may alias inp. */
+GPT2_API int layernorm_forward(float* out, float* mean, float* rstd, const float* inp, const float* w, const float* b, int N,
+                      int C, void* stream);
+
+/* Scratch bytes matmul_forward needs for this shape and precision (0 for
+ * GPT2_FP32 and GPT2_TF32; the bf16 copies of inp and W for GPT2_BF16). */
+GPT2_API size_t matmul_workspace_size(int N, int C, int OC, int precision);
+
+/* MatMul with bias [ECE408 "MatMul"; llm.c GEMMs]:
+ *   out[n, o] = sum_k inp[n, k] * W[o, k] + bias[o]     (bias may be NULL)
+ * out [N,OC], inp [N,C], W [OC,C] (PyTorch Linear layout), bias [OC].
+ * Tensor-core modes need C % 8 == 0 and OC % 4 == 0.  `workspace` of
+ * matmul_workspace_size() bytes is caller-owned scratch (may be NULL when
+ * that size is 0).  out must not alias inp or W. */
+GPT2_API int matmul_forward(float* out, const float* inp, const float* W, const float* bias, int N, int C, int OC,
+                   int precision, void* workspace, size_t ws_bytes, void* stream);
+
+/* Scratch bytes attention_forward needs (the bf16 copy of qkv in GPT2_BF16
+ * and GPT2_TF32 modes, 0 in GPT2_FP32). */
+GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
+
+/* Causal multi-head attention including its softmax [ECE408 "Attention
+ * (including Softmax)"; NTU NanoGPT head splitting; FlashAttention
+ * Algorithm 0 defines the result, Algorithm 1's online softmax computes it]:
+ *   q, k, v = columns [0,C), [C,2C), [2C,3C) of qkv; head h owns columns
+ *   [h*hs, (h+1)*hs) of each; S = q k^T / sqrt(hs) with keys j <= t only;
+ *   out[b,t, h*hs:(h+1)*hs] = softmax_j(S[t, :]) v.
+ * out [B,T,C], qkv [B,T,3C].  Requires hs in {16, 32, 64}.  GPT2_FP32
+ * runs fp32 CUDA-core arithmetic; GPT2_TF32 and GPT2_BF16 both run the bf16
+ * tensor-core kernel (Q, K, V and the probabilities rounded to bf16, fp32
+ * accumulation) on a bf16 copy of qkv made in `workspace`. */
+GPT2_API int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH, int precision, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/* tanh-GELU [ECE408 "GELU"; llm.c gelu_forward]:
+ *   out = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), n elements. */
+GPT2_API int gelu_forward(float* out, const float* inp, int n, void* stream);
+
+/* Residual [ECE408 "Residual"; llm.c residual_forward]: out = a + b, n
+ * elements; out may alias a or b. */
+GPT2_API int residual_forward(float* out, const float* a, const float* b, int n, void* stream);
+
+/* Softmax over the vocabulary [llm.c classifier; the final logits softmax]:
+ *   probs[n, v] = exp(l[n,v] - max_u l[n,u]) / sum_{u<V} exp(l[n,u] - max)
+ * for v < V, and probs[n, v] = 0 for V <= v < Vp.  logits, probs [N,Vp];
+ * requires Vp % 4 == 0.  probs must not alias logits. */
+GPT2_API int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, void* stream);
+
+/* Greedy next token: next[b] = the smallest v < V with the largest
+ * logits[b, v].  next [B] int32, logits [B,Vp]. */
+GPT2_API int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, void* stream);
+
+/* ------------------------------------------------------ the forward pass */
+
+/* Number of fp32 values in the flat parameter buffer.  Tensor order, each
+ * row-major: wte[Vp,C] wpe[maxT,C] ln1w[L,C] ln1b[L,C] qkvw[L,3C,C]
+ * qkvb[L,3C] attprojw[L,C,C] attprojb[L,C] ln2w[L,C] ln2b[L,C] fcw[L,4C,C]
+ * fcb[L,4C] fcprojw[L,C,4C] fcprojb[L,C] lnfw[C] lnfb[C]. */
+GPT2_API size_t gpt2_num_parameters(const GPT2Config* cfg);
+
+/* Bytes of the packed weight buffer for a precision: bf16 copies of the
+ * matrices (wte, qkvw, attprojw, fcw, fcprojw) for GPT2_BF16, 0 otherwise. */
+GPT2_API size_t gpt2_packed_weights_size(const GPT2Config* cfg, int precision);
+
+/* Fills `packed` (caller-owned, gpt2_packed_weights_size bytes) from the
+ * fp32 parameters.  Run once per set of weights; gpt2_forward and
+ * gpt2_decode_step read it in GPT2_BF16 mode. */
+GPT2_API int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, void* packed, size_t bytes, int precision,
+                         void* stream);
+
+/* Scratch bytes gpt2_forward / gpt2_decode_step need for B sequences of T
+ * tokens (use T = 1 for decode). */
+GPT2_API size_t gpt2_workspace_size(const GPT2Config* cfg, int B, int T, int precision);
+
+/* Bytes of a KV cache for B sequences: layout [L][2][B][NH][maxT][hs]
+ * (keys then values per layer), fp32 in GPT2_FP32 / GPT2_TF32, bf16 in
+ * GPT2_BF16. */
+GPT2_API size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision);
+
+/* The GPT-2 forward pass (pre-LayerNorm blocks) over B sequences of T
+ * tokens [ECE408 Introduction: the forward pass; llm.c: encoder, forward
+ * blocks, classifier]:
+ *   x = encoder(tok); for each layer l:
+ *     x += attproj(attention(qkv(LN1(x))));  x += fcproj(GELU(fc(LN2(x))))
+ *   logits = LN_f(x) wte^T (tied, no bias; all Vp columns);
+ *   probs  = softmax over the first V columns (when probs != NULL).
+ * params: flat fp32 buffer (gpt2_num_parameters values, never written);
+ * packed: output of gpt2_prepare_weights (required for GPT2_BF16, else
+ * ignored); tok [B,T] int32; logits [B,T,Vp]; probs [B,T,Vp] or NULL;
+ * kvcache: NULL, or a cache of gpt2_kvcache_size(cfg, B, precision) bytes
+ * whose positions [0, T) are written (the prefill of decoding);
+ * workspace of gpt2_workspace_size(cfg, B, T, precision) bytes.
+ * Requires 1 <= T <= maxT and C % NH == 0. */
+GPT2_API int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                 float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
+                 void* stream);
+
+/* One KV-cached decode step [NTU "KV Caching"]: each of the B sequences has
+ * `pos` tokens in kvcache (positions [0, pos)) and gets one new token
+ * tok[b] at position pos.  Writes this position's keys and values into the
+ * cache and computes logits [B,Vp] (and probs [B,Vp] when non-null) exactly
+ * as row `pos` of gpt2_forward over the whole sequence would.  Requires
+ * 0 <= pos < maxT; workspace of gpt2_workspace_size(cfg, B, 1, precision). */
+GPT2_API int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* packed, void* kvcache, const int* tok,
+                     int B, int pos, float* logits, float* probs, void* workspace, size_t ws_bytes, int precision,
+                     void* stream);
+
+/* ------------------------------------------------------------ diagnostics */
+
+/* Stages of the forward pass, for gpt2_forward_profile. */
+enum {
+  GPT2_STAGE_ENCODER = 0,
+  GPT2_STAGE_LN1 = 1,       /* all L layers summed, likewise below */
+  GPT2_STAGE_QKV = 2,       /* QKV GEMM (+ cache store when caching) */
+  GPT2_STAGE_ATTENTION = 3,
+  GPT2_STAGE_ATTPROJ = 4,   /* attention projection GEMM + residual */
+  GPT2_STAGE_LN2 = 5,
+  GPT2_STAGE_FC = 6,        /* MLP up-projection GEMM + GELU */
+  GPT2_STAGE_FCPROJ = 7,    /* MLP down-projection GEMM + residual */
+  GPT2_STAGE_LNF = 8,
+  GPT2_STAGE_LMHEAD = 9,
+  GPT2_STAGE_SOFTMAX = 10,
+  GPT2_NUM_STAGES = 11
+};
+
+/* gpt2_forward (without a KV cache) with a CUDA event recorded on `stream`
+ * after every stage; waits for the pass to finish and ADDS each stage's
+ * milliseconds into stage_ms (HOST array of n_stages floats, indexed by
+ * GPT2_STAGE_*).  For measurement only: the events serialise nothing but
+ * the call synchronises the stream. */
+GPT2_API int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void* packed, const int* tok,
+                                  int B, int T, float* logits, float* probs, void* workspace, size_t ws_bytes,
+                                  int precision, void* stream, float* stage_ms, int n_stages);
+
+/* Synchronises `stream`, returns the device error word (a set of
+ * GPT2_DEVERR_*_BIT bits, 0 when clean) and clears it; a negative
+ * GPT2_ERR_CUDA if the synchronisation itself failed. */
+GPT2_API int gpt2_get_error(void* stream);
+
+/* Static text for a GPT2_ERR_* code. */
+GPT2_API const char* gpt2_strerror(int code);
+
+/* Text of the last CUDA error seen by the library on this host thread. */
+GPT2_API const char* gpt2_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GPT2FWD_H */

@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads and exports every function the header
+declares; its host-only entry points answer without a GPU (no compute call
+is made here)."""
+import ctypes
+
+import pytest
+
+from gpt_transformer_forward_gb300 import binding as ab
+from gpt_transformer_forward_gb300 import build, inputs
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ab.load(build_if_missing=False)
+
+
+def test_every_declared_function_is_exported(lib):
+    names = ab.header_functions()
+    assert len(names) == 21
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in ab._SIGNATURES, n
+    assert set(ab._SIGNATURES) == set(names)
+
+
+def test_parameter_count_matches_layout():
+    for cfg in (inputs.TINY, inputs.GPT2_124M, inputs.GPT2_MEDIUM):
+        assert ab.gpt2_num_parameters(cfg) == inputs.num_params(cfg)
+    assert ab.gpt2_num_parameters(inputs.GPT2_124M) == 124475904
+
+
+def test_sizes_are_consistent():
+    cfg = inputs.GPT2_124M
+    C, L, Vp, maxT = cfg.channels, cfg.num_layers, cfg.padded_vocab_size, cfg.max_seq_len
+    packed = ab.gpt2_packed_weights_size(cfg, ab.GPT2_BF16)
+    assert packed >= 2 * (Vp * C + L * 12 * C * C)
+    assert ab.gpt2_packed_weights_size(cfg, ab.GPT2_FP32) == 0
+    kv = ab.gpt2_kvcache_size(cfg, 32, ab.GPT2_BF16)
+    assert kv == L * 2 * 32 * maxT * C * 2
+    assert ab.gpt2_kvcache_size(cfg, 32, ab.GPT2_FP32) == 2 * kv
+    ws16 = ab.gpt2_workspace_size(cfg, 16, 1024, ab.GPT2_BF16)
+    ws32 = ab.gpt2_workspace_size(cfg, 16, 1024, ab.GPT2_FP32)
+    N = 16 * 1024
+    assert ws16 >= N * C * 4 + N * C * 2 * (1 + 3 + 1 + 4)
+    assert ws32 > ws16
+    assert ab.matmul_workspace_size(100, 768, 2304, ab.GPT2_BF16) >= 2 * (100 * 768 + 2304 * 768)
+    assert ab.matmul_workspace_size(100, 768, 2304, ab.GPT2_TF32) == 0
+    assert ab.attention_workspace_size(2, 64, 768, ab.GPT2_FP32) == 0
+
+
+def test_invalid_configs_are_rejected():
+    bad = ab.GPT2Config(1024, 50257, 50304, 12, 7, 768)   # C % NH != 0
+    assert ab.gpt2_num_parameters(bad) == 0
+    assert ab.gpt2_workspace_size(bad, 1, 1, ab.GPT2_BF16) == 0
+    worse = ab.GPT2Config(1024, 50257, 50000, 12, 12, 768)  # Vp < V
+    assert ab.gpt2_num_parameters(worse) == 0
+
+
+def test_argument_errors_before_any_launch(lib):
+    # null pointers and bad shapes return an error code before CUDA is touched
+    assert lib.encoder_forward(None, None, None, None, 1, 1, 8, 1, None) == -1
+    assert lib.softmax_forward(None, None, 1, 5, 4, None) == -1
+    cfg = ab.GPT2Config.of(inputs.TINY)
+    assert lib.gpt2_forward(ctypes.byref(cfg), None, None, None, 1, 1, None, None, None, None, 0, 2, None) == -1
+    bad = ab.GPT2Config(64, 512, 512, 2, 3, 64)
+    assert lib.gpt2_forward(ctypes.byref(bad), 16, None, 16, 1, 1, 16, None, None, 16, 0, 2, None) == -2
+    # T > maxT
+    assert lib.gpt2_forward(ctypes.byref(cfg), 256, 256, 256, 1, 65, 256, None, None, 256, 1 << 30, 2,
+                            None) == -2
+    # misaligned logits pointer
+    assert lib.gpt2_forward(ctypes.byref(cfg), 256, 256, 256, 1, 8, 260, None, None, 256, 1 << 30, 2,
+                            None) == -3
+    # decode position beyond maxT
+    assert lib.gpt2_decode_step(ctypes.byref(cfg), 256, 256, 256, 256, 1, 64, 256, None, 256, 1 << 30, 2,
+                                None) == -2
+    assert ab.gpt2_strerror(-4).startswith("workspace")

@@ -1,0 +1,128 @@
+"""KV-cached decoding on the GPU: prefill with gpt2_forward writing the
+cache, then gpt2_decode_step, against the oracle's decode step (itself
+pinned to full recomputation).  The full decode workload (32 sequences) is
+checked through batch independence: its sequences 0 and 1 must equal,
+bitwise, a 2-sequence run that the oracle checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpt_transformer_forward_gb300 import binding as ab
+from gpt_transformer_forward_gb300 import inputs
+from gpt_transformer_forward_gb300.runner import GPT2Model
+
+from gpu_helpers import assert_close, dev, host, need_gpu, no_device_error
+
+pytestmark = pytest.mark.gpu
+LOGIT_TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_TF32: 5e-3, ab.GPT2_FP32: 1e-4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+def teacher_forced(m, cfg, tok, P, steps):
+    """Prefill P tokens, then decode tokens P..P+steps-1 given; returns the
+    prefill logits of the last prompt row and each step's logits."""
+    B = tok.shape[0]
+    cache = m.new_kvcache(B)
+    lg, _ = m.new_outputs(B, P, probs=False)
+    m.forward(dev(tok[:, :P]), lg, kvcache=cache)
+    out = []
+    for i in range(steps):
+        step_lg, _ = m.new_outputs(B, None, probs=False)
+        m.decode_step(cache, dev(tok[:, P + i]), P + i, step_lg)
+        out.append(host(step_lg))
+    no_device_error()
+    return host(lg), np.stack(out, axis=1)
+
+
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_TF32, ab.GPT2_FP32])
+def test_tiny_decode_matches_oracle(precision):
+    cfg = inputs.TINY
+    params = inputs.make_params(cfg, 90, "perturbed")
+    tok = inputs.make_tokens(91, 3, 40, cfg.vocab_size)
+    m = GPT2Model(cfg, params, 3, 40, precision)
+    _, steps = teacher_forced(m, cfg, tok, 20, 20)
+    full, _ = oracle.forward(cfg, params, tok, want_probs=False)
+    assert_close(steps, full[:, 20:40], atol=LOGIT_TOL[precision], what="decode vs recompute")
+
+
+def test_tiny_decode_from_position_zero():
+    cfg = inputs.TINY
+    params = inputs.make_params(cfg, 92, "perturbed")
+    tok = inputs.make_tokens(93, 2, 64, cfg.vocab_size)
+    m = GPT2Model(cfg, params, 2, 64, ab.GPT2_BF16)
+    cache = m.new_kvcache(2)
+    full, _ = oracle.forward(cfg, params, tok, want_probs=False)
+    for pos in range(64):  # up to the last position maxT - 1
+        lg, pr = m.new_outputs(2, None)
+        m.decode_step(cache, dev(tok[:, pos]), pos, lg, pr)
+        assert_close(host(lg), full[:, pos], atol=2e-2, what=f"pos {pos}")
+        np.testing.assert_allclose(host(pr).sum(-1), 1.0, atol=1e-4)
+
+
+def test_decode_rejects_position_past_maxT():
+    cfg = inputs.TINY
+    m = GPT2Model(cfg, inputs.make_params(cfg, 94), 1, 1, ab.GPT2_BF16)
+    cache = m.new_kvcache(1)
+    lg, _ = m.new_outputs(1, None, probs=False)
+    with pytest.raises(ab.GPT2Error) as e:
+        m.decode_step(cache, torch.zeros(1, dtype=torch.int32, device="cuda"), cfg.max_seq_len, lg)
+    assert e.value.code == -2
+
+
+def test_gpt2_124m_decode():
+    w = inputs.WORKLOADS["gpt2-124m-decode"]
+    cfg = w.cfg
+    params = inputs.make_params(cfg, w.weight_seed)
+    P, steps = w.T, 6
+    tok = inputs.make_tokens(w.token_seed, w.B, P + steps, cfg.vocab_size)
+    # a 2-sequence run, checked against the oracle
+    m2 = GPT2Model(cfg, params, 2, P, ab.GPT2_BF16)
+    pre2, st2 = teacher_forced(m2, cfg, tok[:2], P, steps)
+    ref_pre, _, cache = oracle.forward(cfg, params, tok[:2, :P], want_probs=False, with_cache=True)
+    assert_close(pre2[:, P - 1], ref_pre[:, P - 1], atol=2e-2, what="prefill last row")
+    for i in range(steps):
+        ref = oracle.decode_step(cfg, params, cache, tok[:2, P + i], P + i)
+        assert_close(st2[:, i], ref, atol=2e-2, what=f"step {i}")
+    # the full 32-sequence workload: sequences 0 and 1 equal the checked run
+    m32 = GPT2Model(cfg, params, w.B, P, ab.GPT2_BF16)
+    pre32, st32 = teacher_forced(m32, cfg, tok, P, steps)
+    np.testing.assert_array_equal(st32[:2], st2)
+    np.testing.assert_array_equal(pre32[:2], pre2)
+
+
+def test_greedy_generation_matches_oracle_where_decided():
+    cfg = inputs.TINY
+    params = inputs.make_params(cfg, 95, "perturbed")
+    B, P, steps = 4, 16, 24
+    prompt = inputs.make_tokens(96, B, P, cfg.vocab_size)
+    m = GPT2Model(cfg, params, B, P + steps, ab.GPT2_BF16)
+    cache = m.new_kvcache(B)
+    lg, _ = m.new_outputs(B, P, probs=False)
+    m.forward(dev(prompt), lg, kvcache=cache)
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    ab.gpt2_argmax(nxt, lg[:, P - 1].contiguous(), B, cfg.vocab_size, cfg.padded_vocab_size)
+    gen = [host(nxt)]
+    for i in range(steps - 1):
+        step_lg, _ = m.new_outputs(B, None, probs=False)
+        m.decode_step(cache, nxt, P + i, step_lg)
+        ab.gpt2_argmax(nxt, step_lg, B, cfg.vocab_size, cfg.padded_vocab_size)
+        gen.append(host(nxt))
+    gen = np.stack(gen, axis=1)
+    # the oracle follows the GPU's tokens; each GPU choice must be the
+    # oracle's argmax wherever the oracle's top-2 margin exceeds 2 x 2e-2
+    seq = np.concatenate([prompt, gen], axis=1)
+    full, _ = oracle.forward(cfg, params, seq[:, :-1], want_probs=False)
+    decided = 0
+    for i in range(steps):
+        row = full[:, P - 1 + i, :cfg.vocab_size]
+        top2 = np.sort(row, axis=1)[:, -2:]
+        margin = top2[:, 1] - top2[:, 0]
+        sure = margin > 4e-2
+        decided += int(sure.sum())
+        np.testing.assert_array_equal(gen[sure, i], np.argmax(row, axis=1)[sure])
+    assert decided > B * steps // 2

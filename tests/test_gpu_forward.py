@@ -1,0 +1,133 @@
+"""End-to-end parity of gpt2_forward against the oracle.
+
+Tiny GPT-2 (every precision, both initialisations) is compared on every
+element.  At the 124M and medium sizes the oracle computes sampled rows:
+causality makes rows 0..P-1 of a sequence depend on its first P tokens only,
+and batch independence makes each sequence its own problem, so a prefix of
+one sequence and the last row of another are exact references for those
+rows of the full-size run.  Properties that hold at any size (row sums,
+padding, causality, batch permutation) are checked on every row.
+
+Tolerances: logits 2e-2 absolute and probabilities 1e-3 absolute with bf16
+operands; 5e-3 / 1e-3 with tf32 operands; 1e-4 / 1e-6 in fp32 mode."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpt_transformer_forward_gb300 import binding as ab
+from gpt_transformer_forward_gb300 import inputs
+from gpt_transformer_forward_gb300.runner import GPT2Model
+
+from gpu_helpers import assert_close, dev, host, need_gpu, no_device_error
+
+pytestmark = pytest.mark.gpu
+LOGIT_TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_TF32: 5e-3, ab.GPT2_FP32: 1e-4}
+PROB_TOL = {ab.GPT2_BF16: 1e-3, ab.GPT2_TF32: 1e-3, ab.GPT2_FP32: 1e-6}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    need_gpu()
+
+
+@pytest.mark.parametrize("init", ["gpt2", "perturbed"])
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_TF32, ab.GPT2_FP32])
+def test_tiny_forward(precision, init):
+    w = inputs.WORKLOADS["tiny"]
+    params, tok = inputs.workload_inputs(w, init)
+    m = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    rl, rp = oracle.forward(w.cfg, params, tok)
+    assert_close(host(logits), rl, atol=LOGIT_TOL[precision], what="tiny logits")
+    assert_close(host(probs), rp, atol=PROB_TOL[precision], what="tiny probs")
+
+
+@pytest.mark.parametrize("T", [1, 17, 64])
+def test_tiny_forward_short_sequences(T):
+    w = inputs.WORKLOADS["tiny"]
+    params = inputs.make_params(w.cfg, 77, "perturbed")
+    tok = inputs.make_tokens(78, 3, T, w.cfg.vocab_size)
+    m = GPT2Model(w.cfg, params, 3, T, ab.GPT2_BF16)
+    logits, probs = m.new_outputs(3, T)
+    m.forward(dev(tok), logits, probs)
+    rl, rp = oracle.forward(w.cfg, params, tok)
+    assert_close(host(logits), rl, atol=2e-2, what="logits")
+    assert_close(host(probs), rp, atol=1e-3, what="probs")
+
+
+def test_forward_causal_and_batch_permutation_bitwise():
+    w = inputs.WORKLOADS["tiny"]
+    params = inputs.make_params(w.cfg, 79, "perturbed")
+    tok = inputs.make_tokens(80, 4, 48, w.cfg.vocab_size)
+    m = GPT2Model(w.cfg, params, 4, 48, ab.GPT2_BF16)
+    outs = []
+    pert = tok.copy()
+    pert[:, 30:] = (pert[:, 30:] + 5) % w.cfg.vocab_size
+    for t in (tok, pert, tok[[3, 1, 0, 2]]):
+        lg, _ = m.new_outputs(4, 48, probs=False)
+        m.forward(dev(t), lg)
+        outs.append(host(lg))
+    np.testing.assert_array_equal(outs[0][:, :30], outs[1][:, :30])
+    assert np.abs(outs[0][:, 30:] - outs[1][:, 30:]).max() > 1e-3
+    np.testing.assert_array_equal(outs[2], outs[0][[3, 1, 0, 2]])
+
+
+def check_sampled(w, precision, logits, probs, params, tok, prefix_rows, full_seq, full_rows):
+    """Oracle rows: sequence 0's first prefix_rows positions (every column),
+    and rows full_rows of sequence full_seq (needs that whole sequence)."""
+    cfg = w.cfg
+    rl, rp = oracle.forward(cfg, params, tok[:1, :prefix_rows])
+    assert_close(host(logits[:1, :prefix_rows]), rl, atol=LOGIT_TOL[precision], what="prefix logits")
+    assert_close(host(probs[:1, :prefix_rows]), rp, atol=PROB_TOL[precision], what="prefix probs")
+    h = oracle.hidden(cfg, params, tok[full_seq:full_seq + 1])
+    rows = np.array(full_rows)
+    rl = oracle.lm_head(cfg, params, h[0, rows])
+    rp = oracle.softmax(rl, cfg.vocab_size)
+    assert_close(host(logits[full_seq, rows]), rl, atol=LOGIT_TOL[precision], what="late-row logits")
+    assert_close(host(probs[full_seq, rows]), rp, atol=PROB_TOL[precision], what="late-row probs")
+
+
+def check_properties(cfg, logits, probs):
+    V = cfg.vocab_size
+    s = probs[..., :V].sum(dim=-1, dtype=torch.float64)
+    assert float((s - 1).abs().max()) < 1e-4
+    assert bool((probs[..., V:] == 0).all()) and bool((logits[..., V:] == 0).all())
+    assert bool((probs >= 0).all())
+    assert bool(torch.isfinite(logits).all())
+
+
+@pytest.mark.parametrize("name", ["gpt2-124m-b4", "gpt2-124m-b16"])
+def test_gpt2_124m_sampled(name):
+    w = inputs.WORKLOADS[name]
+    params, tok = inputs.workload_inputs(w)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_BF16)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(w.cfg, logits, probs)
+    check_sampled(w, ab.GPT2_BF16, logits, probs, params, tok, 64, w.B - 1, [0, 511, 777, 1023])
+
+
+def test_gpt2_medium_sampled():
+    w = inputs.WORKLOADS["gpt2-medium-b8"]
+    params, tok = inputs.workload_inputs(w)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_BF16)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(w.cfg, logits, probs)
+    check_sampled(w, ab.GPT2_BF16, logits, probs, params, tok, 32, w.B - 1, [1023])
+
+
+def test_gpt2_124m_tf32_sampled():
+    w = inputs.WORKLOADS["gpt2-124m-b4"]
+    params, tok = inputs.workload_inputs(w)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_TF32)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(w.cfg, logits, probs)
+    check_sampled(w, ab.GPT2_TF32, logits, probs, params, tok, 32, 0, [1023])
