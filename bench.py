@@ -276,7 +276,7 @@ def run_ours(args):
         for k, v in model.forward_profile(tok_d, logits, probs).items():
             stage_ms[k] += v / prof_runs
     peaks, peak_src = load_peaks()
-    costs = stage_costs(w.cfg, w.B, w.T, act_bytes=2 if precision == ab.GPT2_BF16 else 4)
+    costs = stage_costs(w.cfg, w.B, w.T, act_bytes=2 if precision in (ab.GPT2_BF16, ab.GPT2_FP16) else 4)
     hbm = peaks["hbm_gbs"] * 1e9
     tensor = peaks["bf16_tflops_sustained"] * 1e12
     stages, roof_ms = {}, 0.0
@@ -338,7 +338,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
-    ap.add_argument("--precision", default="bf16", choices=["bf16", "tf32", "fp32"])
+    ap.add_argument("--precision", default="fp16", choices=["fp16", "bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -15,8 +15,8 @@ import re
 
 from . import build as _build
 
-GPT2_FP32, GPT2_TF32, GPT2_BF16 = 0, 1, 2
-PRECISIONS = {"fp32": GPT2_FP32, "tf32": GPT2_TF32, "bf16": GPT2_BF16}
+GPT2_FP32, GPT2_TF32, GPT2_BF16, GPT2_FP16 = 0, 1, 2, 3
+PRECISIONS = {"fp32": GPT2_FP32, "tf32": GPT2_TF32, "bf16": GPT2_BF16, "fp16": GPT2_FP16}
 
 GPT2_OK = 0
 ERRORS = {-1: "GPT2_ERR_ARG", -2: "GPT2_ERR_SHAPE", -3: "GPT2_ERR_ALIGN", -4: "GPT2_ERR_WORKSPACE",

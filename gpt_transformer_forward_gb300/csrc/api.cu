@@ -9,9 +9,10 @@
 //   (+bias, +residual in place) -> LN2 -> FC GEMM(+bias, GELU) -> FC-proj
 //   GEMM(+bias, +residual in place)] -> LN_f -> LM-head GEMM (tied wte) ->
 //   softmax.
-// In GPT2_BF16 mode LayerNorm, attention and the GELU epilogue write bf16
-// directly, because that is the only form in which the next GEMM consumes
-// them; the residual stream x stays fp32.
+// In the 16-bit modes (GPT2_BF16, GPT2_FP16) LayerNorm, the QKV and GELU
+// epilogues and attention write the 16-bit operand type directly, because
+// that is the only form in which the next tensor-core step consumes them;
+// the residual stream x, the logits and the probabilities stay fp32.
 #include <stdio.h>
 
 #include <cstring>
@@ -63,7 +64,19 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
     if (_rc != GPT2_OK) return _rc; \
   } while (0)
 
-bool valid_precision(int p) { return p == GPT2_FP32 || p == GPT2_TF32 || p == GPT2_BF16; }
+bool valid_precision(int p) { return p == GPT2_FP32 || p == GPT2_TF32 || p == GPT2_BF16 || p == GPT2_FP16; }
+// 16-bit operand modes keep GEMM operands, attention inputs and the KV cache in
+// the 16-bit type; the tensor-core operand type of each mode:
+bool is16(int p) { return p == GPT2_BF16 || p == GPT2_FP16; }
+int op_of(int p) { return p == GPT2_FP16 ? kOpF16 : (p == GPT2_TF32 ? kOpTF32 : kOpBF16); }
+
+// fp32 -> the 16-bit operand type of a 16-bit precision mode
+void to16(int precision, void* out, const float* in, long long n, cudaStream_t s) {
+  if (precision == GPT2_FP16)
+    launch_f32_to_16(static_cast<__half*>(out), in, n, s);
+  else
+    launch_f32_to_16(static_cast<__nv_bfloat16*>(out), in, n, s);
+}
 
 int check_config(const GPT2Config* c) {
   RETURN_IF(c == nullptr, GPT2_ERR_ARG);
@@ -131,12 +144,12 @@ PackedOffsets packed_offsets(const GPT2Config* c) {
 
 // ---------------------------------------------------------- workspace
 struct Workspace {
-  size_t x, ln, qkv, qkv16, att, fch, dec, total;  // byte offsets
+  size_t x, ln, qkv, qkv16, att, fch, dec, stats, total;  // byte offsets
 };
 
 Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
   const size_t N = static_cast<size_t>(B) * T, C = c->channels;
-  const size_t act = (precision == GPT2_BF16) ? 2 : 4;  // operand buffers
+  const size_t act = is16(precision) ? 2 : 4;  // operand buffers
   Workspace w;
   size_t p = 0;
   w.x = p; p = round_up(p + N * C * 4, 256);
@@ -147,11 +160,12 @@ Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
   w.att = p; p = round_up(p + N * C * act, 256);
   w.fch = p; p = round_up(p + N * 4 * C * act, 256);
   w.dec = p; p = round_up(p + decode_attention_scratch_floats(B, c->channels, c->num_heads, c->max_seq_len) * 4, 256);
+  w.stats = p; p = round_up(p + N * gemm_tiles_n(c->padded_vocab_size) * sizeof(float2), 256);  // softmax statistics
   w.total = p;
   return w;
 }
 
-size_t kv_elem_bytes(int precision) { return precision == GPT2_BF16 ? 2 : 4; }
+size_t kv_elem_bytes(int precision) { return is16(precision) ? 2 : 4; }
 
 // elements of one layer's cache slab [2][B][NH][maxT][hs]
 size_t kv_layer_elems(const GPT2Config* c, int B) {
@@ -166,13 +180,13 @@ int gemm(int precision, void* out, const void* A, const void* W, const float* bi
                      N, K, epi, s);
     return check_launch();
   }
-  if (precision == GPT2_TF32 && epi == kEpiGeluBF16) {
+  if (precision == GPT2_TF32 && epi == kEpiGelu16) {
     // tf32 operands with an fp32 GELU output: GEMM then the GELU kernel
-    TRY(launch_gemm_tc(out, A, W, bias, M, N, K, kEpiF32, false, s));
+    TRY(launch_gemm_tc(out, A, W, bias, M, N, K, kEpiF32, kOpTF32, s));
     launch_gelu(static_cast<float*>(out), static_cast<const float*>(out), M * N, s);
     return check_launch();
   }
-  return launch_gemm_tc(out, A, W, bias, M, N, K, epi, precision == GPT2_BF16, s);
+  return launch_gemm_tc(out, A, W, bias, M, N, K, epi, op_of(precision), s);
 }
 
 // Records a CUDA event on the stream after each stage of the forward pass;
@@ -236,7 +250,7 @@ int layernorm_forward(float* out, float* mean, float* rstd, const float* inp, co
 }
 
 size_t matmul_workspace_size(int N, int C, int OC, int precision) {
-  if (precision != GPT2_BF16 || N <= 0 || C <= 0 || OC <= 0) return 0;
+  if (!is16(precision) || N <= 0 || C <= 0 || OC <= 0) return 0;
   return round_up(static_cast<size_t>(N) * C * 2, 256) + round_up(static_cast<size_t>(OC) * C * 2, 256);
 }
 
@@ -249,17 +263,16 @@ int matmul_forward(float* out, const float* inp, const float* W, const float* bi
   cudaStream_t s = as_stream(stream);
   if (precision == GPT2_FP32) return gemm(precision, out, inp, W, bias, N, OC, C, kEpiF32, s);
   RETURN_IF(C % 8 != 0 || OC % 4 != 0, GPT2_ERR_SHAPE);
-  if (precision == GPT2_TF32) return launch_gemm_tc(out, inp, W, bias, N, OC, C, kEpiF32, false, s);
+  if (precision == GPT2_TF32) return launch_gemm_tc(out, inp, W, bias, N, OC, C, kEpiF32, kOpTF32, s);
   const size_t need = matmul_workspace_size(N, C, OC, precision);
   RETURN_IF(workspace == nullptr || ws_bytes < need, GPT2_ERR_WORKSPACE);
   RETURN_IF((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0, GPT2_ERR_ALIGN);
-  __nv_bfloat16* a16 = static_cast<__nv_bfloat16*>(workspace);
-  __nv_bfloat16* w16 =
-      reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + round_up(static_cast<size_t>(N) * C * 2, 256));
-  launch_f32_to_bf16(a16, inp, static_cast<long long>(N) * C, s);
-  launch_f32_to_bf16(w16, W, static_cast<long long>(OC) * C, s);
+  void* a16 = workspace;
+  void* w16 = static_cast<uint8_t*>(workspace) + round_up(static_cast<size_t>(N) * C * 2, 256);
+  to16(precision, a16, inp, static_cast<long long>(N) * C, s);
+  to16(precision, w16, W, static_cast<long long>(OC) * C, s);
   TRY(check_launch());
-  return launch_gemm_tc(out, a16, w16, bias, N, OC, C, kEpiF32, true, s);
+  return launch_gemm_tc(out, a16, w16, bias, N, OC, C, kEpiF32, op_of(precision), s);
 }
 
 size_t attention_workspace_size(int B, int T, int C, int precision) {
@@ -282,9 +295,10 @@ int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH,
   }
   RETURN_IF(workspace == nullptr || ws_bytes < attention_workspace_size(B, T, C, precision), GPT2_ERR_WORKSPACE);
   RETURN_IF(!aligned16(workspace), GPT2_ERR_ALIGN);
-  __nv_bfloat16* q16 = static_cast<__nv_bfloat16*>(workspace);
-  launch_f32_to_bf16(q16, qkv, static_cast<long long>(B) * T * 3 * C, s);
-  TRY(launch_attention_bf16(out, false, q16, B, T, C, NH, s));
+  // GPT2_TF32 runs the bf16 kernel; GPT2_BF16 / GPT2_FP16 their own type
+  const int p16 = precision == GPT2_FP16 ? GPT2_FP16 : GPT2_BF16;
+  to16(p16, workspace, qkv, static_cast<long long>(B) * T * 3 * C, s);
+  TRY(launch_attention_16(out, false, workspace, op_of(p16), B, T, C, NH, s));
   return check_launch();
 }
 
@@ -326,7 +340,7 @@ size_t gpt2_num_parameters(const GPT2Config* cfg) {
 }
 
 size_t gpt2_packed_weights_size(const GPT2Config* cfg, int precision) {
-  if (check_config(cfg) != GPT2_OK || precision != GPT2_BF16) return 0;
+  if (check_config(cfg) != GPT2_OK || !is16(precision)) return 0;
   return packed_offsets(cfg).total;
 }
 
@@ -334,7 +348,7 @@ int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, void* packe
                          void* stream) {
   TRY(check_config(cfg));
   RETURN_IF(!params || !valid_precision(precision), GPT2_ERR_ARG);
-  if (precision != GPT2_BF16) return GPT2_OK;
+  if (!is16(precision)) return GPT2_OK;
   RETURN_IF(!packed, GPT2_ERR_ARG);
   RETURN_IF(bytes < gpt2_packed_weights_size(cfg, precision), GPT2_ERR_WORKSPACE);
   RETURN_IF(!aligned16(params) || (reinterpret_cast<uintptr_t>(packed) & 255u) != 0, GPT2_ERR_ALIGN);
@@ -344,8 +358,7 @@ int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, void* packe
   uint8_t* base = static_cast<uint8_t*>(packed);
   cudaStream_t s = as_stream(stream);
   auto conv = [&](size_t dst_off, size_t src_off, size_t n) {
-    launch_f32_to_bf16(reinterpret_cast<__nv_bfloat16*>(base + dst_off), params + src_off,
-                       static_cast<long long>(n), s);
+    to16(precision, base + dst_off, params + src_off, static_cast<long long>(n), s);
   };
   conv(ko.wte, po.wte, Vp * C);
   conv(ko.qkvw, po.qkvw, L * 3 * C * C);
@@ -385,7 +398,8 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
   void* att = ws + wl.att;
   void* fch = ws + wl.fch;
   float* dec_scratch = reinterpret_cast<float*>(ws + wl.dec);
-  const bool bf16 = precision == GPT2_BF16;
+  const bool bf16 = is16(precision);  // 16-bit operand buffers (bf16 or fp16)
+  const int op = op_of(precision);
   const PackedOffsets ko = packed_offsets(cfg);
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
   const size_t kv_slab = kv_layer_elems(cfg, B);
@@ -397,8 +411,10 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     return params + f32_off + static_cast<size_t>(l) * per_layer;
   };
   auto layernorm = [&](void* out, const float* in, size_t w_off, size_t b_off) {
-    if (bf16)
-      launch_layernorm_bf16(static_cast<__nv_bfloat16*>(out), in, params + w_off, params + b_off, N, C, s);
+    if (precision == GPT2_FP16)
+      launch_layernorm_16(static_cast<__half*>(out), in, params + w_off, params + b_off, N, C, s);
+    else if (precision == GPT2_BF16)
+      launch_layernorm_16(static_cast<__nv_bfloat16*>(out), in, params + w_off, params + b_off, N, C, s);
     else
       launch_layernorm_f32(static_cast<float*>(out), nullptr, nullptr, in, params + w_off, params + b_off, N, C, s);
   };
@@ -415,12 +431,12 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     layernorm(ln, x, po.ln1w + static_cast<size_t>(l) * C, po.ln1b + static_cast<size_t>(l) * C);
     TRY(mark(GPT2_STAGE_LN1));
     TRY(gemm(precision, qkv, ln, wmat(po.qkvw, ko.qkvw, 3 * CC, l), params + po.qkvb + static_cast<size_t>(l) * 3 * C,
-             N, 3 * C, C, bf16 ? kEpiBF16 : kEpiF32, s));
+             N, 3 * C, C, bf16 ? kEpiOut16 : kEpiF32, s));
     if (kvcache != nullptr) {
       const int pos0 = decode_pos < 0 ? 0 : decode_pos;
       if (bf16)
-        launch_kv_store_bf16(static_cast<__nv_bfloat16*>(kvcache) + l * kv_slab,
-                             static_cast<const __nv_bfloat16*>(qkv), B, T, C, NH, maxT, pos0, s);
+        launch_kv_store_16(static_cast<uint16_t*>(kvcache) + l * kv_slab, static_cast<const uint16_t*>(qkv), B, T,
+                           C, NH, maxT, pos0, s);
       else
         launch_kv_store_f32(static_cast<float*>(kvcache) + l * kv_slab, static_cast<const float*>(qkv), B, T, C, NH,
                             maxT, pos0, s);
@@ -430,17 +446,16 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
       if (precision == GPT2_FP32) {
         TRY(launch_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), B, T, C, NH, s));
       } else if (precision == GPT2_TF32) {
-        __nv_bfloat16* q16 = reinterpret_cast<__nv_bfloat16*>(ws + wl.qkv16);
-        launch_f32_to_bf16(q16, static_cast<const float*>(qkv), static_cast<long long>(N) * 3 * C, s);
-        TRY(launch_attention_bf16(att, false, q16, B, T, C, NH, s));
+        void* q16 = ws + wl.qkv16;
+        to16(GPT2_BF16, q16, static_cast<const float*>(qkv), static_cast<long long>(N) * 3 * C, s);
+        TRY(launch_attention_16(att, false, q16, kOpBF16, B, T, C, NH, s));
       } else {
-        TRY(launch_attention_bf16(att, true, static_cast<const __nv_bfloat16*>(qkv), B, T, C, NH, s));
+        TRY(launch_attention_16(att, true, qkv, op, B, T, C, NH, s));
       }
     } else {
       if (bf16) {
-        const __nv_bfloat16* kc = static_cast<const __nv_bfloat16*>(kvcache) + l * kv_slab;
-        launch_decode_attention_bf16(att, true, static_cast<const __nv_bfloat16*>(qkv), kc, kc + kv_half, B, C, NH,
-                                     maxT, decode_pos, dec_scratch, s);
+        const uint16_t* kc = static_cast<const uint16_t*>(kvcache) + l * kv_slab;
+        launch_decode_attention_16(att, true, qkv, kc, kc + kv_half, op, B, C, NH, maxT, decode_pos, dec_scratch, s);
       } else {
         const float* kc = static_cast<const float*>(kvcache) + l * kv_slab;
         launch_decode_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), kc, kc + kv_half, B, C,
@@ -455,7 +470,7 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     layernorm(ln, x, po.ln2w + static_cast<size_t>(l) * C, po.ln2b + static_cast<size_t>(l) * C);
     TRY(mark(GPT2_STAGE_LN2));
     TRY(gemm(precision, fch, ln, wmat(po.fcw, ko.fcw, 4 * CC, l), params + po.fcb + static_cast<size_t>(l) * 4 * C, N,
-             4 * C, C, kEpiGeluBF16, s));
+             4 * C, C, kEpiGelu16, s));
     TRY(mark(GPT2_STAGE_FC));
     TRY(gemm(precision, x, fch, wmat(po.fcprojw, ko.fcprojw, 4 * CC, l),
              params + po.fcprojb + static_cast<size_t>(l) * C, N, C, 4 * C, kEpiResidF32, s));
@@ -464,9 +479,18 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
   layernorm(ln, x, po.lnfw, po.lnfb);
   TRY(mark(GPT2_STAGE_LNF));
   const void* wte = bf16 ? static_cast<const void*>(pk + ko.wte) : static_cast<const void*>(params + po.wte);
-  TRY(gemm(precision, logits, ln, wte, nullptr, N, Vp, C, kEpiF32, s));
+  float2* stats = reinterpret_cast<float2*>(ws + wl.stats);
+  if (precision == GPT2_FP32)
+    TRY(gemm(precision, logits, ln, wte, nullptr, N, Vp, C, kEpiF32, s));
+  else
+    TRY(launch_gemm_logits(logits, stats, ln, wte, N, Vp, C, V, op, s));
   TRY(mark(GPT2_STAGE_LMHEAD));
-  if (probs != nullptr) launch_softmax(probs, logits, N, V, Vp, s);
+  if (probs != nullptr) {
+    if (precision == GPT2_FP32)
+      launch_softmax(probs, logits, N, V, Vp, s);
+    else
+      launch_softmax_from_stats(probs, logits, stats, gemm_tiles_n(Vp), N, V, Vp, s);
+  }
   TRY(check_launch());
   TRY(mark(GPT2_STAGE_SOFTMAX));
   return GPT2_OK;
@@ -480,7 +504,7 @@ int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed,
   RETURN_IF(B <= 0 || T <= 0, GPT2_ERR_ARG);
   RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(cfg->channels, cfg->num_heads));
-  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(is16(precision) && packed == nullptr, GPT2_ERR_ARG);
   RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
                 (kvcache && !aligned16(kvcache)) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
@@ -497,7 +521,7 @@ int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void*
   RETURN_IF(B <= 0 || T <= 0 || n_stages <= 0, GPT2_ERR_ARG);
   RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(cfg->channels, cfg->num_heads));
-  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(is16(precision) && packed == nullptr, GPT2_ERR_ARG);
   RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
                 (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
@@ -519,7 +543,7 @@ int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* pac
   RETURN_IF(B <= 0, GPT2_ERR_ARG);
   RETURN_IF(pos < 0 || pos >= cfg->max_seq_len, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(cfg->channels, cfg->num_heads));
-  RETURN_IF(precision == GPT2_BF16 && packed == nullptr, GPT2_ERR_ARG);
+  RETURN_IF(is16(precision) && packed == nullptr, GPT2_ERR_ARG);
   RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) || !aligned16(kvcache) ||
                 (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),

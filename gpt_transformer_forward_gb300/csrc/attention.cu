@@ -10,9 +10,9 @@
 // h = columns h*hs .. h*hs+hs-1 of each), and the output is written straight
 // into [B, T, C]: no permute or unpermute pass.
 //
-//   attn_bf16_kernel    bf16 tensor cores (mma.sync m16n8k16, fp32
-//                       accumulate), head size 16, 32 or 64, 64 query rows
-//                       per block;
+//   attn_tc_kernel      tensor cores (mma.sync m16n8k16 on bf16 or fp16
+//                       operands, fp32 accumulate), head size 16, 32 or 64,
+//                       64 query rows per block;
 //   attn_f32_kernel     fp32 CUDA cores, reference-grade (GPT2_FP32 mode);
 //   decode kernels      one query per sequence against the KV cache, split
 //                       over positions, then a combine pass.
@@ -43,13 +43,22 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr));
 }
 
-// d += a * b, m16n8k16, bf16 inputs, fp32 accumulators
-__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// d += a * b, m16n8k16, 16-bit inputs of type T (bf16 or fp16), fp32 accumulators
+template <typename T>
+__device__ __forceinline__ void mma16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (std::is_same<T, __half>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 }
 
 __device__ __forceinline__ float exp2_fast(float x) {
@@ -76,22 +85,21 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // HS-wide column block starting at `col` of qkv into a swizzled tile; rows
 // at or beyond T are zero-filled.
 template <int HS>
-__device__ __forceinline__ void load_tile(uint8_t* tile, const __nv_bfloat16* qkv, int b, int T, int C3, int col,
+__device__ __forceinline__ void load_tile(uint8_t* tile, const uint16_t* qkv, int b, int T, int C3, int col,
                                           int row0) {
   constexpr int kChunks = HS / 8;
   for (int idx = threadIdx.x; idx < kBKV * kChunks; idx += kAttnThreads) {
     const int r = idx / kChunks, c = idx % kChunks;
     const int t = row0 + r;
     const bool valid = t < T;
-    const __nv_bfloat16* src = qkv + (static_cast<size_t>(b) * T + (valid ? t : 0)) * C3 + col + c * 8;
+    const uint16_t* src = qkv + (static_cast<size_t>(b) * T + (valid ? t : 0)) * C3 + col + c * 8;
     cp_async16(tile + swz<HS>(r, c), src, valid);
   }
 }
 
-template <int HS, bool kOutBF16>
-__global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(void* __restrict__ out,
-                                                                 const __nv_bfloat16* __restrict__ qkv, int T, int C,
-                                                                 float scale_log2) {
+template <int HS, typename T16, bool kOut16>
+__global__ void __launch_bounds__(kAttnThreads) attn_tc_kernel(void* __restrict__ out, const uint16_t* __restrict__ qkv,
+                                                               int T, int C, float scale_log2) {
   constexpr int kKS = HS / 16;  // k-steps of Q K^T over the head dimension
   constexpr int kDT = HS / 8;   // 8-wide output column tiles
   __shared__ __align__(128) uint8_t q_s[kBQ * HS * 2];
@@ -149,8 +157,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(void* __restric
         const int c = ks * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kb + swz<HS>(key, c), b0, b1, b2, b3);
-        mma_bf16(s[2 * np], qf[ks], b0, b1);
-        mma_bf16(s[2 * np + 1], qf[ks], b2, b3);
+        mma16<T16>(s[2 * np], qf[ks], b0, b1);
+        mma16<T16>(s[2 * np + 1], qf[ks], b2, b3);
       }
     }
     // scale into log2 units and mask the diagonal tile
@@ -200,18 +208,18 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(void* __restric
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
-      pa[1] = pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
-      pa[2] = pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+      pa[0] = pack2<T16>(s[2 * ks][0], s[2 * ks][1]);
+      pa[1] = pack2<T16>(s[2 * ks][2], s[2 * ks][3]);
+      pa[2] = pack2<T16>(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      pa[3] = pack2<T16>(s[2 * ks + 1][2], s[2 * ks + 1][3]);
 #pragma unroll
       for (int dp = 0; dp < kDT / 2; ++dp) {
         const int key = ks * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int c = dp * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vb + swz<HS>(key, c), b0, b1, b2, b3);
-        mma_bf16(o[2 * dp], pa, b0, b1);
-        mma_bf16(o[2 * dp + 1], pa, b2, b3);
+        mma16<T16>(o[2 * dp], pa, b0, b1);
+        mma16<T16>(o[2 * dp + 1], pa, b2, b3);
       }
     }
     __syncthreads();  // this buffer is refilled by the next iteration's prefetch
@@ -230,8 +238,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_bf16_kernel(void* __restric
     for (int dt = 0; dt < kDT; ++dt) {
       const int d = dt * 8 + 2 * tig;
       const float x0 = o[dt][2 * r] * inv, x1 = o[dt][2 * r + 1] * inv;
-      if constexpr (kOutBF16) {
-        *reinterpret_cast<uint32_t*>(reinterpret_cast<__nv_bfloat16*>(out) + base + d) = pack_bf16x2(x0, x1);
+      if constexpr (kOut16) {
+        *reinterpret_cast<uint32_t*>(reinterpret_cast<T16*>(out) + base + d) = pack2<T16>(x0, x1);
       } else {
         *reinterpret_cast<float2*>(reinterpret_cast<float*>(out) + base + d) = make_float2(x0, x1);
       }
@@ -317,7 +325,7 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __re
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int d = threadIdx.x; d < HS; d += blockDim.x)
-    q_s[d] = static_cast<float>(qkv[static_cast<size_t>(b) * 3 * C + h * HS + d]);
+    q_s[d] = to_f32(qkv[static_cast<size_t>(b) * 3 * C + h * HS + d]);
   __syncthreads();
   const int chunk = split * kDecWarps + warp;
   const int j = chunk * kDecPos + lane;
@@ -327,7 +335,7 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __re
     const E* krow = kcache + (head + j) * HS;
     float dot = 0.f;
 #pragma unroll
-    for (int d = 0; d < HS; ++d) dot = fmaf(q_s[d], static_cast<float>(krow[d]), dot);
+    for (int d = 0; d < HS; ++d) dot = fmaf(q_s[d], to_f32(krow[d]), dot);
     sc = dot * scale;
   }
   const float mx = warp_max(sc);
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __re
   for (int d = lane; d < HS; d += 32) {
     float acc = 0.f;
     for (int r = 0; r < jmax; ++r)
-      acc = fmaf(p_s[warp][r], static_cast<float>(vcache[(head + chunk * kDecPos + r) * HS + d]), acc);
+      acc = fmaf(p_s[warp][r], to_f32(vcache[(head + chunk * kDecPos + r) * HS + d]), acc);
     part[2 + d] = acc;
   }
   if (lane == 0) {
@@ -366,35 +374,37 @@ __global__ void decode_combine_kernel(OutT* __restrict__ out, const float* __res
       L += part[c * (HS + 2) + 1] * w;
       acc += part[c * (HS + 2) + 2 + d] * w;
     }
-    const float v = acc / L;
-    if constexpr (sizeof(OutT) == 2)
-      out[static_cast<size_t>(b) * C + h * HS + d] = __float2bfloat16_rn(v);
-    else
-      out[static_cast<size_t>(b) * C + h * HS + d] = v;
+    out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(acc / L);
   }
 }
 
 }  // namespace
 
-template <int HS>
-static void attention_bf16_hs(void* out, bool out_bf16, const __nv_bfloat16* qkv, int B, int T, int C, int NH,
-                              cudaStream_t s) {
+template <int HS, typename T16>
+static void attention_tc_hs(void* out, bool out16, const void* qkv, int B, int T, int C, int NH, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
   dim3 grid((T + kBQ - 1) / kBQ, NH, B);
-  if (out_bf16)
-    attn_bf16_kernel<HS, true><<<grid, kAttnThreads, 0, s>>>(out, qkv, T, C, scale_log2);
+  const uint16_t* q = static_cast<const uint16_t*>(qkv);
+  if (out16)
+    attn_tc_kernel<HS, T16, true><<<grid, kAttnThreads, 0, s>>>(out, q, T, C, scale_log2);
   else
-    attn_bf16_kernel<HS, false><<<grid, kAttnThreads, 0, s>>>(out, qkv, T, C, scale_log2);
+    attn_tc_kernel<HS, T16, false><<<grid, kAttnThreads, 0, s>>>(out, q, T, C, scale_log2);
 }
 
-int launch_attention_bf16(void* out, bool out_bf16, const __nv_bfloat16* qkv, int B, int T, int C, int NH,
-                          cudaStream_t s) {
+template <typename T16>
+static int attention_tc(void* out, bool out16, const void* qkv, int B, int T, int C, int NH, cudaStream_t s) {
   switch (C / NH) {
-    case 16: attention_bf16_hs<16>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
-    case 32: attention_bf16_hs<32>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
-    case 64: attention_bf16_hs<64>(out, out_bf16, qkv, B, T, C, NH, s); return GPT2_OK;
+    case 16: attention_tc_hs<16, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
+    case 32: attention_tc_hs<32, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
+    case 64: attention_tc_hs<64, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
   }
   return GPT2_ERR_UNSUPPORTED;
+}
+
+int launch_attention_16(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
+                        cudaStream_t s) {
+  if (op == kOpF16) return attention_tc<__half>(out, out16, qkv, B, T, C, NH, s);
+  return attention_tc<__nv_bfloat16>(out, out16, qkv, B, T, C, NH, s);
 }
 
 int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s) {
@@ -425,26 +435,36 @@ static void decode_typed(OutT* out, const E* qkv, const E* kc, const E* vc, int 
   decode_combine_kernel<OutT, HS><<<dim3(NH, B), 64, 0, s>>>(out, scratch, C, NH, nsplit * kDecWarps);
 }
 
-void launch_decode_attention_bf16(void* out, bool out_bf16, const __nv_bfloat16* qkv, const __nv_bfloat16* kcache,
-                                  const __nv_bfloat16* vcache, int B, int C, int NH, int maxT, int pos,
-                                  float* scratch, cudaStream_t s) {
-  using bf = __nv_bfloat16;
-  bf* o16 = reinterpret_cast<bf*>(out);
-  float* o32 = reinterpret_cast<float*>(out);
+template <typename E>
+static void decode_16(void* out, bool out16, const void* qkv, const void* kcache, const void* vcache, int B, int C,
+                      int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+  const E* q = static_cast<const E*>(qkv);
+  const E* kc = static_cast<const E*>(kcache);
+  const E* vc = static_cast<const E*>(vcache);
+  E* o16 = static_cast<E*>(out);
+  float* o32 = static_cast<float*>(out);
   switch (C / NH) {
     case 16:
-      if (out_bf16) decode_typed<bf, bf, 16>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<bf, float, 16>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 16>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<E, float, 16>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
       break;
     case 32:
-      if (out_bf16) decode_typed<bf, bf, 32>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<bf, float, 32>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 32>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<E, float, 32>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
       break;
     default:
-      if (out_bf16) decode_typed<bf, bf, 64>(o16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<bf, float, 64>(o32, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 64>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      else decode_typed<E, float, 64>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
       break;
   }
+}
+
+void launch_decode_attention_16(void* out, bool out16, const void* qkv, const void* kcache, const void* vcache,
+                                int op, int B, int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+  if (op == kOpF16)
+    decode_16<__half>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+  else
+    decode_16<__nv_bfloat16>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
 }
 
 void launch_decode_attention_f32(float* out, const float* qkv, const float* kcache, const float* vcache, int B,

@@ -7,8 +7,11 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "../../include/gpt2fwd.h"
 
@@ -249,6 +252,40 @@ __device__ __forceinline__ float gelu_fast(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two floats rounded to the 16-bit operand type T (bf16 or fp16), packed.
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (sizeof(T) == 2 && std::is_same<T, __half>::value)
+    return pack_half2(lo, hi);
+  else
+    return pack_bf16x2(lo, hi);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x) {
+  if constexpr (std::is_same<T, float>::value)
+    return x;
+  else if constexpr (std::is_same<T, __half>::value)
+    return __float2half_rn(x);
+  else
+    return __float2bfloat16_rn(x);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x) {
+  if constexpr (std::is_same<T, float>::value)
+    return x;
+  else if constexpr (std::is_same<T, __half>::value)
+    return __half2float(x);
+  else
+    return __bfloat162float(x);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(float* __restrict__ out,
       if (n >= N) continue;
       float v = acc[i][j] + (bias ? bias[n] : 0.f);
       float* o = out + static_cast<size_t>(m) * N + n;
-      if constexpr (kEpi == kEpiGeluBF16) {
+      if constexpr (kEpi == kEpiGelu16) {
         v = gelu_exact(v);  // fp32 mode keeps an fp32 output
       }
       if constexpr (kEpi == kEpiResidF32) v = *o + v;
@@ -74,7 +74,7 @@ void launch_gemm_simt(float* out, const float* A, const float* W, const float* b
   if (M <= 0 || N <= 0) return;
   dim3 grid((N + kT - 1) / kT, (M + kT - 1) / kT);
   switch (epi) {
-    case kEpiGeluBF16: gemm_simt_kernel<kEpiGeluBF16><<<grid, 256, 0, s>>>(out, A, W, bias, M, N, K); break;
+    case kEpiGelu16: gemm_simt_kernel<kEpiGelu16><<<grid, 256, 0, s>>>(out, A, W, bias, M, N, K); break;
     case kEpiResidF32: gemm_simt_kernel<kEpiResidF32><<<grid, 256, 0, s>>>(out, A, W, bias, M, N, K); break;
     default: gemm_simt_kernel<kEpiF32><<<grid, 256, 0, s>>>(out, A, W, bias, M, N, K); break;
   }

@@ -9,11 +9,15 @@
 //   warp 0      TMA producer: 128 x 128-byte A and 256 x 128-byte B boxes
 //               (128-byte swizzle) into a 4-stage shared-memory ring;
 //   warp 1      allocates 512 TMEM columns, and one lane issues tcgen05.mma
-//               (128 x 256 x 16 bf16 or 128 x 256 x 8 tf32 per instruction)
+//               (128 x 256 x 16 for bf16 or fp16 operands, 128 x 256 x 8
+//               for tf32, per instruction)
 //               into one of two 128 x 256 fp32 TMEM accumulators;
 //   warps 2-5   epilogue: tcgen05.ld 32 columns of their 32 TMEM lanes,
 //               add bias, apply GELU or add the residual (TMA-loaded), stage
-//               the tile in swizzled shared memory and TMA-store it.
+//               the tile in swizzled shared memory and TMA-store it.  The
+//               LM-head epilogue also leaves, per row and per 256-column
+//               tile, the maximum and the sum of exp(logit - maximum) over
+//               the real vocabulary, so that the softmax needs one pass.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Tiles are walked M-fastest so that concurrently running CTAs share
 // one weight tile (B) while the activation matrix (A) stays in L2.
@@ -50,11 +54,13 @@ struct SmemLayout {
 };
 static_assert(SmemLayout::alloc <= 232448, "shared memory budget");
 
-template <int kEpi, bool kTF32>
+__host__ __device__ constexpr int gridDim_n(int N) { return (N + kBN - 1) / kBN; }
+
+template <int kEpi, int kOp>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
-                   int K, int tiles_m, int num_tiles) {
+                   int K, int tiles_m, int num_tiles, float2* __restrict__ row_stats, int V) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bar_off);
@@ -69,10 +75,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr bool kTF32 = (kOp == kOpTF32);
+  using Out16 = typename std::conditional<kOp == kOpF16, __half, __nv_bfloat16>::type;
   constexpr int kElemBytes = kTF32 ? 4 : 2;
   constexpr int kBKElems = kRowBytes / kElemBytes;  // K elements per stage
   constexpr int kMmaK = 32 / kElemBytes;            // K per instruction (32 bytes)
-  constexpr uint32_t kIdesc = make_idesc(kTF32 ? 2u : 1u, kBM, kBN);
+  // operand format field: fp16 0, bf16 1 (kind::f16), tf32 2 (kind::tf32)
+  constexpr uint32_t kIdesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kBM, kBN);
   const int num_kb = (K + kBKElems - 1) / kBKElems;
 
   if (threadIdx.x == 0) {
@@ -210,9 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = m_blk * kBM + row_in_tile;
       const int n0 = n_blk * kBN;
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
-      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32);
+      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
       constexpr int kChunkCols = kOutF32 ? 32 : 64;  // 128 bytes of output per row
       bool ok = true;
+      // logits epilogue: this row's running max and sum of exp over the
+      // tile's columns below V
+      float run_m = -INFINITY, run_s = 0.f;
 #pragma unroll 1
       for (int ch = 0; ch < kBN / kChunkCols; ++ch) {
         const int buf = chunk_ctr & 1;
@@ -257,6 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (col0 + j < N) v[j] += __ldg(bias + col0 + j);
           }
         }
+        if constexpr (kEpi == kEpiLogits) {
+          float cmax = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < V) cmax = fmaxf(cmax, v[j]);
+          if (cmax != -INFINITY) {
+            const float m_new = fmaxf(run_m, cmax);
+            float acc = run_s * __expf(run_m - m_new);  // 0 while run_m is -inf
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < V) acc += __expf(v[j] - m_new);
+            run_m = m_new;
+            run_s = acc;
+          }
+        }
         const int sw = lane & 7;
         uint8_t* my_row = stg + lane * 128;
         if constexpr (kOutF32) {
@@ -283,13 +310,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               a[e] = v[8 * j + e];
-              if constexpr (kEpi == kEpiGeluBF16) a[e] = gelu_fast(a[e]);
+              if constexpr (kEpi == kEpiGelu16) a[e] = gelu_fast(a[e]);
             }
             uint4 p;
-            p.x = pack_bf16x2(a[0], a[1]);
-            p.y = pack_bf16x2(a[2], a[3]);
-            p.z = pack_bf16x2(a[4], a[5]);
-            p.w = pack_bf16x2(a[6], a[7]);
+            p.x = pack2<Out16>(a[0], a[1]);
+            p.y = pack2<Out16>(a[2], a[3]);
+            p.z = pack2<Out16>(a[4], a[5]);
+            p.w = pack2<Out16>(a[6], a[7]);
             *reinterpret_cast<uint4*>(my_row + ((j ^ sw) << 4)) = p;
           }
         }
@@ -301,6 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++chunk_ctr;
         if (!ok) break;
+      }
+      if constexpr (kEpi == kEpiLogits) {
+        const int row = m0 + lane;
+        if (row < M) row_stats[static_cast<size_t>(row) * gridDim_n(N) + n_blk] = make_float2(run_m, run_s);
       }
       // this warp is done reading the accumulator
       tc_fence_before();
@@ -357,25 +388,29 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
   return r == CUDA_SUCCESS;
 }
 
-template <int kEpi, bool kTF32>
-int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s) {
+template <int kEpi, int kOp>
+int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
+                 float2* row_stats = nullptr, int V = 0) {
   CUtensorMap ta, tb, to;
-  const CUtensorMapDataType dt_in = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  constexpr bool kTF32 = (kOp == kOpTF32);
+  const CUtensorMapDataType dt16 =
+      kOp == kOpF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt_in = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt16;
   const int eb = kTF32 ? 4 : 2;
   const int bk = kRowBytes / eb;
-  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32);
+  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
   if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
   if (!make_map(&tb, B, dt_in, eb, N, K, bk, kBN)) return GPT2_ERR_CUDA;
   if (kOutF32) {
     if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 32, 32)) return GPT2_ERR_CUDA;
   } else {
-    if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, M, N, 64, 32)) return GPT2_ERR_CUDA;
+    if (!make_map(&to, out, dt16, 2, M, N, 64, 32)) return GPT2_ERR_CUDA;
   }
   const int tiles_m = (M + kBM - 1) / kBM;
   const int tiles_n = (N + kBN - 1) / kBN;
   const int num_tiles = tiles_m * tiles_n;
   const int grid = num_tiles < num_sms() ? num_tiles : num_sms();
-  auto kern = gemm_tc_kernel<kEpi, kTF32>;
+  auto kern = gemm_tc_kernel<kEpi, kOp>;
   static bool attr_set[kMaxDevices] = {};  // per template instance and device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
@@ -384,29 +419,53 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
       return GPT2_ERR_CUDA;
     attr_set[dev] = true;
   }
-  kern<<<grid, kThreads, SmemLayout::alloc, s>>>(ta, tb, to, bias, M, N, K, tiles_m, num_tiles);
+  kern<<<grid, kThreads, SmemLayout::alloc, s>>>(ta, tb, to, bias, M, N, K, tiles_m, num_tiles, row_stats, V);
   return cudaPeekAtLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi,
-                   bool ab_bf16, cudaStream_t s) {
+int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
+                   cudaStream_t s) {
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
-  if (ab_bf16) {
-    switch (epi) {
-      case kEpiF32: return launch_typed<kEpiF32, false>(out, A, B, bias, M, N, K, s);
-      case kEpiBF16: return launch_typed<kEpiBF16, false>(out, A, B, bias, M, N, K, s);
-      case kEpiGeluBF16: return launch_typed<kEpiGeluBF16, false>(out, A, B, bias, M, N, K, s);
-      case kEpiResidF32: return launch_typed<kEpiResidF32, false>(out, A, B, bias, M, N, K, s);
-    }
-  } else {
-    switch (epi) {
-      case kEpiF32: return launch_typed<kEpiF32, true>(out, A, B, bias, M, N, K, s);
-      case kEpiResidF32: return launch_typed<kEpiResidF32, true>(out, A, B, bias, M, N, K, s);
-    }
+  switch (op) {
+    case kOpBF16:
+      switch (epi) {
+        case kEpiF32: return launch_typed<kEpiF32, kOpBF16>(out, A, B, bias, M, N, K, s);
+        case kEpiOut16: return launch_typed<kEpiOut16, kOpBF16>(out, A, B, bias, M, N, K, s);
+        case kEpiGelu16: return launch_typed<kEpiGelu16, kOpBF16>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpBF16>(out, A, B, bias, M, N, K, s);
+      }
+      break;
+    case kOpF16:
+      switch (epi) {
+        case kEpiF32: return launch_typed<kEpiF32, kOpF16>(out, A, B, bias, M, N, K, s);
+        case kEpiOut16: return launch_typed<kEpiOut16, kOpF16>(out, A, B, bias, M, N, K, s);
+        case kEpiGelu16: return launch_typed<kEpiGelu16, kOpF16>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpF16>(out, A, B, bias, M, N, K, s);
+      }
+      break;
+    case kOpTF32:
+      switch (epi) {
+        case kEpiF32: return launch_typed<kEpiF32, kOpTF32>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpTF32>(out, A, B, bias, M, N, K, s);
+      }
+      break;
   }
   return GPT2_ERR_UNSUPPORTED;
 }
+
+int launch_gemm_logits(float* logits, float2* row_stats, const void* A, const void* B, int M, int N, int K, int V,
+                       int op, cudaStream_t s) {
+  if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
+  switch (op) {
+    case kOpBF16: return launch_typed<kEpiLogits, kOpBF16>(logits, A, B, nullptr, M, N, K, s, row_stats, V);
+    case kOpF16: return launch_typed<kEpiLogits, kOpF16>(logits, A, B, nullptr, M, N, K, s, row_stats, V);
+    case kOpTF32: return launch_typed<kEpiLogits, kOpTF32>(logits, A, B, nullptr, M, N, K, s, row_stats, V);
+  }
+  return GPT2_ERR_UNSUPPORTED;
+}
+
+int gemm_tiles_n(int N) { return gridDim_n(N); }
 
 }  // namespace gpt2

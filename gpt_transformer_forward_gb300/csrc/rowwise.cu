@@ -1,6 +1,6 @@
 // rowwise.cu -- the HBM-bound steps of the GPT-2 forward pass: encoder,
 // LayerNorm, GELU, residual add, vocabulary softmax, argmax, plus the fp32
-// to bf16 conversions and the KV-cache writes the forward pass needs.
+// to 16-bit (bf16 or fp16) conversions and the KV-cache writes the forward pass needs.
 //
 // Every kernel streams its rows with 128-bit loads and stores where the
 // layout allows; row reductions are warp-shuffle (LayerNorm: one warp per
@@ -113,8 +113,8 @@ __global__ void __launch_bounds__(256) layernorm_warp_kernel(OutT* __restrict__ 
       reinterpret_cast<float4*>(out + static_cast<size_t>(row) * C)[c4] = make_float4(y0, y1, y2, y3);
     } else {
       uint2 p;
-      p.x = pack_bf16x2(y0, y1);
-      p.y = pack_bf16x2(y2, y3);
+      p.x = pack2<OutT>(y0, y1);
+      p.y = pack2<OutT>(y2, y3);
       reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * C)[c4] = p;
     }
   }
@@ -155,10 +155,7 @@ __global__ void __launch_bounds__(256) layernorm_block_kernel(OutT* __restrict__
   const float rstd = rsqrtf(block_sum(q) / C + 1e-5f);
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
     const float y = (x[c] - mean) * rstd * w[c] + b[c];
-    if constexpr (sizeof(OutT) == 4)
-      out[static_cast<size_t>(row) * C + c] = y;
-    else
-      out[static_cast<size_t>(row) * C + c] = __float2bfloat16_rn(y);
+    out[static_cast<size_t>(row) * C + c] = from_f32<OutT>(y);
   }
   if (threadIdx.x == 0) {
     if (mean_out) mean_out[row] = mean;
@@ -187,10 +184,13 @@ void launch_layernorm_f32(float* out, float* mean, float* rstd, const float* inp
   layernorm_dispatch<float>(out, mean, rstd, inp, w, b, N, C, s);
 }
 
-void launch_layernorm_bf16(__nv_bfloat16* out, const float* inp, const float* w, const float* b, int N, int C,
-                           cudaStream_t s) {
-  layernorm_dispatch<__nv_bfloat16>(out, nullptr, nullptr, inp, w, b, N, C, s);
+template <typename T>
+void launch_layernorm_16(T* out, const float* inp, const float* w, const float* b, int N, int C, cudaStream_t s) {
+  layernorm_dispatch<T>(out, nullptr, nullptr, inp, w, b, N, C, s);
 }
+template void launch_layernorm_16<__nv_bfloat16>(__nv_bfloat16*, const float*, const float*, const float*, int, int,
+                                                 cudaStream_t);
+template void launch_layernorm_16<__half>(__half*, const float*, const float*, const float*, int, int, cudaStream_t);
 
 // ------------------------------------------------------- GELU and residual
 __global__ void gelu_kernel(float4* __restrict__ out, const float4* __restrict__ inp, long long n4) {
@@ -247,64 +247,110 @@ void launch_residual(float* out, const float* a, const float* b, int n, cudaStre
 // ---------------------------------------------------------------- softmax
 constexpr int kSoftmaxThreads = 1024;
 
-// One block per row: an online max/sum pass over the row, then the
-// normalised write pass.
-__global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float* __restrict__ probs,
-                                                                        const float* __restrict__ logits, int V,
-                                                                        int Vp) {
+// Combines two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void merge_stats(float& m, float& s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) return;  // both empty
+  s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
+  m = mm;
+}
+
+// Block-wide reduction of (max, sum) pairs; every thread gets the result.
+__device__ __forceinline__ float2 block_merge_stats(float m, float s) {
   __shared__ float red_m[32], red_s[32];
-  __shared__ float bm, bs;
-  const size_t row = blockIdx.x;
-  const float* lrow = logits + row * Vp;
-  float* prow = probs + row * Vp;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  float m = -INFINITY, s = 0.f;
-  for (int c = tid; c < V; c += blockDim.x) {
-    const float x = lrow[c];
-    if (x > m) {
-      s = s * __expf(m - x) + 1.f;
-      m = x;
-    } else {
-      s += __expf(x - m);
-    }
-  }
+  __shared__ float2 result;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    const float mm = fmaxf(m, m2);
-    s = (mm == -INFINITY) ? 0.f : s * __expf(m - mm) + s2 * __expf(m2 - mm);
-    m = mm;
-  }
+  for (int o = 16; o > 0; o >>= 1)
+    merge_stats(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
   if (lane == 0) {
     red_m[wid] = m;
     red_s[wid] = s;
   }
   __syncthreads();
   if (wid == 0) {
-    m = red_m[lane];
-    s = red_s[lane];
+    m = lane < nw ? red_m[lane] : -INFINITY;
+    s = lane < nw ? red_s[lane] : 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      const float mm = fmaxf(m, m2);
-      s = (mm == -INFINITY) ? 0.f : s * __expf(m - mm) + s2 * __expf(m2 - mm);
-      m = mm;
-    }
-    if (lane == 0) {
-      bm = m;
-      bs = s;
-    }
+    for (int o = 16; o > 0; o >>= 1)
+      merge_stats(m, s, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, s, o));
+    if (lane == 0) result = make_float2(m, s);
   }
   __syncthreads();
-  const float mx = bm, inv = 1.0f / bs;
-  for (int c = tid; c < Vp; c += blockDim.x) prow[c] = (c < V) ? __expf(lrow[c] - mx) * inv : 0.f;
+  return result;
+}
+
+// Writes probs for one row given its max and 1/sum: float4 streaming.
+__device__ __forceinline__ void softmax_write_row(float4* __restrict__ prow, const float4* __restrict__ lrow, int V,
+                                                  int Vp4, float mx, float inv) {
+  for (int c4 = threadIdx.x; c4 < Vp4; c4 += blockDim.x) {
+    const float4 x = __ldcs(lrow + c4);
+    const int c = c4 * 4;
+    float4 p;
+    p.x = (c + 0 < V) ? __expf(x.x - mx) * inv : 0.f;
+    p.y = (c + 1 < V) ? __expf(x.y - mx) * inv : 0.f;
+    p.z = (c + 2 < V) ? __expf(x.z - mx) * inv : 0.f;
+    p.w = (c + 3 < V) ? __expf(x.w - mx) * inv : 0.f;
+    __stcs(prow + c4, p);
+  }
+}
+
+// Standalone softmax, one block per row: an online (max, sum) pass over the
+// row, then the normalised write pass.  The second pass re-reads a row the
+// block has just read; the rows in flight (a few MB) stay in L2, so HBM sees
+// about one read and one write per element.
+__global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float4* __restrict__ probs,
+                                                                        const float4* __restrict__ logits, int V,
+                                                                        int Vp4) {
+  const size_t row = blockIdx.x;
+  const float4* lrow = logits + row * Vp4;
+  float m = -INFINITY, s = 0.f;
+  for (int c4 = threadIdx.x; c4 < Vp4; c4 += blockDim.x) {
+    const float4 x = lrow[c4];
+    const int c = c4 * 4;
+    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (c + k >= V) continue;
+      if (xs[k] > m) {
+        s = s * __expf(m - xs[k]) + 1.f;
+        m = xs[k];
+      } else {
+        s += __expf(xs[k] - m);
+      }
+    }
+  }
+  const float2 r = block_merge_stats(m, s);
+  softmax_write_row(probs + row * Vp4, lrow, V, Vp4, r.x, 1.0f / r.y);
 }
 
 void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s) {
-  // The second pass re-reads a row the same block has just read; with one
-  // row per block the rows in flight (a few MB) stay in L2, so HBM sees one
-  // read and one write per element.
-  softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(probs, logits, V, Vp);
+  softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
+                                                     reinterpret_cast<const float4*>(logits), V, Vp / 4);
+}
+
+// Softmax after the LM-head GEMM: the row's (max, sum) come from the
+// per-tile statistics the GEMM epilogue left, so the logits are read once.
+constexpr int kStatsThreads = 256;
+__global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(float4* __restrict__ probs,
+                                                                           const float4* __restrict__ logits,
+                                                                           const float2* __restrict__ stats,
+                                                                           int tiles, int V, int Vp4) {
+  const size_t row = blockIdx.x;
+  float m = -INFINITY, s = 0.f;
+  for (int i = threadIdx.x; i < tiles; i += blockDim.x) {
+    const float2 p = stats[row * tiles + i];
+    merge_stats(m, s, p.x, p.y);
+  }
+  const float2 r = block_merge_stats(m, s);
+  softmax_write_row(probs + row * Vp4, logits + row * Vp4, V, Vp4, r.x, 1.0f / r.y);
+}
+
+void launch_softmax_from_stats(float* probs, const float* logits, const float2* row_stats, int tiles, int N, int V,
+                               int Vp, cudaStream_t s) {
+  softmax_from_stats_kernel<<<N, kStatsThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
+                                                        reinterpret_cast<const float4*>(logits), row_stats, tiles, V,
+                                                        Vp / 4);
 }
 
 // ----------------------------------------------------------------- argmax
@@ -360,23 +406,27 @@ void launch_argmax(int* next, const float* logits, int B, int V, int Vp, cudaStr
 }
 
 // ------------------------------------------------------------ conversions
-__global__ void f32_to_bf16_kernel(__nv_bfloat16* __restrict__ out, const float* __restrict__ in, long long n) {
+template <typename T>
+__global__ void f32_to_16_kernel(T* __restrict__ out, const float* __restrict__ in, long long n) {
   const long long n4 = n / 4;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const float4 x = reinterpret_cast<const float4*>(in)[i];
     uint2 p;
-    p.x = pack_bf16x2(x.x, x.y);
-    p.y = pack_bf16x2(x.z, x.w);
+    p.x = pack2<T>(x.x, x.y);
+    p.y = pack2<T>(x.z, x.w);
     reinterpret_cast<uint2*>(out)[i] = p;
   }
   const long long i = n4 * 4 + blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (blockIdx.x == 0 && i < n) out[i] = __float2bfloat16_rn(in[i]);
+  if (blockIdx.x == 0 && i < n) out[i] = from_f32<T>(in[i]);
 }
 
-void launch_f32_to_bf16(__nv_bfloat16* out, const float* in, long long n, cudaStream_t s) {
-  f32_to_bf16_kernel<<<stream_grid(n / 4 + 1, 256), 256, 0, s>>>(out, in, n);
+template <typename T>
+void launch_f32_to_16(T* out, const float* in, long long n, cudaStream_t s) {
+  f32_to_16_kernel<T><<<stream_grid(n / 4 + 1, 256), 256, 0, s>>>(out, in, n);
 }
+template void launch_f32_to_16<__nv_bfloat16>(__nv_bfloat16*, const float*, long long, cudaStream_t);
+template void launch_f32_to_16<__half>(__half*, const float*, long long, cudaStream_t);
 
 // ----------------------------------------------------------- KV cache
 // Copies keys and values of rows [0, T) of each sequence from the QKV buffer
@@ -410,10 +460,10 @@ void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, in
   kv_store_kernel<float><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
 }
 
-void launch_kv_store_bf16(__nv_bfloat16* cache, const __nv_bfloat16* qkv, int B, int T, int C, int NH, int maxT,
-                          int pos0, cudaStream_t s) {
+void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
+                        cudaStream_t s) {
   const long long total = 2LL * B * T * C / 8;
-  kv_store_kernel<__nv_bfloat16><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
+  kv_store_kernel<uint16_t><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
 }
 
 }  // namespace gpt2

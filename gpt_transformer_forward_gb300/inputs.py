@@ -176,6 +176,21 @@ def make_normal(seed: int, shape, std: float = 1.0, dtype=np.float32) -> np.ndar
     return (std * normal_stream(seed, n)).astype(dtype).reshape(shape)
 
 
+def on_grid(a: np.ndarray, fmt: str) -> np.ndarray:
+    """float32 copy of `a` with every value rounded (to nearest, ties to even)
+    onto the grid of a narrower format, "bf16", "fp16" or "tf32", so that a
+    conversion to that format is exact.  Test-input preparation only."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    if fmt == "fp16":
+        return a.astype(np.float16).astype(np.float32)
+    drop = {"bf16": 16, "tf32": 13}[fmt]  # low mantissa bits removed
+    u = a.view(np.uint32).astype(np.uint64)
+    half = np.uint64(1 << (drop - 1))
+    lsb = (u >> np.uint64(drop)) & np.uint64(1)
+    u = ((u + half - np.uint64(1) + lsb) >> np.uint64(drop)) << np.uint64(drop)
+    return u.astype(np.uint32).view(np.float32)
+
+
 def workload_inputs(w: Workload, init: str = "gpt2"):
     """(params, tokens) for a named workload."""
     params = make_params(w.cfg, w.weight_seed, init)

@@ -62,13 +62,18 @@ typedef struct {
 
 /* Operand precision of the matrix products (GEMMs and attention).
  *   GPT2_FP32: fp32 CUDA-core arithmetic throughout (reference-grade mode).
- *   GPT2_TF32: tensor cores (tcgen05 kind::tf32) on fp32 operands.
- *   GPT2_BF16: tensor cores (tcgen05 kind::f16) on bf16 operands; operand
- *              buffers internal to gpt2_forward are stored as bf16 (the
- *              tensor cores would round them to bf16 anyway); the residual
- *              stream, logits and probabilities stay fp32.
- * Accumulation is fp32 in every mode. */
-typedef enum { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2 } GPT2Precision;
+ *   GPT2_TF32: tensor cores (tcgen05 kind::tf32) on fp32 operands; the
+ *              attention runs the bf16 tensor-core kernel.
+ *   GPT2_BF16: tensor cores (tcgen05 kind::f16) on bf16 operands.
+ *   GPT2_FP16: tensor cores (tcgen05 kind::f16) on fp16 operands: the same
+ *              rate as bf16 with 8x finer rounding (11 significant bits
+ *              against 8) and a range of +-65504, ample for GPT-2's
+ *              normalised activations and 0.02-scale weights.
+ * In the 16-bit modes the operand buffers internal to gpt2_forward (and
+ * the KV cache) hold the 16-bit type, since the tensor cores would round
+ * them to it anyway; the residual stream, logits and probabilities stay
+ * fp32.  Accumulation is fp32 in every mode. */
+typedef enum { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2, GPT2_FP16 = 3 } GPT2Precision;
 
 enum {
   GPT2_OK = 0,
@@ -106,7 +111,8 @@ GPT2_API int layernorm_forward(float* out, float* mean, float* rstd, const float
                       int C, void* stream);
 
 /* Scratch bytes matmul_forward needs for this shape and precision (0 for
- * GPT2_FP32 and GPT2_TF32; the bf16 copies of inp and W for GPT2_BF16). */
+ * GPT2_FP32 and GPT2_TF32; the 16-bit copies of inp and W for GPT2_BF16 and
+ * GPT2_FP16). */
 GPT2_API size_t matmul_workspace_size(int N, int C, int OC, int precision);
 
 /* MatMul with bias [ECE408 "MatMul"; llm.c GEMMs]:
@@ -118,8 +124,8 @@ GPT2_API size_t matmul_workspace_size(int N, int C, int OC, int precision);
 GPT2_API int matmul_forward(float* out, const float* inp, const float* W, const float* bias, int N, int C, int OC,
                    int precision, void* workspace, size_t ws_bytes, void* stream);
 
-/* Scratch bytes attention_forward needs (the bf16 copy of qkv in GPT2_BF16
- * and GPT2_TF32 modes, 0 in GPT2_FP32). */
+/* Scratch bytes attention_forward needs (the 16-bit copy of qkv in the
+ * tensor-core modes, 0 in GPT2_FP32). */
 GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
 
 /* Causal multi-head attention including its softmax [ECE408 "Attention
@@ -129,9 +135,10 @@ GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
  *   [h*hs, (h+1)*hs) of each; S = q k^T / sqrt(hs) with keys j <= t only;
  *   out[b,t, h*hs:(h+1)*hs] = softmax_j(S[t, :]) v.
  * out [B,T,C], qkv [B,T,3C].  Requires hs in {16, 32, 64}.  GPT2_FP32
- * runs fp32 CUDA-core arithmetic; GPT2_TF32 and GPT2_BF16 both run the bf16
- * tensor-core kernel (Q, K, V and the probabilities rounded to bf16, fp32
- * accumulation) on a bf16 copy of qkv made in `workspace`. */
+ * runs fp32 CUDA-core arithmetic; the tensor-core modes round Q, K, V and
+ * the probabilities to the 16-bit type (bf16 for GPT2_TF32 and GPT2_BF16,
+ * fp16 for GPT2_FP16) of a copy of qkv made in `workspace`, and accumulate
+ * in fp32. */
 GPT2_API int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH, int precision, void* workspace,
                       size_t ws_bytes, void* stream);
 
@@ -161,13 +168,14 @@ GPT2_API int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, v
  * fcb[L,4C] fcprojw[L,C,4C] fcprojb[L,C] lnfw[C] lnfb[C]. */
 GPT2_API size_t gpt2_num_parameters(const GPT2Config* cfg);
 
-/* Bytes of the packed weight buffer for a precision: bf16 copies of the
- * matrices (wte, qkvw, attprojw, fcw, fcprojw) for GPT2_BF16, 0 otherwise. */
+/* Bytes of the packed weight buffer for a precision: 16-bit copies of the
+ * matrices (wte, qkvw, attprojw, fcw, fcprojw) for GPT2_BF16 and
+ * GPT2_FP16, 0 otherwise. */
 GPT2_API size_t gpt2_packed_weights_size(const GPT2Config* cfg, int precision);
 
 /* Fills `packed` (caller-owned, gpt2_packed_weights_size bytes) from the
  * fp32 parameters.  Run once per set of weights; gpt2_forward and
- * gpt2_decode_step read it in GPT2_BF16 mode. */
+ * gpt2_decode_step read it in the 16-bit modes. */
 GPT2_API int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, void* packed, size_t bytes, int precision,
                          void* stream);
 
@@ -176,8 +184,8 @@ GPT2_API int gpt2_prepare_weights(const GPT2Config* cfg, const float* params, vo
 GPT2_API size_t gpt2_workspace_size(const GPT2Config* cfg, int B, int T, int precision);
 
 /* Bytes of a KV cache for B sequences: layout [L][2][B][NH][maxT][hs]
- * (keys then values per layer), fp32 in GPT2_FP32 / GPT2_TF32, bf16 in
- * GPT2_BF16. */
+ * (keys then values per layer), fp32 in GPT2_FP32 / GPT2_TF32, the 16-bit
+ * type in GPT2_BF16 / GPT2_FP16. */
 GPT2_API size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision);
 
 /* The GPT-2 forward pass (pre-LayerNorm blocks) over B sequences of T
@@ -188,8 +196,8 @@ GPT2_API size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision);
  *   logits = LN_f(x) wte^T (tied, no bias; all Vp columns);
  *   probs  = softmax over the first V columns (when probs != NULL).
  * params: flat fp32 buffer (gpt2_num_parameters values, never written);
- * packed: output of gpt2_prepare_weights (required for GPT2_BF16, else
- * ignored); tok [B,T] int32; logits [B,T,Vp]; probs [B,T,Vp] or NULL;
+ * packed: output of gpt2_prepare_weights (required in the 16-bit modes,
+ * else ignored); tok [B,T] int32; logits [B,T,Vp]; probs [B,T,Vp] or NULL;
  * kvcache: NULL, or a cache of gpt2_kvcache_size(cfg, B, precision) bytes
  * whose positions [0, T) are written (the prefill of decoding);
  * workspace of gpt2_workspace_size(cfg, B, T, precision) bytes.

@@ -2,8 +2,12 @@
 
 Shapes cover T = 1, T below, at and past one 64-row tile, ragged tails,
 the GPT-2 width (12 heads of 64) at T = 1024, and head sizes 16, 32 and 64.
-Tolerances: fp32 CUDA cores 1e-5 absolute (outputs are convex combinations
-of O(1) values); bf16 tensor cores 2e-2 absolute."""
+Q, K and V are drawn at the workload's scale (std 0.55: a LayerNorm output
+times 0.02-scale weights over 768 channels).  Tolerances: tensor cores 2e-2
+absolute (the bar for tensor-core results); fp32 CUDA cores 1e-5 absolute.
+Inputs drawn on the 16-bit grid at std 1 (and with peaked scores) isolate
+the kernel's own rounding, that of the probabilities P to the 16-bit type:
+|err| <= u * max|v| with unit roundoff u = 2^-8 (bf16) or 2^-11 (fp16)."""
 import numpy as np
 import pytest
 import torch
@@ -15,7 +19,9 @@ from gpt_transformer_forward_gb300 import inputs
 from gpu_helpers import assert_close, dev, host, need_gpu, no_device_error
 
 pytestmark = pytest.mark.gpu
-TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_TF32: 2e-2, ab.GPT2_FP32: 1e-5}
+TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_FP16: 2e-2, ab.GPT2_TF32: 2e-2, ab.GPT2_FP32: 1e-5}
+UNIT = {ab.GPT2_BF16: 2.0 ** -8, ab.GPT2_FP16: 2.0 ** -11}
+GRID = {ab.GPT2_BF16: "bf16", ab.GPT2_FP16: "fp16"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -23,38 +29,50 @@ def _gpu():
     need_gpu()
 
 
-def run_attention(B, T, C, NH, precision, seed=0, qk_std=1.0):
-    qkv = inputs.make_normal(400 + seed, (B, T, 3 * C), 1.0)
+def run_attention(B, T, C, NH, precision, seed=0, std=0.55, qk_std=1.0, grid=None):
+    qkv = inputs.make_normal(400 + seed, (B, T, 3 * C), std)
     qkv[..., :2 * C] *= qk_std
+    if grid is not None:
+        qkv = inputs.on_grid(qkv, grid)
     out = torch.full((B, T, C), float("nan"), device="cuda")
     wsz = ab.attention_workspace_size(B, T, C, precision)
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
     ab.attention_forward(out, dev(qkv), B, T, C, NH, precision, ws, wsz)
     no_device_error()
-    return host(out), oracle.attention(qkv, NH)
+    return host(out), oracle.attention(qkv, NH), qkv
 
 
 SHAPES = [(1, 1, 64, 4), (2, 32, 64, 4), (1, 64, 128, 2), (2, 65, 128, 4), (1, 200, 768, 12),
           (1, 130, 256, 8), (2, 1024, 768, 12), (3, 97, 192, 12)]
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP32])
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16, ab.GPT2_TF32, ab.GPT2_FP32])
 @pytest.mark.parametrize("B,T,C,NH", SHAPES)
 def test_attention(B, T, C, NH, precision):
-    got, ref = run_attention(B, T, C, NH, precision)
+    got, ref, _ = run_attention(B, T, C, NH, precision)
     assert_close(got, ref, atol=TOL[precision], what=f"attention {B}x{T}x{C}/{NH} p{precision}")
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP32])
-def test_attention_peaked_scores(precision):
-    # large scores: a few keys dominate each row, exercising the running max
-    got, ref = run_attention(1, 300, 768, 12, precision, seed=3, qk_std=3.0)
-    assert_close(got, ref, atol=TOL[precision], what="peaked")
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16])
+@pytest.mark.parametrize("qk_std", [1.0, 3.0])
+@pytest.mark.parametrize("B,T,C,NH", [(2, 65, 128, 4), (1, 300, 768, 12), (1, 1024, 768, 12), (2, 40, 64, 4)])
+def test_attention_on_grid(B, T, C, NH, precision, qk_std):
+    # qk_std 3: a few keys dominate each row, exercising the running max
+    got, ref, qkv = run_attention(B, T, C, NH, precision, seed=3, std=1.0, qk_std=qk_std, grid=GRID[precision])
+    vmax = np.abs(qkv[..., 2 * C:]).max()
+    assert_close(got, ref, atol=UNIT[precision] * vmax, what=f"on-grid attention qk_std {qk_std}")
+
+
+def test_attention_fp32_peaked():
+    # scores of magnitude up to ~40: their fp32 rounding (ulp 3.8e-6) moves
+    # each probability by a few 1e-6 relative, times |v| <= ~4
+    got, ref, _ = run_attention(1, 300, 768, 12, ab.GPT2_FP32, seed=3, std=1.0, qk_std=3.0)
+    assert_close(got, ref, atol=5e-5, what="peaked fp32")
 
 
 def test_attention_causal_bitwise():
     B, T, C, NH = 1, 150, 768, 12
-    qkv = inputs.make_normal(9, (B, T, 3 * C))
+    qkv = inputs.make_normal(9, (B, T, 3 * C), 0.55)
     ws = torch.empty(ab.attention_workspace_size(B, T, C, ab.GPT2_BF16), dtype=torch.uint8, device="cuda")
     outs = []
     for q in (qkv, np.concatenate([qkv[:, :100], inputs.make_normal(10, (B, T - 100, 3 * C))], axis=1)):

@@ -3,8 +3,12 @@ oracle, in each precision mode, on GPT-2-scale values: activations N(0, 1)
 as a LayerNorm produces them, weights N(0, 0.02), biases N(0, 0.02).
 
 Tolerances: bf16 operands 2e-2 absolute (the bar for tensor-core results);
-tf32 operands 2e-3 absolute; fp32 CUDA cores 1e-5 absolute (outputs are of
-order 1, fp32 accumulation over K <= 3072 terms)."""
+fp16 operands (unit roundoff 2^-11) and tf32 operands (10 stored bits,
+truncated) 5e-3 absolute; fp32 CUDA cores 1e-5 * max(1, |ref|) (fp32
+accumulation over K <= 3072 terms).  Inputs drawn on the 16-bit
+grid are converted exactly, so there the tensor-core result must equal the
+oracle to fp32-accumulation accuracy (1e-4): any fault in the TMA, swizzle,
+descriptor or TMEM path shows up as an O(1) error."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +20,8 @@ from gpt_transformer_forward_gb300 import inputs
 from gpu_helpers import assert_close, dev, host, need_gpu, no_device_error
 
 pytestmark = pytest.mark.gpu
-TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_TF32: 2e-3, ab.GPT2_FP32: 1e-5}
+TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_FP16: 5e-3, ab.GPT2_TF32: 5e-3, ab.GPT2_FP32: 1e-5}
+ALL = [ab.GPT2_BF16, ab.GPT2_FP16, ab.GPT2_TF32, ab.GPT2_FP32]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -24,10 +29,12 @@ def _gpu():
     need_gpu()
 
 
-def run_matmul(N, C, OC, precision, bias=True, seed=0):
+def run_matmul(N, C, OC, precision, bias=True, seed=0, grid=None):
     x = inputs.make_normal(100 + seed, (N, C), 1.0)
     W = inputs.make_normal(200 + seed, (OC, C), 0.02)
     b = inputs.make_normal(300 + seed, (OC,), 0.02) if bias else None
+    if grid is not None:
+        x, W = inputs.on_grid(x, grid), inputs.on_grid(W, grid)
     out = torch.full((N, OC), float("nan"), device="cuda")
     wsz = ab.matmul_workspace_size(N, C, OC, precision)
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
@@ -50,14 +57,25 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_TF32, ab.GPT2_FP32])
+@pytest.mark.parametrize("precision", ALL)
 @pytest.mark.parametrize("N,C,OC", SHAPES)
 def test_matmul(N, C, OC, precision):
     got, ref = run_matmul(N, C, OC, precision)
-    assert_close(got, ref, atol=TOL[precision], what=f"matmul {N}x{C}x{OC} p{precision}")
+    if precision == ab.GPT2_FP32:  # fp32 rounding: relative to max(1, |ref|)
+        assert_close(got, ref, rtol=TOL[precision], floor=1.0, what=f"matmul {N}x{C}x{OC} fp32")
+    else:
+        assert_close(got, ref, atol=TOL[precision], what=f"matmul {N}x{C}x{OC} p{precision}")
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_TF32])
+@pytest.mark.parametrize("precision,grid", [(ab.GPT2_BF16, "bf16"), (ab.GPT2_FP16, "fp16"),
+                                            (ab.GPT2_TF32, "tf32")])
+@pytest.mark.parametrize("N,C,OC", [(300, 768, 2304), (128 * 20, 256, 256 * 20), (64, 3072, 50304), (7, 64, 40)])
+def test_matmul_on_grid_is_exact_to_fp32_accumulation(N, C, OC, precision, grid):
+    got, ref = run_matmul(N, C, OC, precision, seed=9, grid=grid)
+    assert_close(got, ref, atol=1e-4, what=f"on-grid matmul {N}x{C}x{OC} {grid}")
+
+
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16, ab.GPT2_TF32])
 def test_matmul_no_bias_and_persistent_tiles(precision):
     # 2 * 148 + tiles: every CTA walks several tiles through both TMEM buffers
     got, ref = run_matmul(128 * 20, 256, 256 * 20, precision, bias=False, seed=5)
