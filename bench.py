@@ -70,6 +70,21 @@ def stage_costs(cfg, B, T, act_bytes=2):
     }
 
 
+def measured_traffic(stage):
+    """DRAM bytes per launch of a stage's kernel from the committed ncu
+    record, or None when absent or taken on a different kernel source."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[stage]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return rec["bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def load_peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -296,7 +311,8 @@ def run_ours(args):
         achieved = nbytes / launches / (per_launch_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = measured_traffic(dom) if args.workload == "gpt2-124m-b16" else None
+    roof["algorithmic_per_launch"] = flops / launches if roof["bound"] == "tensor" else nbytes / launches
     roof["kernel"] = dom
     roof["peak_source"] = peak_src
 
