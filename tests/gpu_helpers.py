@@ -9,6 +9,9 @@ from gpt_transformer_forward_gb300 import binding as ab
 
 def need_gpu():
     assert torch.cuda.is_available(), "the -m gpu tests need a CUDA GPU"
+    # output buffers are made with explicit dtypes, and no test may change
+    # torch's default dtype for the others
+    assert torch.get_default_dtype() == torch.float32
     ab.load()
 
 

@@ -34,7 +34,7 @@ def run_attention(B, T, C, NH, precision, seed=0, std=0.55, qk_std=1.0, grid=Non
     qkv[..., :2 * C] *= qk_std
     if grid is not None:
         qkv = inputs.on_grid(qkv, grid)
-    out = torch.full((B, T, C), float("nan"), device="cuda")
+    out = torch.full((B, T, C), float("nan"), dtype=torch.float32, device="cuda")
     wsz = ab.attention_workspace_size(B, T, C, precision)
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
     ab.attention_forward(out, dev(qkv), B, T, C, NH, precision, ws, wsz)
@@ -76,7 +76,7 @@ def test_attention_causal_bitwise():
     ws = torch.empty(ab.attention_workspace_size(B, T, C, ab.GPT2_BF16), dtype=torch.uint8, device="cuda")
     outs = []
     for q in (qkv, np.concatenate([qkv[:, :100], inputs.make_normal(10, (B, T - 100, 3 * C))], axis=1)):
-        o = torch.empty(B, T, C, device="cuda")
+        o = torch.empty(B, T, C, dtype=torch.float32, device="cuda")
         ab.attention_forward(o, dev(q), B, T, C, NH, ab.GPT2_BF16, ws, ws.numel())
         outs.append(host(o))
     np.testing.assert_array_equal(outs[0][:, :100], outs[1][:, :100])

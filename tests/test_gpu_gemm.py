@@ -35,7 +35,7 @@ def run_matmul(N, C, OC, precision, bias=True, seed=0, grid=None):
     b = inputs.make_normal(300 + seed, (OC,), 0.02) if bias else None
     if grid is not None:
         x, W = inputs.on_grid(x, grid), inputs.on_grid(W, grid)
-    out = torch.full((N, OC), float("nan"), device="cuda")
+    out = torch.full((N, OC), float("nan"), dtype=torch.float32, device="cuda")
     wsz = ab.matmul_workspace_size(N, C, OC, precision)
     ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
     ab.matmul_forward(out, dev(x), dev(W), dev(b) if bias else None, N, C, OC, precision, ws, wsz)
@@ -88,7 +88,7 @@ def test_matmul_bf16_is_bf16_rounded():
     N, C, OC = 128, 16, 256
     x = np.round(inputs.make_normal(7, (N, C), 4.0)).astype(np.float32)
     W = np.round(inputs.make_normal(8, (OC, C), 4.0)).astype(np.float32)
-    out = torch.empty(N, OC, device="cuda")
+    out = torch.empty(N, OC, dtype=torch.float32, device="cuda")
     wsz = ab.matmul_workspace_size(N, C, OC, ab.GPT2_BF16)
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
     ab.matmul_forward(out, dev(x), dev(W), None, N, C, OC, ab.GPT2_BF16, ws, wsz)
@@ -97,7 +97,7 @@ def test_matmul_bf16_is_bf16_rounded():
 
 def test_matmul_rejects_small_workspace():
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
-    out = torch.empty(8, 8, device="cuda")
+    out = torch.empty(8, 8, dtype=torch.float32, device="cuda")
     x = torch.zeros(8, 8, device="cuda")
     with pytest.raises(ab.GPT2Error) as e:
         ab.matmul_forward(out, x, x, None, 8, 8, 8, ab.GPT2_BF16, ws, 16)

@@ -26,7 +26,7 @@ def test_encoder_bit_exact(B, T, C, V):
     wte = inputs.make_normal(1, (V + 3, C), 0.02)
     wpe = inputs.make_normal(2, (T + 5, C), 0.02)
     tok = inputs.make_tokens(3, B, T, V)
-    out = torch.empty(B, T, C, device="cuda")
+    out = torch.empty(B, T, C, dtype=torch.float32, device="cuda")
     ab.encoder_forward(out, dev(tok), dev(wte), dev(wpe), B, T, C, V)
     ref = oracle.encoder(tok, wte, wpe).astype(np.float32)  # correctly rounded fp32 sums
     np.testing.assert_array_equal(host(out), ref)
@@ -38,7 +38,7 @@ def test_encoder_flags_bad_token():
     wte = inputs.make_normal(4, (V, C))
     wpe = inputs.make_normal(5, (T, C))
     tok = np.array([[1, 10, -3, 2]], dtype=np.int32)
-    out = torch.empty(B, T, C, device="cuda")
+    out = torch.empty(B, T, C, dtype=torch.float32, device="cuda")
     ab.encoder_forward(out, dev(tok), dev(wte), dev(wpe), B, T, C, V)
     assert ab.gpt2_get_error() == ab.DEVERR_TOKEN
     assert ab.gpt2_get_error() == 0  # reading clears the word
@@ -52,9 +52,9 @@ def test_layernorm(N, C):
     x = inputs.make_normal(6, (N, C), 1.3) + 0.25
     w = inputs.make_normal(7, (C,), 0.3) + 1.0
     b = inputs.make_normal(8, (C,), 0.1)
-    out = torch.empty(N, C, device="cuda")
-    mean = torch.empty(N, device="cuda")
-    rstd = torch.empty(N, device="cuda")
+    out = torch.empty(N, C, dtype=torch.float32, device="cuda")
+    mean = torch.empty(N, dtype=torch.float32, device="cuda")
+    rstd = torch.empty(N, dtype=torch.float32, device="cuda")
     ab.layernorm_forward(out, mean, rstd, dev(x), dev(w), dev(b), N, C)
     ref, rm, rr = oracle.layernorm(x, w, b)
     assert_close(host(out), ref, rtol=REL, floor=1.0, what="layernorm out")
@@ -74,7 +74,7 @@ def test_layernorm_in_place():
 @pytest.mark.parametrize("n", [1, 3, 4, 1001, 16384 * 3 + 2])
 def test_gelu(n):
     x = inputs.make_normal(10, (n,), 3.0)
-    out = torch.empty(n, device="cuda")
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
     ab.gelu_forward(out, dev(x), n)
     assert_close(host(out), oracle.gelu(x), rtol=REL, floor=1.0, what="gelu")
 
@@ -83,7 +83,7 @@ def test_gelu(n):
 def test_residual_bit_exact(n):
     a = inputs.make_normal(11, (n,))
     b = inputs.make_normal(12, (n,))
-    out = torch.empty(n, device="cuda")
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
     ab.residual_forward(out, dev(a), dev(b), n)
     np.testing.assert_array_equal(host(out), oracle.residual(a, b).astype(np.float32))
     ta = dev(a)
@@ -95,7 +95,7 @@ def test_residual_bit_exact(n):
                                         (7, 5, 8, 2.0), (1, 1000, 1024, 30.0)])
 def test_softmax(N, V, Vp, std):
     lg = inputs.make_normal(13, (N, Vp), std)
-    out = torch.empty(N, Vp, device="cuda")
+    out = torch.empty(N, Vp, dtype=torch.float32, device="cuda")
     ab.softmax_forward(out, dev(lg), N, V, Vp)
     ref = oracle.softmax(lg, V)
     got = host(out)

@@ -17,8 +17,6 @@ from scipy.special import ndtr
 import oracle
 from gpt_transformer_forward_gb300 import inputs
 
-torch.set_default_dtype(torch.float64)
-
 
 def rnd(seed, shape, std=1.0):
     return inputs.make_normal(seed, shape, std=std, dtype=np.float64)
