@@ -57,6 +57,7 @@ _SIGNATURES = {
     "layernorm_forward": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _P]),
     "matmul_workspace_size": (_Z, [_I, _I, _I, _I]),
     "matmul_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "matmul_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attention_workspace_size": (_Z, [_I, _I, _I, _I]),
     "attention_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "gelu_forward": (_I, [_P, _P, _I, _P]),
@@ -162,6 +163,13 @@ def matmul_workspace_size(N, C, OC, precision) -> int:
 def matmul_forward(out, inp, W, bias, N, C, OC, precision, workspace=None, ws_bytes=0, stream=None):
     _check("matmul_forward", _lib().matmul_forward(_ptr(out), _ptr(inp), _ptr(W), _ptr(bias), N, C, OC, precision,
                                                    _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def matmul_forward_noalloc(out, inp, W, bias, N, C, OC, precision, stream=None):
+    """matmul_forward with its scratch in the library's fixed 16 MiB device
+    array instead of a caller workspace (for callers that cannot allocate)."""
+    _check("matmul_forward_noalloc", _lib().matmul_forward_noalloc(_ptr(out), _ptr(inp), _ptr(W), _ptr(bias), N, C,
+                                                                   OC, precision, _stream(stream)))
 
 
 def attention_workspace_size(B, T, C, precision) -> int:

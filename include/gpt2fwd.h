@@ -124,6 +124,27 @@ GPT2_API size_t matmul_workspace_size(int N, int C, int OC, int precision);
 GPT2_API int matmul_forward(float* out, const float* inp, const float* W, const float* bias, int N, int C, int OC,
                    int precision, void* workspace, size_t ws_bytes, void* stream);
 
+/* matmul_forward without a caller workspace, for callers that cannot
+ * allocate device memory (code that must not call cudaMalloc because it can
+ * synchronise the device, or a plugin inside a program that owns every
+ * device allocation and offers it no workspace).  The pages have no
+ * counterpart of this call; it exists for such callers only.
+ * Arguments, layouts and results are those of matmul_forward.  The 16-bit
+ * copies that the GPT2_BF16 and GPT2_FP16 modes need live in a fixed 16 MiB
+ * device array inside the library (every GPU that loads the library holds
+ * it until the process exits): shapes with matmul_workspace_size(N, C, OC,
+ * precision) > 16 MiB are rejected with GPT2_ERR_WORKSPACE.  GPT2_FP32 and
+ * GPT2_TF32 need no scratch.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the one array and each overwrites it before reading it, so
+ * calls whose work overlaps on the GPU (on different streams, or different
+ * host threads without ordering) race and give wrong results: order them on
+ * one stream.  Allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine is called. */
+GPT2_API int matmul_forward_noalloc(float* out, const float* inp, const float* W, const float* bias, int N, int C,
+                                   int OC, int precision, void* stream);
+
 /* Scratch bytes attention_forward needs (the 16-bit copy of qkv in the
  * tensor-core modes, 0 in GPT2_FP32). */
 GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
