@@ -403,6 +403,7 @@ static int attention_tc(void* out, bool out16, const void* qkv, int B, int T, in
 
 int launch_attention_16(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
                         cudaStream_t s) {
+  if (C / NH == 64) return launch_attention_tc05(out, out16, qkv, op, B, T, C, NH, s);  // tcgen05 kernel
   if (op == kOpF16) return attention_tc<__half>(out, out16, qkv, B, T, C, NH, s);
   return attention_tc<__nv_bfloat16>(out, out16, qkv, B, T, C, NH, s);
 }

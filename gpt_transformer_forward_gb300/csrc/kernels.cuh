@@ -30,6 +30,12 @@ void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, in
 void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
                         cudaStream_t s);
 
+// Encodes a tiled TMA map with the 128-byte swizzle: dims[0] innermost (in
+// elements), strides_bytes[i] the byte stride of dimension i + 1, box the
+// box extent per dimension.  false when the driver rejects it.
+bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                             const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
+
 // gemm_tc.cu: D[M,N] = A[M,K] B[N,K]^T on tcgen05 tensor cores, A and B
 // K-major (row-major [rows, K]), fp32 accumulation in TMEM, fused epilogue.
 enum GemmEpilogue {
@@ -67,6 +73,9 @@ void launch_gemm_simt(float* out, const float* A, const float* W, const float* b
 // the operand type when out16.
 int launch_attention_16(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
                         cudaStream_t s);
+// The same on tcgen05/TMEM (attention_tc.cu), head size 64 only.
+int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
+                          cudaStream_t s);
 // fp32 CUDA-core causal attention (head size 16, 32 or 64).
 int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s);
 // Decode attention: one query per sequence (row b of qkv [B,3C]) against the

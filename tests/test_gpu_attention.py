@@ -42,8 +42,11 @@ def run_attention(B, T, C, NH, precision, seed=0, std=0.55, qk_std=1.0, grid=Non
     return host(out), oracle.attention(qkv, NH), qkv
 
 
-SHAPES = [(1, 1, 64, 4), (2, 32, 64, 4), (1, 64, 128, 2), (2, 65, 128, 4), (1, 200, 768, 12),
-          (1, 130, 256, 8), (2, 1024, 768, 12), (3, 97, 192, 12)]
+# head size 64 (the tcgen05 kernel): T = 1, within, at and past a 128-row
+# tile, the GPT-2 width; head sizes 16 and 32 (the mma.sync kernel)
+SHAPES = [(1, 1, 128, 2), (2, 64, 128, 2), (1, 128, 128, 2), (2, 129, 128, 2), (1, 200, 768, 12),
+          (2, 1024, 768, 12), (1, 1000, 1024, 16),
+          (1, 1, 64, 4), (2, 32, 64, 4), (2, 65, 128, 4), (1, 130, 256, 8), (3, 97, 192, 12)]
 
 
 @pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16, ab.GPT2_TF32, ab.GPT2_FP32])
@@ -55,7 +58,8 @@ def test_attention(B, T, C, NH, precision):
 
 @pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16])
 @pytest.mark.parametrize("qk_std", [1.0, 3.0])
-@pytest.mark.parametrize("B,T,C,NH", [(2, 65, 128, 4), (1, 300, 768, 12), (1, 1024, 768, 12), (2, 40, 64, 4)])
+@pytest.mark.parametrize("B,T,C,NH", [(2, 65, 128, 4), (1, 300, 768, 12), (1, 1024, 768, 12), (2, 40, 64, 4),
+                                      (2, 257, 128, 2)])
 def test_attention_on_grid(B, T, C, NH, precision, qk_std):
     # qk_std 3: a few keys dominate each row, exercising the running max
     got, ref, qkv = run_attention(B, T, C, NH, precision, seed=3, std=1.0, qk_std=qk_std, grid=GRID[precision])
