@@ -36,8 +36,16 @@ int num_sms() {
 }
 
 namespace {
-
 thread_local std::string g_last_cuda_error;
+}  // namespace
+
+int note_cuda_error(cudaError_t e) {
+  g_last_cuda_error = cudaGetErrorString(e);
+  cudaGetLastError();
+  return GPT2_ERR_CUDA;
+}
+
+namespace {
 
 int check_launch() {
   const cudaError_t e = cudaPeekAtLastError();

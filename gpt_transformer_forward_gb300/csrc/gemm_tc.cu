@@ -432,12 +432,13 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc) != cudaSuccess)
-      return GPT2_ERR_CUDA;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc);
+    if (e != cudaSuccess) return note_cuda_error(e);
     attr_set[dev] = true;
   }
   kern<<<grid, kThreads, SmemLayout::alloc, s>>>(ta, tb, to, bias, M, N, K, tiles_m, num_tiles, row_stats, V);
-  return cudaPeekAtLastError() == cudaSuccess ? GPT2_OK : GPT2_ERR_CUDA;
+  const cudaError_t e = cudaPeekAtLastError();
+  return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 
 }  // namespace

@@ -7,6 +7,9 @@ namespace gpt2 {
 
 constexpr int kMaxDevices = 64;
 int num_sms();  // SM count of the current device (cached)
+// Records a CUDA error's text for gpt2_last_cuda_error(), clears it from the
+// runtime, and returns GPT2_ERR_CUDA.
+int note_cuda_error(cudaError_t e);
 
 // rowwise.cu
 void launch_encoder(float* out, const int* tok, const float* wte, const float* wpe, int N, int T, int C, int V,
