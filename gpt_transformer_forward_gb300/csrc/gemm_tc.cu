@@ -5,13 +5,20 @@
 //   D[M, N] = A[M, K] * B[N, K]^T   (A: activations, B: a Linear weight
 //                                     stored [out, in], both K-major)
 //
-// Design (persistent, warp-specialised, one CTA per SM):
-//   warp 0      TMA producer: 128 x 128-byte A and 256 x 128-byte B boxes
-//               (128-byte swizzle) into a 4-stage shared-memory ring;
-//   warp 1      allocates 512 TMEM columns, and one lane issues tcgen05.mma
-//               (128 x 256 x 16 for bf16 or fp16 operands, 128 x 256 x 8
-//               for tf32, per instruction)
-//               into one of two 128 x 256 fp32 TMEM accumulators;
+// Design (persistent, warp-specialised, one CTA per SM).  For M > 128 the
+// CTAs run as pairs (clusters of two): a pair owns a 256 x 256 tile, each
+// CTA loads its 128 rows of A and one half (128 rows) of the B tile, and
+// the even CTA issues the pair MMA (tcgen05 cta_group::2, M = 256) that
+// writes each CTA's 128 rows into its own TMEM.  A single CTA's MMA runs at
+// about half the SM's tensor rate; the pair form reaches the full rate and
+// halves the B bytes each SM loads.  Small M uses one CTA per 128 x 256 tile.
+//   warp 0      TMA producer: 128 x 128-byte A and 256 (single) or 128
+//               (pair) x 128-byte B boxes (128-byte swizzle) into a 4-stage
+//               (single) or 6-stage (pair) shared-memory ring;
+//   warp 1      allocates 512 TMEM columns, and one lane (in a pair: of the
+//               even CTA) issues tcgen05.mma (128 or 256 x 256 x 16 for bf16
+//               or fp16 operands, x 8 for tf32, per instruction) into one of
+//               two 256-column fp32 TMEM accumulators;
 //   warps 2-5   epilogue: tcgen05.ld 32 columns of their 32 TMEM lanes,
 //               add bias, apply GELU or add the residual (TMA-loaded), stage
 //               the tile in swizzled shared memory and TMA-store it.  The
@@ -30,18 +37,21 @@
 namespace gpt2 {
 namespace {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kStages = 4;
+constexpr int kBM = 128;  // rows of A (and of D) per CTA
+constexpr int kBN = 256;  // columns of D per tile
 constexpr int kRowBytes = 128;  // one swizzle atom row: 64 bf16 or 32 fp32 of K
-constexpr int kAStageBytes = kBM * kRowBytes;
-constexpr int kBStageBytes = kBN * kRowBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kStageBufBytes = 32 * 128;  // 32 rows x 128 bytes
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 
-struct SmemLayout {
+// Shared-memory layout of a CTA, single (kPair false) or one of a pair.
+template <bool kPair>
+struct Layout {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // B rows this CTA loads per stage
+  static constexpr int kAStageBytes = kBM * kRowBytes;
+  static constexpr int kBStageBytes = kBRows * kRowBytes;
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kStages * kAStageBytes;
   static constexpr int stg_off = b_off + kStages * kBStageBytes;
@@ -52,46 +62,55 @@ struct SmemLayout {
   static constexpr int total = misc_off + 16;
   static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
 };
-static_assert(SmemLayout::alloc <= 232448, "shared memory budget");
+static_assert(Layout<false>::alloc <= 232448 && Layout<true>::alloc <= 232448, "shared memory budget");
 
 __host__ __device__ constexpr int gridDim_n(int N) { return (N + kBN - 1) / kBN; }
 
-template <int kEpi, int kOp>
+template <int kEpi, int kOp, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
                    int K, int tiles_m, int num_tiles, float2* __restrict__ row_stats, int V) {
+  using L = Layout<kPair>;
+  constexpr int kStages = L::kStages;
+  constexpr int kAStageBytes = L::kAStageBytes;
+  constexpr int kBStageBytes = L::kBStageBytes;
+  constexpr int kTileM = kPair ? 2 * kBM : kBM;  // rows of a tile (a pair's or a CTA's)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bar_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar_off);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tmem_full = bars + 2 * kStages;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* res_bar = tmem_empty + 2;
   uint64_t* drain_bar = res_bar + 2 * kEpiWarps;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc_off);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SmemLayout::misc_off + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // a pair walks the tiles together: rank 0 or 1 within it, pair index
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int n_units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
   constexpr bool kTF32 = (kOp == kOpTF32);
   using Out16 = typename std::conditional<kOp == kOpF16, __half, __nv_bfloat16>::type;
   constexpr int kElemBytes = kTF32 ? 4 : 2;
   constexpr int kBKElems = kRowBytes / kElemBytes;  // K elements per stage
   constexpr int kMmaK = 32 / kElemBytes;            // K per instruction (32 bytes)
   // operand format field: fp16 0, bf16 1 (kind::f16), tf32 2 (kind::tf32)
-  constexpr uint32_t kIdesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kBM, kBN);
+  constexpr uint32_t kIdesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kTileM, kBN);
   const int num_kb = (K + kBKElems - 1) / kBKElems;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], kPair ? 2 : 1);  // pair: both producers arrive on the even CTA's barrier
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], kEpiWarps);
+      mbar_init(&tmem_empty[a], kPair ? 2 * kEpiWarps : kEpiWarps);  // pair: both CTAs' epilogues
     }
     for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&res_bar[i], 1);
     mbar_init(drain_bar, 1);
@@ -104,11 +123,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_out);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_slot, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();  // the peer's barriers are initialised before any remote arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -119,19 +146,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled, parity of its last fill
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+      for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units) {
         const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
+        const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
+        const int b_row = n_blk * kBN + static_cast<int>(rank) * L::kBRows;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kAStageBytes + kBStageBytes);
-          tma_load_2d_hint(smem + SmemLayout::a_off + stage * kAStageBytes, &tmap_a, &full[stage], kb * kBKElems,
-                           m_blk * kBM, pol_a);
-          tma_load_2d(smem + SmemLayout::b_off + stage * kBStageBytes, &tmap_b, &full[stage], kb * kBKElems,
-                      n_blk * kBN);
+          if constexpr (kPair) {  // both CTAs' bytes complete the even CTA's full barrier
+            const uint32_t full_even = mapa_shared(smem_u32(&full[stage]), 0);
+            mbar_arrive_expect_tx_cluster(full_even, kAStageBytes + kBStageBytes);
+            tma_load_2d_pair(smem + L::a_off + stage * kAStageBytes, &tmap_a, full_even, kb * kBKElems, a_row);
+            tma_load_2d_pair(smem + L::b_off + stage * kBStageBytes, &tmap_b, full_even, kb * kBKElems, b_row);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], kAStageBytes + kBStageBytes);
+            tma_load_2d_hint(smem + L::a_off + stage * kAStageBytes, &tmap_a, &full[stage], kb * kBKElems, a_row,
+                             pol_a);
+            tma_load_2d(smem + L::b_off + stage * kBStageBytes, &tmap_b, &full[stage], kb * kBKElems, b_row);
+          }
           filled |= 1u << stage;
           fill_parity = (fill_parity & ~(1u << stage)) | (phase << stage);
           if (++stage == kStages) {
@@ -144,20 +179,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
       }
-      // Only this thread arms the full barriers, so the phase of a stage's
-      // last fill completes exactly when its bytes have landed: wait for
-      // every such phase before the CTA may exit (immediate when the MMA
-      // warp has consumed them, which is the normal case).
+      // Before the CTA may exit, the copies issued here must have landed:
+      // single, only this thread arms the full barriers, so the phase of a
+      // stage's last fill completes exactly when its bytes have landed; in a
+      // pair the full barriers are the even CTA's, so wait instead for the
+      // MMAs that consumed the last fill to release the slot (immediate in
+      // the normal case).
       for (int s = 0; s < kStages; ++s)
-        if ((filled >> s) & 1u) mbar_wait(&full[s], (fill_parity >> s) & 1u);
+        if ((filled >> s) & 1u) mbar_wait(kPair ? &empty[s] : &full[s], (fill_parity >> s) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {  // in a pair the even CTA issues for both
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+      for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1)) {
@@ -173,14 +210,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(smem + SmemLayout::a_off + stage * kAStageBytes);
-          const uint32_t b_addr = smem_u32(smem + SmemLayout::b_off + stage * kBStageBytes);
+          const uint32_t a_addr = smem_u32(smem + L::a_off + stage * kAStageBytes);
+          const uint32_t b_addr = smem_u32(smem + L::b_off + stage * kBStageBytes);
 #pragma unroll
           for (int k = 0; k < kBKElems / kMmaK; ++k) {
-            tc_mma<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                          (kb | k) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              tc_mma_pair<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+            else
+              tc_mma<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                            (kb | k) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);  // frees the smem slot once these MMAs have read it
+          // frees the smem slot (in both CTAs of a pair) once these MMAs have read it
+          if constexpr (kPair)
+            tc_commit_pair(&empty[stage], 3);
+          else
+            tc_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -190,10 +235,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           *abort_flag = 1;
           break;
         }
-        tc_commit(&tmem_full[acc]);  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (kPair)
+          tc_commit_pair(&tmem_full[acc], 3);
+        else
+          tc_commit(&tmem_full[acc]);
       }
       // every MMA issued above has completed once this commit arrives
-      tc_commit(drain_bar);
+      if constexpr (kPair)
+        tc_commit_pair(drain_bar, 1);
+      else
+        tc_commit(drain_bar);
       mbar_wait(drain_bar, 0);
     }
   } else {
@@ -201,11 +253,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;            // epilogue warp index 0..3
     const int quad = warp & 3;          // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32;  // tile rows [row_in_tile, row_in_tile + 32)
-    uint8_t* stg0 = smem + SmemLayout::stg_off + ew * 2 * kStageBufBytes;
+    uint8_t* stg0 = smem + L::stg_off + ew * 2 * kStageBufBytes;
     uint32_t res_phase = 0;  // bit b: parity of the next residual load into buffer b
     uint32_t chunk_ctr = 0;
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x, ++local) {
+    for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units, ++local) {
       const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
@@ -216,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int m0 = m_blk * kBM + row_in_tile;
+      const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile;
       const int n0 = n_blk * kBN;
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
       constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
@@ -336,7 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this warp is done reading the accumulator
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+      if (lane == 0) {
+        if constexpr (kPair)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));  // the even CTA's barrier
+        else
+          mbar_arrive(&tmem_empty[acc]);
+      }
       if (!ok) {
         *abort_flag = 1;
         break;
@@ -347,10 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();  // neither CTA leaves while the pair MMAs may read its shared memory
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
@@ -405,9 +468,10 @@ bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank,
 
 namespace {
 
-template <int kEpi, int kOp>
-int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
-                 float2* row_stats = nullptr, int V = 0) {
+template <int kEpi, int kOp, bool kPair>
+int launch_impl(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
+                float2* row_stats, int V) {
+  using L = Layout<kPair>;
   CUtensorMap ta, tb, to;
   constexpr bool kTF32 = (kOp == kOpTF32);
   const CUtensorMapDataType dt16 =
@@ -417,28 +481,58 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
   const int bk = kRowBytes / eb;
   constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
   if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
-  if (!make_map(&tb, B, dt_in, eb, N, K, bk, kBN)) return GPT2_ERR_CUDA;
+  if (!make_map(&tb, B, dt_in, eb, N, K, bk, L::kBRows)) return GPT2_ERR_CUDA;
   if (kOutF32) {
     if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 32, 32)) return GPT2_ERR_CUDA;
   } else {
     if (!make_map(&to, out, dt16, 2, M, N, 64, 32)) return GPT2_ERR_CUDA;
   }
-  const int tiles_m = (M + kBM - 1) / kBM;
+  constexpr int kTileM = kPair ? 2 * kBM : kBM;
+  const int tiles_m = (M + kTileM - 1) / kTileM;
   const int tiles_n = (N + kBN - 1) / kBN;
   const int num_tiles = tiles_m * tiles_n;
-  const int grid = num_tiles < num_sms() ? num_tiles : num_sms();
-  auto kern = gemm_tc_kernel<kEpi, kOp>;
-  static bool attr_set[kMaxDevices] = {};  // per template instance and device
+  auto kern = gemm_tc_kernel<kEpi, kOp, kPair>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::alloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // per template instance and device: the shared-memory attribute and how
+  // many CTAs (or pairs) can be resident at once
+  static int resident[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
-  if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::alloc);
+  if (resident[dev] == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::alloc);
     if (e != cudaSuccess) return note_cuda_error(e);
-    attr_set[dev] = true;
+    int n = kPair ? num_sms() / 2 : num_sms();
+    if (kPair) {
+      cfg.gridDim = dim3(2 * n);
+      int clusters = 0;
+      e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+      if (e != cudaSuccess) return note_cuda_error(e);
+      if (clusters > 0 && clusters < n) n = clusters;
+    }
+    resident[dev] = n;
   }
-  kern<<<grid, kThreads, SmemLayout::alloc, s>>>(ta, tb, to, bias, M, N, K, tiles_m, num_tiles, row_stats, V);
-  const cudaError_t e = cudaPeekAtLastError();
+  const int units = num_tiles < resident[dev] ? num_tiles : resident[dev];
+  cfg.gridDim = dim3(kPair ? 2 * units : units);
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, row_stats, V);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
+}
+
+template <int kEpi, int kOp>
+int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
+                 float2* row_stats = nullptr, int V = 0) {
+  if (M > kBM) return launch_impl<kEpi, kOp, true>(out, A, B, bias, M, N, K, s, row_stats, V);
+  return launch_impl<kEpi, kOp, false>(out, A, B, bias, M, N, K, s, row_stats, V);
 }
 
 }  // namespace
