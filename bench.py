@@ -46,25 +46,31 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def stage_costs(cfg, B, T, act_bytes=2):
     """Algorithmic FLOPs and bytes of each stage of one forward pass (every
     layer summed): bytes count each input read once and each output written
-    once, with operand buffers of act_bytes (2 for bf16), the residual
-    stream, logits and probabilities fp32, weights bf16, and the causal
-    attention FLOPs only (j <= t)."""
+    once, with operand buffers of act_bytes (2 for bf16/fp16), the residual
+    stream, logits and probabilities fp32, weights 16-bit, and the causal
+    attention FLOPs only (j <= t).  With 16-bit operands the two projections
+    write their output y in 16 bits and the residual add x += y runs in the
+    LayerNorm that follows (layer 0's first LayerNorm has no y to add; the
+    final one does not write x back)."""
     C, L, NH, Vp = cfg.channels, cfg.num_layers, cfg.num_heads, cfg.padded_vocab_size
     hs = C // NH
     N = B * T
     a, w = act_bytes, 2
+    fused = act_bytes == 2
     ln_bytes = N * C * 4 + N * C * a + 2 * C * 4
+    fused_ln = ln_bytes + N * C * a + N * C * 4   # + read y, + write x
+    proj_out = N * C * a if fused else 2 * N * C * 4
     pairs = T * (T + 1) // 2
     return {
         "encoder": (0, 4 * N + N * C * 4 + T * C * 4 + N * C * 4),
-        "ln1": (0, L * ln_bytes),
+        "ln1": (0, ln_bytes + (L - 1) * (fused_ln if fused else ln_bytes)),
         "qkv": (L * 2 * N * C * 3 * C, L * (N * C * a + 3 * C * C * w + 3 * C * 4 + N * 3 * C * a)),
         "attention": (L * B * NH * 4 * hs * pairs, L * (N * 3 * C * a + N * C * a)),
-        "attproj": (L * 2 * N * C * C, L * (N * C * a + C * C * w + C * 4 + 2 * N * C * 4)),
-        "ln2": (0, L * ln_bytes),
+        "attproj": (L * 2 * N * C * C, L * (N * C * a + C * C * w + C * 4 + proj_out)),
+        "ln2": (0, L * (fused_ln if fused else ln_bytes)),
         "fc": (L * 2 * N * C * 4 * C, L * (N * C * a + 4 * C * C * w + 4 * C * 4 + N * 4 * C * a)),
-        "fcproj": (L * 2 * N * 4 * C * C, L * (N * 4 * C * a + 4 * C * C * w + C * 4 + 2 * N * C * 4)),
-        "lnf": (0, ln_bytes),
+        "fcproj": (L * 2 * N * 4 * C * C, L * (N * 4 * C * a + 4 * C * C * w + C * 4 + proj_out)),
+        "lnf": (0, ln_bytes + (N * C * a if fused else 0)),
         "lm_head": (2 * N * C * Vp, N * C * a + Vp * C * w + N * Vp * 4),
         "softmax": (0, 2 * N * Vp * 4),
     }

@@ -426,6 +426,20 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     else
       launch_layernorm_f32(static_cast<float*>(out), nullptr, nullptr, in, params + w_off, params + b_off, N, C, s);
   };
+  // In the 16-bit modes the attention and MLP projections write their
+  // output y (bias added) as 16-bit into the QKV buffer, which is free by
+  // then, and the residual add x += y runs in the LayerNorm that reads x
+  // next: the same bytes as a residual-accumulating GEMM epilogue plus a
+  // plain LayerNorm, without the epilogue's serial read of x.
+  void* y16 = qkv;
+  auto resid_layernorm = [&](size_t w_off, size_t b_off, bool write_x) {
+    if (precision == GPT2_FP16)
+      launch_residual_layernorm_16(x, static_cast<const __half*>(y16), static_cast<__half*>(ln), params + w_off,
+                                   params + b_off, N, C, write_x, s);
+    else
+      launch_residual_layernorm_16(x, static_cast<const __nv_bfloat16*>(y16), static_cast<__nv_bfloat16*>(ln),
+                                   params + w_off, params + b_off, N, C, write_x, s);
+  };
 
   if (decode_pos < 0)
     launch_encoder(x, tok, params + po.wte, params + po.wpe, N, T, C, V, s);
@@ -436,7 +450,10 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
 
   for (int l = 0; l < L; ++l) {
     const size_t CC = static_cast<size_t>(C) * C;
-    layernorm(ln, x, po.ln1w + static_cast<size_t>(l) * C, po.ln1b + static_cast<size_t>(l) * C);
+    if (bf16 && l > 0)  // the previous layer's MLP output is still to be added
+      resid_layernorm(po.ln1w + static_cast<size_t>(l) * C, po.ln1b + static_cast<size_t>(l) * C, true);
+    else
+      layernorm(ln, x, po.ln1w + static_cast<size_t>(l) * C, po.ln1b + static_cast<size_t>(l) * C);
     TRY(mark(GPT2_STAGE_LN1));
     TRY(gemm(precision, qkv, ln, wmat(po.qkvw, ko.qkvw, 3 * CC, l), params + po.qkvb + static_cast<size_t>(l) * 3 * C,
              N, 3 * C, C, bf16 ? kEpiOut16 : kEpiF32, s));
@@ -472,19 +489,25 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     }
     TRY(check_launch());
     TRY(mark(GPT2_STAGE_ATTENTION));
-    TRY(gemm(precision, x, att, wmat(po.attprojw, ko.attprojw, CC, l), params + po.attprojb + static_cast<size_t>(l) * C,
-             N, C, C, kEpiResidF32, s));
+    TRY(gemm(precision, bf16 ? y16 : static_cast<void*>(x), att, wmat(po.attprojw, ko.attprojw, CC, l),
+             params + po.attprojb + static_cast<size_t>(l) * C, N, C, C, bf16 ? kEpiOut16 : kEpiResidF32, s));
     TRY(mark(GPT2_STAGE_ATTPROJ));
-    layernorm(ln, x, po.ln2w + static_cast<size_t>(l) * C, po.ln2b + static_cast<size_t>(l) * C);
+    if (bf16)
+      resid_layernorm(po.ln2w + static_cast<size_t>(l) * C, po.ln2b + static_cast<size_t>(l) * C, true);
+    else
+      layernorm(ln, x, po.ln2w + static_cast<size_t>(l) * C, po.ln2b + static_cast<size_t>(l) * C);
     TRY(mark(GPT2_STAGE_LN2));
     TRY(gemm(precision, fch, ln, wmat(po.fcw, ko.fcw, 4 * CC, l), params + po.fcb + static_cast<size_t>(l) * 4 * C, N,
              4 * C, C, kEpiGelu16, s));
     TRY(mark(GPT2_STAGE_FC));
-    TRY(gemm(precision, x, fch, wmat(po.fcprojw, ko.fcprojw, 4 * CC, l),
-             params + po.fcprojb + static_cast<size_t>(l) * C, N, C, 4 * C, kEpiResidF32, s));
+    TRY(gemm(precision, bf16 ? y16 : static_cast<void*>(x), fch, wmat(po.fcprojw, ko.fcprojw, 4 * CC, l),
+             params + po.fcprojb + static_cast<size_t>(l) * C, N, C, 4 * C, bf16 ? kEpiOut16 : kEpiResidF32, s));
     TRY(mark(GPT2_STAGE_FCPROJ));
   }
-  layernorm(ln, x, po.lnfw, po.lnfb);
+  if (bf16 && L > 0)  // the residual stream is not read after the final LayerNorm
+    resid_layernorm(po.lnfw, po.lnfb, false);
+  else
+    layernorm(ln, x, po.lnfw, po.lnfb);
   TRY(mark(GPT2_STAGE_LNF));
   const void* wte = bf16 ? static_cast<const void*>(pk + ko.wte) : static_cast<const void*>(params + po.wte);
   float2* stats = reinterpret_cast<float2*>(ws + wl.stats);

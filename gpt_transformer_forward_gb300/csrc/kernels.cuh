@@ -21,6 +21,11 @@ void launch_layernorm_f32(float* out, float* mean, float* rstd, const float* inp
 // LayerNorm writing the 16-bit operand type T (bf16 or fp16)
 template <typename T>
 void launch_layernorm_16(T* out, const float* inp, const float* w, const float* b, int N, int C, cudaStream_t s);
+// x += y and out = LN(x) in one pass (y and out 16-bit); x is written back
+// unless write_x is false
+template <typename T16>
+void launch_residual_layernorm_16(float* x, const T16* y, T16* out, const float* w, const float* b, int N, int C,
+                                  bool write_x, cudaStream_t s);
 void launch_gelu(float* out, const float* inp, int n, cudaStream_t s);
 void launch_residual(float* out, const float* a, const float* b, int n, cudaStream_t s);
 void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s);

@@ -192,6 +192,104 @@ template void launch_layernorm_16<__nv_bfloat16>(__nv_bfloat16*, const float*, c
                                                  cudaStream_t);
 template void launch_layernorm_16<__half>(__half*, const float*, const float*, const float*, int, int, cudaStream_t);
 
+// grid of a grid-stride elementwise kernel: enough blocks for n work items,
+// at most 8 per SM
+static unsigned stream_grid(long long n4, int threads) {
+  int sms = num_sms();
+  long long want = (n4 + threads - 1) / threads;
+  long long cap = static_cast<long long>(sms) * 8;
+  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+// ------------------------------------------------ residual + LayerNorm
+// x += y (the sublayer output, 16-bit) and out = LN(x) (16-bit) in one pass:
+// the residual add of the attention and MLP projections, fused into the
+// LayerNorm that reads x next.  One warp per row of C = 128 * kVec; x is
+// written back unless write_x is false (the last LayerNorm).
+template <int kVec, typename T16>
+__global__ void __launch_bounds__(256) residual_layernorm_kernel(float* __restrict__ x, const T16* __restrict__ y,
+                                                                 T16* __restrict__ out, const float* __restrict__ w,
+                                                                 const float* __restrict__ b, int N, int write_x) {
+  constexpr int C = 128 * kVec;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= N) return;
+  float4* x4 = reinterpret_cast<float4*>(x + static_cast<size_t>(row) * C);
+  const uint2* y4 = reinterpret_cast<const uint2*>(y + static_cast<size_t>(row) * C);
+  float4 v[kVec];
+  uint2 yy[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    v[i] = x4[lane + 32 * i];
+    yy[i] = __ldcs(y4 + lane + 32 * i);
+  }
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const T16* h = reinterpret_cast<const T16*>(&yy[i]);
+    v[i].x += to_f32(h[0]);
+    v[i].y += to_f32(h[1]);
+    v[i].z += to_f32(h[2]);
+    v[i].w += to_f32(h[3]);
+    if (write_x) x4[lane + 32 * i] = v[i];
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+  const float mean = warp_sum(s) * (1.0f / C);
+  float q = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const float dx = v[i].x - mean, dy = v[i].y - mean, dz = v[i].z - mean, dw = v[i].w - mean;
+    q += (dx * dx + dy * dy) + (dz * dz + dw * dw);
+  }
+  const float rstd = rsqrtf(warp_sum(q) * (1.0f / C) + 1e-5f);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+  const float4* b4 = reinterpret_cast<const float4*>(b);
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const int c4 = lane + 32 * i;
+    const float4 ww = __ldg(w4 + c4), bb = __ldg(b4 + c4);
+    uint2 p;
+    p.x = pack2<T16>((v[i].x - mean) * rstd * ww.x + bb.x, (v[i].y - mean) * rstd * ww.y + bb.y);
+    p.y = pack2<T16>((v[i].z - mean) * rstd * ww.z + bb.z, (v[i].w - mean) * rstd * ww.w + bb.w);
+    reinterpret_cast<uint2*>(out + static_cast<size_t>(row) * C)[c4] = p;
+  }
+}
+
+// x += y for any C (the fallback before a plain LayerNorm)
+template <typename T16>
+__global__ void add16_kernel(float* __restrict__ x, const T16* __restrict__ y, long long n) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    x[i] += to_f32(y[i]);
+}
+
+template <typename T16>
+void launch_residual_layernorm_16(float* x, const T16* y, T16* out, const float* w, const float* b, int N, int C,
+                                  bool write_x, cudaStream_t s) {
+  const int rows_per_block = 8;
+  const unsigned grid = static_cast<unsigned>((N + rows_per_block - 1) / rows_per_block);
+  const int wx = write_x ? 1 : 0;
+  switch (C) {
+    case 256: residual_layernorm_kernel<2, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 512: residual_layernorm_kernel<4, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 768: residual_layernorm_kernel<6, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 1024: residual_layernorm_kernel<8, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 1280: residual_layernorm_kernel<10, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 1536: residual_layernorm_kernel<12, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    default: {
+      const long long n = static_cast<long long>(N) * C;
+      add16_kernel<T16><<<stream_grid(n, 256), 256, 0, s>>>(x, y, n);
+      launch_layernorm_16(out, x, w, b, N, C, s);
+      return;
+    }
+  }
+}
+template void launch_residual_layernorm_16<__nv_bfloat16>(float*, const __nv_bfloat16*, __nv_bfloat16*,
+                                                          const float*, const float*, int, int, bool, cudaStream_t);
+template void launch_residual_layernorm_16<__half>(float*, const __half*, __half*, const float*, const float*, int,
+                                                   int, bool, cudaStream_t);
+
 // ------------------------------------------------------- GELU and residual
 __global__ void gelu_kernel(float4* __restrict__ out, const float4* __restrict__ inp, long long n4) {
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
@@ -217,13 +315,6 @@ __global__ void residual_kernel(float4* out, const float4* a, const float4* b, l
 __global__ void residual_tail_kernel(float* out, const float* a, const float* b, int start, int n) {
   const int i = start + blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) out[i] = a[i] + b[i];
-}
-
-static unsigned stream_grid(long long n4, int threads) {
-  int sms = num_sms();
-  long long want = (n4 + threads - 1) / threads;
-  long long cap = static_cast<long long>(sms) * 8;
-  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 void launch_gelu(float* out, const float* inp, int n, cudaStream_t s) {
