@@ -190,22 +190,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    if (lane == 0 && rank == 0) {  // in a pair the even CTA issues for both
+    if (rank == 0) {  // in a pair the even CTA issues for both; the warp runs the loop, one lane issues
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units, ++local) {
+      for (int tile = unit; tile < num_tiles && __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+           tile += n_units, ++local) {  // one read for the whole warp: it must not split
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1)) {
-          *abort_flag = 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tmem_empty[acc], acc_phase ^ 1))) {
+          if (lane == 0) *abort_flag = 1;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
             ok = false;
             break;
           }
@@ -215,17 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBKElems / kMmaK; ++k) {
             if constexpr (kPair)
-              tc_mma_pair<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                                 (kb | k) != 0 ? 1u : 0u);
+              tc_mma_pair_warp<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
+                                      kIdesc, (kb | k) != 0 ? 1u : 0u);
             else
-              tc_mma<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                            (kb | k) != 0 ? 1u : 0u);
+              tc_mma_warp<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
+                                 (kb | k) != 0 ? 1u : 0u);
           }
           // frees the smem slot (in both CTAs of a pair) once these MMAs have read it
           if constexpr (kPair)
-            tc_commit_pair(&empty[stage], 3);
+            tc_commit_pair_warp(&empty[stage], 3);
           else
-            tc_commit(&empty[stage]);
+            tc_commit_warp(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -237,15 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // accumulator ready for the epilogue (of both CTAs of a pair)
         if constexpr (kPair)
-          tc_commit_pair(&tmem_full[acc], 3);
+          tc_commit_pair_warp(&tmem_full[acc], 3);
         else
-          tc_commit(&tmem_full[acc]);
+          tc_commit_warp(&tmem_full[acc]);
       }
       // every MMA issued above has completed once this commit arrives
       if constexpr (kPair)
-        tc_commit_pair(drain_bar, 1);
+        tc_commit_pair_warp(drain_bar, 1);
       else
-        tc_commit(drain_bar);
+        tc_commit_warp(drain_bar);
       mbar_wait(drain_bar, 0);
     }
   } else {
@@ -448,8 +449,8 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
 
 }  // namespace
 
-bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
-                             const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn || rank < 1 || rank > 5) return false;
   cuuint64_t d[5], st[4];
@@ -461,9 +462,14 @@ bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank,
     if (i + 1 < rank) st[i] = strides_bytes[i];
   }
   const CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, bx, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
+                             const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box) {
+  return encode_tensor_map(map, dt, rank, base, dims, strides_bytes, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 namespace {

@@ -38,9 +38,12 @@ void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, in
 void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
                         cudaStream_t s);
 
-// Encodes a tiled TMA map with the 128-byte swizzle: dims[0] innermost (in
-// elements), strides_bytes[i] the byte stride of dimension i + 1, box the
-// box extent per dimension.  false when the driver rejects it.
+// Encodes a tiled TMA map with the given shared-memory swizzle: dims[0]
+// innermost (in elements), strides_bytes[i] the byte stride of dimension
+// i + 1, box the box extent per dimension.  false when the driver rejects
+// it.  encode_tensor_map_sw128: the 128-byte swizzle.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle swizzle);
 bool encode_tensor_map_sw128(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                              const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box);
 
