@@ -168,7 +168,7 @@ Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
   w.att = p; p = round_up(p + N * C * act, 256);
   w.fch = p; p = round_up(p + N * 4 * C * act, 256);
   w.dec = p; p = round_up(p + decode_attention_scratch_floats(B, c->channels, c->num_heads, c->max_seq_len) * 4, 256);
-  w.stats = p; p = round_up(p + N * gemm_tiles_n(c->padded_vocab_size) * sizeof(float2), 256);  // softmax statistics
+  w.stats = p; p = round_up(p + N * logits_stat_blocks(c->padded_vocab_size) * sizeof(float2), 256);  // softmax statistics
   w.total = p;
   return w;
 }
@@ -520,7 +520,7 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     if (precision == GPT2_FP32)
       launch_softmax(probs, logits, N, V, Vp, s);
     else
-      launch_softmax_from_stats(probs, logits, stats, gemm_tiles_n(Vp), N, V, Vp, s);
+      launch_softmax_from_stats(probs, logits, stats, logits_stat_blocks(Vp), N, V, Vp, s);
   }
   TRY(check_launch());
   TRY(mark(GPT2_STAGE_SOFTMAX));

@@ -9,22 +9,27 @@
 // CTAs run as pairs (clusters of two): a pair owns a 256 x 256 tile, each
 // CTA loads its 128 rows of A and one half (128 rows) of the B tile, and
 // the even CTA issues the pair MMA (tcgen05 cta_group::2, M = 256) that
-// writes each CTA's 128 rows into its own TMEM.  A single CTA's MMA runs at
-// about half the SM's tensor rate; the pair form reaches the full rate and
-// halves the B bytes each SM loads.  Small M uses one CTA per 128 x 256 tile.
+// writes each CTA's 128 rows into its own TMEM.  The pair form runs at the
+// full tensor rate (a 256 x 256 x 16 instruction per ~130 cycles, measured)
+// and halves the B bytes each SM loads.  Small M uses one CTA per 128 x 256
+// tile.
 //   warp 0      TMA producer: 128 x 128-byte A and 256 (single) or 128
-//               (pair) x 128-byte B boxes (128-byte swizzle) into a 4-stage
-//               (single) or 6-stage (pair) shared-memory ring;
-//   warp 1      allocates 512 TMEM columns, and one lane (in a pair: of the
-//               even CTA) issues tcgen05.mma (128 or 256 x 256 x 16 for bf16
-//               or fp16 operands, x 8 for tf32, per instruction) into one of
-//               two 256-column fp32 TMEM accumulators;
-//   warps 2-5   epilogue: tcgen05.ld 32 columns of their 32 TMEM lanes,
+//               (pair) x 128-byte B boxes (128-byte swizzle) into a 3-stage
+//               (single) or 5-stage (pair) shared-memory ring;
+//   warp 1      allocates 512 TMEM columns and (in a pair: the even CTA's)
+//               issues tcgen05.mma (128 or 256 x 256 x 16 for bf16 or fp16
+//               operands, x 8 for tf32, per instruction) into one of two
+//               256-column fp32 TMEM accumulators; the warp runs the loop,
+//               one elected lane issues;
+//   warps 2-9   epilogue, two warps per TMEM lane quadrant, each on half of
+//               the tile's columns: tcgen05.ld 32 columns of their 32 lanes,
 //               add bias, apply GELU or add the residual (TMA-loaded), stage
-//               the tile in swizzled shared memory and TMA-store it.  The
-//               LM-head epilogue also leaves, per row and per 256-column
-//               tile, the maximum and the sum of exp(logit - maximum) over
-//               the real vocabulary, so that the softmax needs one pass.
+//               in swizzled shared memory and TMA-store.  Eight warps, not
+//               four: with four the epilogue of a tile took longer than its
+//               MMAs (measured).  The LM-head epilogue also leaves, per row
+//               and per 128 columns, the maximum and the sum of
+//               exp(logit - maximum) over the real vocabulary, so that the
+//               softmax needs one pass.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
 // i+1.  Tiles are walked M-fastest so that concurrently running CTAs share
 // one weight tile (B) while the activation matrix (A) stays in L2.
@@ -40,24 +45,24 @@ namespace {
 constexpr int kBM = 128;  // rows of A (and of D) per CTA
 constexpr int kBN = 256;  // columns of D per tile
 constexpr int kRowBytes = 128;  // one swizzle atom row: 64 bf16 or 32 fp32 of K
-constexpr int kEpiWarps = 4;
-constexpr int kStageBufBytes = 32 * 128;  // 32 rows x 128 bytes
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, each on half the tile's columns
+constexpr int kStageBufBytes = 32 * 128;  // an epilogue warp's output staging: 32 rows x 128 bytes
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 
 // Shared-memory layout of a CTA, single (kPair false) or one of a pair.
 template <bool kPair>
 struct Layout {
-  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kStages = kPair ? 6 : 3;
   static constexpr int kBRows = kPair ? kBN / 2 : kBN;  // B rows this CTA loads per stage
   static constexpr int kAStageBytes = kBM * kRowBytes;
   static constexpr int kBStageBytes = kBRows * kRowBytes;
   static constexpr int a_off = 0;
   static constexpr int b_off = a_off + kStages * kAStageBytes;
   static constexpr int stg_off = b_off + kStages * kBStageBytes;
-  static constexpr int bar_off = stg_off + kEpiWarps * 2 * kStageBufBytes;
-  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], res[kEpiWarps*2], drain
-  static constexpr int n_bars = 2 * kStages + 4 + 2 * kEpiWarps + 1;
+  static constexpr int bar_off = stg_off + kEpiWarps * kStageBufBytes;
+  // barriers: full[S], empty[S], tmem_full[2], tmem_empty[2], res[kEpiWarps], drain
+  static constexpr int n_bars = 2 * kStages + 4 + kEpiWarps + 1;
   static constexpr int misc_off = bar_off + n_bars * 8;
   static constexpr int total = misc_off + 16;
   static constexpr int alloc = total + 1024;  // slack for 1024-byte alignment
@@ -65,6 +70,9 @@ struct Layout {
 static_assert(Layout<false>::alloc <= 232448 && Layout<true>::alloc <= 232448, "shared memory budget");
 
 __host__ __device__ constexpr int gridDim_n(int N) { return (N + kBN - 1) / kBN; }
+// LM-head softmax statistics per row: one (max, sum) per half tile (the
+// columns one epilogue warp covers)
+__host__ __device__ constexpr int stat_blocks(int N) { return 2 * gridDim_n(N); }
 
 template <int kEpi, int kOp, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -84,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tmem_full = bars + 2 * kStages;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* res_bar = tmem_empty + 2;
-  uint64_t* drain_bar = res_bar + 2 * kEpiWarps;
+  uint64_t* drain_bar = res_bar + kEpiWarps;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc_off + 4);
 
@@ -112,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_full[a], 1);
       mbar_init(&tmem_empty[a], kPair ? 2 * kEpiWarps : kEpiWarps);  // pair: both CTAs' epilogues
     }
-    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(&res_bar[i], 1);
+    for (int i = 0; i < kEpiWarps; ++i) mbar_init(&res_bar[i], 1);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -251,17 +259,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int ew = warp - 2;            // epilogue warp index 0..3
+    const int ew = warp - 2;            // epilogue warp index 0..7
     const int quad = warp & 3;          // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32;  // tile rows [row_in_tile, row_in_tile + 32)
-    uint8_t* stg0 = smem + L::stg_off + ew * 2 * kStageBufBytes;
-    uint32_t res_phase = 0;  // bit b: parity of the next residual load into buffer b
-    uint32_t chunk_ctr = 0;
+    const int col_half = ew >> 2;       // tile columns [128 col_half, 128 col_half + 128)
+    uint8_t* stg = smem + L::stg_off + ew * kStageBufBytes;
+    uint32_t res_phase = 0;  // parity of this warp's next residual load
+    // The bias of this warp's 128 columns of a tile, lane l holding columns
+    // 4l .. 4l + 3 (zero past N), loaded a tile ahead and handed out by
+    // shuffles: with most of the SM's shared memory in use the L1 cache is
+    // small, and a load per chunk would wait on L2 every time.
+    auto load_bias = [&](int tile) -> float4 {
+      float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (bias != nullptr && tile < num_tiles) {
+        const int c = (tile / tiles_m) * kBN + col_half * (kBN / 2) + 4 * lane;
+        if (c + 3 < N) {
+          r = __ldg(reinterpret_cast<const float4*>(bias + c));
+        } else {
+          if (c < N) r.x = __ldg(bias + c);
+          if (c + 1 < N) r.y = __ldg(bias + c + 1);
+          if (c + 2 < N) r.z = __ldg(bias + c + 2);
+        }
+      }
+      return r;
+    };
+    float4 bias_cur = load_bias(unit);
     int local = 0;
-    for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units, ++local) {
+    for (int tile = unit; tile < num_tiles && __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
+         tile += n_units, ++local) {  // one read for the whole warp: it must not split
       const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      const float4 bias_next = load_bias(tile + n_units);
       // every lane waits; the outcome is made warp-uniform so that the
       // .sync.aligned tcgen05 instructions below never run divergent
       if (!__all_sync(0xffffffffu, mbar_wait(&tmem_full[acc], acc_phase))) {
@@ -274,21 +303,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
       constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
       constexpr int kChunkCols = kOutF32 ? 32 : 64;  // 128 bytes of output per row
-      bool ok = true;
       // logits epilogue: this row's running max and sum of exp over the
       // tile's columns below V
       float run_m = -INFINITY, run_s = 0.f;
 #pragma unroll 1
-      for (int ch = 0; ch < kBN / kChunkCols; ++ch) {
-        const int buf = chunk_ctr & 1;
-        uint8_t* stg = stg0 + buf * kStageBufBytes;
+      for (int ch = col_half * (kBN / kChunkCols / 2); ch < (col_half + 1) * (kBN / kChunkCols / 2); ++ch) {
         const int col0 = n0 + ch * kChunkCols;
-        if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer is done
-        __syncwarp();
-        if constexpr (kEpi == kEpiResidF32) {
+        bool ok = true;
+        if constexpr (kEpi == kEpiResidF32) {  // the residual tile into the staging buffer
           if (lane == 0) {
-            mbar_arrive_expect_tx(&res_bar[ew * 2 + buf], kStageBufBytes);
-            tma_load_2d(stg, &tmap_out, &res_bar[ew * 2 + buf], col0, m0);
+            bulk_wait_group_read<0>();  // the previous store has read the buffer
+            mbar_arrive_expect_tx(&res_bar[ew], kStageBufBytes);
+            tma_load_2d(stg, &tmap_out, &res_bar[ew], col0, m0);
           }
         }
         float v[kChunkCols];
@@ -306,20 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (bias != nullptr) {
-          if (col0 + kChunkCols <= N) {
-            const float4* b4 = reinterpret_cast<const float4*>(bias + col0);
+          const int src0 = (ch * kChunkCols - col_half * (kBN / 2)) / 4;  // lane holding the chunk's column 0
 #pragma unroll
-            for (int j = 0; j < kChunkCols / 4; ++j) {
-              const float4 bb = __ldg(b4 + j);
-              v[4 * j] += bb.x;
-              v[4 * j + 1] += bb.y;
-              v[4 * j + 2] += bb.z;
-              v[4 * j + 3] += bb.w;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < kChunkCols; ++j)
-              if (col0 + j < N) v[j] += __ldg(bias + col0 + j);
+          for (int j = 0; j < kChunkCols / 4; ++j) {
+            v[4 * j] += __shfl_sync(0xffffffffu, bias_cur.x, src0 + j);
+            v[4 * j + 1] += __shfl_sync(0xffffffffu, bias_cur.y, src0 + j);
+            v[4 * j + 2] += __shfl_sync(0xffffffffu, bias_cur.z, src0 + j);
+            v[4 * j + 3] += __shfl_sync(0xffffffffu, bias_cur.w, src0 + j);
           }
         }
         if constexpr (kEpi == kEpiLogits) {
@@ -337,12 +356,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             run_s = acc;
           }
         }
+        // Stage the chunk (32 rows x 128 bytes, 128-byte swizzle) in this
+        // warp's buffer and TMA-store it.  One buffer per warp: the store of
+        // the previous chunk has had this chunk's loads and math to read it.
+        if (kEpi != kEpiResidF32 && lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
         const int sw = lane & 7;
         uint8_t* my_row = stg + lane * 128;
         if constexpr (kOutF32) {
           if constexpr (kEpi == kEpiResidF32) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&res_bar[ew * 2 + buf], (res_phase >> buf) & 1u));
-            res_phase ^= 1u << buf;
+            ok = __all_sync(0xffffffffu, mbar_wait(&res_bar[ew], res_phase));
+            res_phase ^= 1u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 old = *reinterpret_cast<const float4*>(my_row + ((j ^ sw) << 4));
@@ -379,12 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_2d(&tmap_out, stg, col0, m0);
           bulk_commit_group();
         }
-        ++chunk_ctr;
-        if (!ok) break;
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
       }
       if constexpr (kEpi == kEpiLogits) {
         const int row = m0 + lane;
-        if (row < M) row_stats[static_cast<size_t>(row) * gridDim_n(N) + n_blk] = make_float2(run_m, run_s);
+        if (row < M) row_stats[static_cast<size_t>(row) * stat_blocks(N) + 2 * n_blk + col_half] = make_float2(run_m, run_s);
       }
       // this warp is done reading the accumulator
       tc_fence_before();
@@ -395,10 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           mbar_arrive(&tmem_empty[acc]);
       }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
+      bias_cur = bias_next;
     }
     if (lane == 0) bulk_wait_group<0>();  // stores complete before the CTA exits
     __syncwarp();
@@ -584,6 +607,6 @@ int launch_gemm_logits(float* logits, float2* row_stats, const void* A, const vo
   return GPT2_ERR_UNSUPPORTED;
 }
 
-int gemm_tiles_n(int N) { return gridDim_n(N); }
+int logits_stat_blocks(int N) { return stat_blocks(N); }
 
 }  // namespace gpt2

@@ -63,12 +63,12 @@ enum OperandType { kOpBF16 = 0, kOpF16 = 1, kOpTF32 = 2 };
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s);
 
-// The LM head: logits = A B^T (no bias) and row_stats[row * tiles + tile] =
-// (max, sum of exp(x - max)) over the tile's columns < V, tiles =
-// gemm_tiles_n(N).
+// The LM head: logits = A B^T (no bias) and row_stats[row * blocks + i] =
+// (max, sum of exp(x - max)) over the columns < V of column block i (128
+// columns), blocks = logits_stat_blocks(N) (a block past V holds (-inf, 0)).
 int launch_gemm_logits(float* logits, float2* row_stats, const void* A, const void* B, int M, int N, int K, int V,
                        int op, cudaStream_t s);
-int gemm_tiles_n(int N);
+int logits_stat_blocks(int N);
 // Softmax from those statistics: one read of the logits, one write.
 void launch_softmax_from_stats(float* probs, const float* logits, const float2* row_stats, int tiles, int N, int V,
                                int Vp, cudaStream_t s);
