@@ -31,8 +31,11 @@
 //               exp(logit - maximum) over the real vocabulary, so that the
 //               softmax needs one pass.
 // Two TMEM accumulators let the epilogue of tile i overlap the MMAs of tile
-// i+1.  Tiles are walked M-fastest so that concurrently running CTAs share
-// one weight tile (B) while the activation matrix (A) stays in L2.
+// i+1.  Tiles are walked M-fastest, so that concurrently running CTAs share
+// one weight tile (B) while the activation matrix (A) stays in L2, unless A
+// is too large for L2 and B small (the MLP down-projection: A is 100 MB at
+// 16 x 1024 tokens): then N-fastest, so that the few tiles that read one
+// block of A run together and A crosses HBM once.
 // Every wait is bounded (about one second); on a timeout the CTA records
 // GPT2_DEVERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and exits.
 #include <mutex>
@@ -78,7 +81,7 @@ template <int kEpi, int kOp, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
-                   int K, int tiles_m, int num_tiles, float2* __restrict__ row_stats, int V) {
+                   int K, int tiles_m, int num_tiles, int n_fast, float2* __restrict__ row_stats, int V) {
   using L = Layout<kPair>;
   constexpr int kStages = L::kStages;
   constexpr int kAStageBytes = L::kAStageBytes;
@@ -110,6 +113,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operand format field: fp16 0, bf16 1 (kind::f16), tf32 2 (kind::tf32)
   constexpr uint32_t kIdesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kTileM, kBN);
   const int num_kb = (K + kBKElems - 1) / kBKElems;
+  // tile index -> (row block, column block): M-fastest (concurrent tiles
+  // share a weight tile) or, with n_fast, N-fastest (they share an
+  // activation block: for a large A and a small B)
+  const int tiles_n = num_tiles / tiles_m;
+  auto tile_m = [&](int tile) { return n_fast ? tile / tiles_n : tile % tiles_m; };
+  auto tile_n = [&](int tile) { return n_fast ? tile % tiles_n : tile / tiles_m; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       uint32_t filled = 0, fill_parity = 0;  // per stage: ever filled, parity of its last fill
       for (int tile = unit; tile < num_tiles && !*abort_flag; tile += n_units) {
-        const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
+        const int m_blk = tile_m(tile), n_blk = tile_n(tile);
         const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = n_blk * kBN + static_cast<int>(rank) * L::kBRows;
         bool ok = true;
@@ -272,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_bias = [&](int tile) -> float4 {
       float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
       if (bias != nullptr && tile < num_tiles) {
-        const int c = (tile / tiles_m) * kBN + col_half * (kBN / 2) + 4 * lane;
+        const int c = tile_n(tile) * kBN + col_half * (kBN / 2) + 4 * lane;
         if (c + 3 < N) {
           r = __ldg(reinterpret_cast<const float4*>(bias + c));
         } else {
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int local = 0;
     for (int tile = unit; tile < num_tiles && __shfl_sync(0xffffffffu, *abort_flag, 0) == 0;
          tile += n_units, ++local) {  // one read for the whole warp: it must not split
-      const int m_blk = tile % tiles_m, n_blk = tile / tiles_m;
+      const int m_blk = tile_m(tile), n_blk = tile_n(tile);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const float4 bias_next = load_bias(tile + n_units);
@@ -520,6 +529,8 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const int tiles_m = (M + kTileM - 1) / kTileM;
   const int tiles_n = (N + kBN - 1) / kBN;
   const int num_tiles = tiles_m * tiles_n;
+  const size_t a_bytes = static_cast<size_t>(M) * K * eb, b_bytes = static_cast<size_t>(N) * K * eb;
+  const int n_fast = (a_bytes > (48u << 20) && b_bytes < (32u << 20)) ? 1 : 0;
   auto kern = gemm_tc_kernel<kEpi, kOp, kPair>;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads);
@@ -553,7 +564,7 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const int units = num_tiles < resident[dev] ? num_tiles : resident[dev];
   cfg.gridDim = dim3(kPair ? 2 * units : units);
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, row_stats, V);
+      cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, n_fast, row_stats, V);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 
