@@ -215,11 +215,6 @@ __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_add
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Orders this thread's memory operations at cluster scope; after a wait
-// that observed another CTA's release arrival it makes what that CTA wrote
-// before arriving visible here.
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
 // mbar_wait with acquire semantics at cluster scope: what the arriving
 // threads of the other CTA wrote before their release arrival is visible.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
