@@ -491,6 +491,14 @@ __device__ __forceinline__ float tanh_fast(float x) {
 
 // GELU, tanh form.  The fast variant uses the hardware tanh approximation
 // (relative error near 2^-11) and feeds bf16 outputs only.
+// 2^x from the SFU's approximate base-2 exponential (PTX ex2.approx.ftz:
+// relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float gelu_exact(float x) {
   const float k = 0.7978845608028654f;  // sqrt(2/pi)
   return 0.5f * x * (1.0f + tanhf(k * (x + 0.044715f * x * x * x)));

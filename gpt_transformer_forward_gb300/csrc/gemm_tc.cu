@@ -351,18 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if constexpr (kEpi == kEpiLogits) {
-          float cmax = -INFINITY;
+          // (max, sum of exp) over the chunk's columns below V, folded into
+          // the row's running pair.  Four independent max and sum chains
+          // (one long chain per thread left the epilogue slower than the
+          // MMAs), exp(x - m) as exp2(x log2e - m log2e).
+          constexpr float kLog2e = 1.4426950408889634f;
+          const bool full = col0 + 32 <= V;  // the same for the whole warp
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (col0 + j < V) cmax = fmaxf(cmax, v[j]);
+            if (full || col0 + j < V) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
+          const float cmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
           if (cmax != -INFINITY) {
             const float m_new = fmaxf(run_m, cmax);
-            float acc = run_s * __expf(run_m - m_new);  // 0 while run_m is -inf
+            const float mb = m_new * kLog2e;
+            float s4[4] = {run_s * exp2_approx(run_m * kLog2e - mb), 0.f, 0.f, 0.f};  // 0 while run_m is -inf
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (col0 + j < V) acc += __expf(v[j] - m_new);
+              if (full || col0 + j < V) s4[j & 3] += exp2_approx(fmaf(v[j], kLog2e, -mb));
             run_m = m_new;
-            run_s = acc;
+            run_s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
           }
         }
         // Stage the chunk (32 rows x 128 bytes, 128-byte swizzle) in this
