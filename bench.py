@@ -268,22 +268,40 @@ def run_ours(args):
         ms = float(t.item())
     err = ab.gpt2_get_error()
 
-    # ---- end to end: pinned host tokens in, logits and probabilities out
+    # ---- end to end: pinned host tokens in, logits and probabilities out.
+    # A serving loop: two sets of device outputs, and the device-to-host
+    # copy of step i (6.6 GB at B=16, bound by the host link) runs on a copy
+    # stream while step i + 1 computes; every step's copies are inside the
+    # timed region, the last one included.
     tok_h = torch.from_numpy(tok).pin_memory()
     logits_h = torch.empty(logits.shape, dtype=torch.float32, pin_memory=True)
     probs_h = torch.empty(probs.shape, dtype=torch.float32, pin_memory=True)
+    bufs = [(logits, probs), model.new_outputs(w.B, w.T)]
+    copy_stream = torch.cuda.Stream()
+    copied = [None, None]  # event: the copy out of buffer set b is done
     e2e_steps = max(3, min(args.steps, 20))
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(e2e_steps):
+    for i in range(e2e_steps):
+        lg, pr = bufs[i & 1]
+        if copied[i & 1] is not None:
+            stream.wait_event(copied[i & 1])
         tok_d.copy_(tok_h, non_blocking=True)
-        model.forward(tok_d, logits, probs)
-        logits_h.copy_(logits, non_blocking=True)
-        probs_h.copy_(probs, non_blocking=True)
+        model.forward(tok_d, lg, pr)
+        computed = torch.cuda.Event()
+        computed.record(stream)
+        copy_stream.wait_event(computed)
+        with torch.cuda.stream(copy_stream):
+            logits_h.copy_(lg, non_blocking=True)
+            probs_h.copy_(pr, non_blocking=True)
+        copied[i & 1] = torch.cuda.Event()
+        copied[i & 1].record(copy_stream)
+    stream.wait_stream(copy_stream)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
+    del bufs
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if pg is not None:
         t = torch.tensor([e2e_ms], device="cuda")
