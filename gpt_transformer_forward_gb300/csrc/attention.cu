@@ -11,8 +11,9 @@
 // into [B, T, C]: no permute or unpermute pass.
 //
 //   attn_tc_kernel      tensor cores (mma.sync m16n8k16 on bf16 or fp16
-//                       operands, fp32 accumulate), head size 16, 32 or 64,
-//                       64 query rows per block;
+//                       operands, fp32 accumulate), head size 16 or 32, 64
+//                       query rows per block (head size 64, GPT-2's, runs
+//                       on the tcgen05 kernel of attention_tc.cu);
 //   attn_f32_kernel     fp32 CUDA cores, reference-grade (GPT2_FP32 mode);
 //   decode kernels      one query per sequence against the KV cache, split
 //                       over positions, then a combine pass.
@@ -396,7 +397,6 @@ static int attention_tc(void* out, bool out16, const void* qkv, int B, int T, in
   switch (C / NH) {
     case 16: attention_tc_hs<16, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
     case 32: attention_tc_hs<32, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
-    case 64: attention_tc_hs<64, T16>(out, out16, qkv, B, T, C, NH, s); return GPT2_OK;
   }
   return GPT2_ERR_UNSUPPORTED;
 }

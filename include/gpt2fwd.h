@@ -71,8 +71,10 @@ typedef struct {
  *              normalised activations and 0.02-scale weights.
  * In the 16-bit modes the operand buffers internal to gpt2_forward (and
  * the KV cache) hold the 16-bit type, since the tensor cores would round
- * them to it anyway; the residual stream, logits and probabilities stay
- * fp32.  Accumulation is fp32 in every mode. */
+ * them to it anyway, and so do the attention and MLP projections' outputs
+ * before the residual add (performed in the LayerNorm that follows); the
+ * residual stream, logits and probabilities stay fp32.  Accumulation is
+ * fp32 in every mode. */
 typedef enum { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2, GPT2_FP16 = 3 } GPT2Precision;
 
 enum {
@@ -242,13 +244,16 @@ GPT2_API int gpt2_decode_step(const GPT2Config* cfg, const float* params, const 
 /* Stages of the forward pass, for gpt2_forward_profile. */
 enum {
   GPT2_STAGE_ENCODER = 0,
-  GPT2_STAGE_LN1 = 1,       /* all L layers summed, likewise below */
+  GPT2_STAGE_LN1 = 1,       /* all L layers summed, likewise below; in the
+                               16-bit modes LN1 of layers 1.. and LN2 and
+                               LN_f also add the preceding projection's
+                               output into the residual stream */
   GPT2_STAGE_QKV = 2,       /* QKV GEMM (+ cache store when caching) */
   GPT2_STAGE_ATTENTION = 3,
-  GPT2_STAGE_ATTPROJ = 4,   /* attention projection GEMM + residual */
+  GPT2_STAGE_ATTPROJ = 4,   /* attention projection GEMM (+ residual in the fp32 and tf32 modes) */
   GPT2_STAGE_LN2 = 5,
   GPT2_STAGE_FC = 6,        /* MLP up-projection GEMM + GELU */
-  GPT2_STAGE_FCPROJ = 7,    /* MLP down-projection GEMM + residual */
+  GPT2_STAGE_FCPROJ = 7,    /* MLP down-projection GEMM (+ residual in the fp32 and tf32 modes) */
   GPT2_STAGE_LNF = 8,
   GPT2_STAGE_LMHEAD = 9,
   GPT2_STAGE_SOFTMAX = 10,
