@@ -188,6 +188,30 @@ def dist_setup(n_gpus):
     return rank, world, local, pg
 
 
+def rank_tokens(w, tok, rank):
+    """The token batch of replica `rank`: the workload's own on rank 0, a
+    differently seeded batch of the same shape on every other rank."""
+    if rank == 0:
+        return tok
+    return inputs.make_tokens(w.token_seed + 7919 * rank, w.B, w.T, w.cfg.vocab_size)
+
+
+def max_over_ranks(value, pg, device):
+    """The largest of every rank's `value` (a float), on every rank; `device`
+    holds the reduction tensor ("cuda" with NCCL, "cpu" with gloo)."""
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_rank, ms_per_step):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def run_reference(args):
     rank, world, _, pg = dist_setup(args.gpus)
     if rank != 0:
@@ -231,8 +255,7 @@ def run_ours(args):
     w = inputs.WORKLOADS[args.workload]
     precision = ab.PRECISIONS[args.precision]
     params, tok = inputs.workload_inputs(w)
-    if rank > 0:  # replicas: each rank its own batch of token ids
-        tok = inputs.make_tokens(w.token_seed + 7919 * rank, w.B, w.T, w.cfg.vocab_size)
+    tok = rank_tokens(w, tok, rank)  # replicas: each rank its own batch of token ids
     model = GPT2Model(w.cfg, params, w.B, w.T, precision)
     logits, probs = model.new_outputs(w.B, w.T)
     tok_d = torch.from_numpy(tok).cuda()
@@ -261,11 +284,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if pg is not None:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
     err = ab.gpt2_get_error()
 
     # ---- end to end: pinned host tokens in, logits and probabilities out.
@@ -302,11 +321,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     del bufs
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, pg, "cuda")
 
     # ---- per-stage times (CUDA events between stages) and the roofline
     prof_runs = 5
@@ -341,7 +356,7 @@ def run_ours(args):
     roof["peak_source"] = peak_src
 
     tokens = w.B * w.T
-    value = world * tokens / (ms * 1e-3)
+    value = job_tokens_per_s(world, tokens, ms)
     launches_per_step = 1 + 7 * w.cfg.num_layers + 3
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -354,7 +369,7 @@ def run_ours(args):
                    "channels": w.cfg.channels, "heads": w.cfg.num_heads, "vocab": w.cfg.vocab_size,
                    "padded_vocab": w.cfg.padded_vocab_size, "outputs": "logits+probs",
                    "l2": "no flush: working set > 7 GB, L2 129 MB", "parallelism": f"replicas{world}"},
-        "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": UNIT,
+        "e2e": {"value": job_tokens_per_s(world, tokens, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": int(tok.nbytes), "d2h_bytes_per_step": int(logits.numel() * 4 * 2)},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
