@@ -1,7 +1,7 @@
 """Benchmark of the GPT-2 forward pass on GB300: one JSON line on stdout.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2-124m-b16] [--precision bf16]
+                    [--workload gpt2-124m-b16] [--precision fp16] [--gemm-diag]
 
 A step is one gpt2_forward over a batch of B sequences of T tokens of
 seeded synthetic input (random-init GPT-2 weights, uniform token ids), with
@@ -18,6 +18,11 @@ touches the data path, and scaling is weak.
 --impl reference times the CPU oracle (the plain double-precision C
 implementation) on the host cores, on a bounded sample of the same workload
 per step; rank 0 alone runs it.
+
+--workload gpt2-124m-decode measures KV-cached decoding instead: per run a
+prefill of 32 prompts of 512 tokens (reported apart), then 128 greedy steps
+(argmax + gpt2_decode_step), K runs timed; value = decoded tokens/s.
+--gemm-diag adds each GEMM site's time beside cuBLAS at the same shape.
 """
 from __future__ import annotations
 
@@ -188,6 +193,43 @@ def dist_setup(n_gpus):
     return rank, world, local, pg
 
 
+def gemm_vs_library(cfg, N, stage_ms):
+    """Diagnostic (--gemm-diag): per GEMM site, this library's time per launch
+    (its stage time from gpt2_forward_profile, epilogue included) beside the
+    vendor library's plain fp16 matrix product of the same shape
+    (torch.matmul: cuBLAS; fp16 out, fp32 out for the LM head)."""
+    import torch
+    C, L, Vp = cfg.channels, cfg.num_layers, cfg.padded_vocab_size
+    sites = {"qkv": (C, 3 * C, L), "attproj": (C, C, L), "fc": (C, 4 * C, L), "fcproj": (4 * C, C, L),
+             "lm_head": (C, Vp, 1)}
+    out = {}
+    for name, (K, OC, launches) in sites.items():
+        a = torch.randn(N, K, device="cuda", dtype=torch.float16)
+        wt = torch.randn(OC, K, device="cuda", dtype=torch.float16)
+        f32 = name == "lm_head"
+        f = (lambda: torch.mm(a, wt.t(), out_dtype=torch.float32)) if f32 else (lambda: a @ wt.t())
+        try:
+            f()
+        except (TypeError, RuntimeError):  # no fp32-output matmul in this torch: fp16 out
+            f32 = False
+            f = lambda: a @ wt.t()
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(10):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        lib_us = e0.elapsed_time(e1) / 10 * 1e3
+        ours_us = stage_ms[name] / launches * 1e3
+        out[name] = {"shape_mnk": [N, OC, K], "ours_us": round(ours_us, 1), "cublas_us": round(lib_us, 1),
+                     "cublas_out": "fp32" if f32 else "fp16"}
+        del a, wt
+    return out
+
+
 def rank_tokens(w, tok, rank):
     """The token batch of replica `rank`: the workload's own on rank 0, a
     differently seeded batch of the same shape on every other rank."""
@@ -244,16 +286,85 @@ def run_reference(args):
         pg.barrier()
 
 
-def run_ours(args):
+DECODE_METRIC = "GPT-2 124M KV-cached decode tokens/s (B=32, prompt 512, 128 greedy steps) on 1 GB300"
+
+
+def run_decode(args, w, precision):
+    """The KV-cached decode workload: per run, a prefill of the B prompts of T
+    tokens (gpt2_forward filling the cache; timed and reported apart), then
+    w.decode_steps steps of greedy argmax + gpt2_decode_step (timed).  K runs
+    after W warm-up runs; tokens/s = B x steps x K / decode time."""
     import torch
     from gpt_transformer_forward_gb300 import binding as ab
     from gpt_transformer_forward_gb300.runner import GPT2Model
 
     rank, world, local, pg = dist_setup(args.gpus)
     torch.cuda.set_device(local)
-    dev_index = torch.cuda.current_device()
+    params, tok = inputs.workload_inputs(w)
+    tok = rank_tokens(w, tok, rank)
+    cfg, B, T, n = w.cfg, w.B, w.T, w.decode_steps
+    model = GPT2Model(cfg, params, B, T, precision)
+    cache = model.new_kvcache(B)
+    tok_d = torch.from_numpy(tok).cuda()
+    prefill_logits, _ = model.new_outputs(B, T, probs=False)
+    last = torch.empty((B, cfg.padded_vocab_size), dtype=torch.float32, device="cuda")
+    logits, probs = model.new_outputs(B, None)
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    prefill_ms = decode_ms = 0.0
+    for run in range(args.warmup + args.steps):
+        cache.zero_()
+        p0.record(stream)
+        model.forward(tok_d, prefill_logits, None, cache)
+        p1.record(stream)
+        last.copy_(prefill_logits[:, T - 1])
+        e0.record(stream)
+        src = last
+        for i in range(n):
+            ab.gpt2_argmax(nxt, src, B, cfg.vocab_size, cfg.padded_vocab_size)
+            model.decode_step(cache, nxt, T + i, logits, probs)
+            src = logits
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if run >= args.warmup:
+            prefill_ms += p0.elapsed_time(p1)
+            decode_ms += e0.elapsed_time(e1)
+    err = ab.gpt2_get_error()
+    decode_ms = max_over_ranks(decode_ms, pg, "cuda")
+    tokens = B * n * args.steps
+    line = {
+        "metric": DECODE_METRIC, "value": job_tokens_per_s(world, tokens, decode_ms), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": decode_ms / (args.steps * n),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.precision,
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "prompt": T, "decode_steps": n, "layers": cfg.num_layers,
+                   "outputs": "logits+probs per step, greedy argmax", "parallelism": f"replicas{world}"},
+        "prefill_ms": prefill_ms / args.steps,
+        # per step: argmax, encoder, 9 per layer (LN, QKV, cache store, attention
+        # partials + combine, projection, LN, FC, FC-proj), LN_f, LM head, softmax
+        "gpu_launches": (9 * cfg.num_layers + 5) * n * args.steps,
+        "device_error_word": err,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def run_ours(args):
+    import torch
+    from gpt_transformer_forward_gb300 import binding as ab
+    from gpt_transformer_forward_gb300.runner import GPT2Model
+
     w = inputs.WORKLOADS[args.workload]
     precision = ab.PRECISIONS[args.precision]
+    if w.decode_steps:
+        return run_decode(args, w, precision)
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev_index = torch.cuda.current_device()
     params, tok = inputs.workload_inputs(w)
     tok = rank_tokens(w, tok, rank)  # replicas: each rank its own batch of token ids
     model = GPT2Model(w.cfg, params, w.B, w.T, precision)
@@ -380,6 +491,8 @@ def run_ours(args):
         "device_error_word": err,
         "cpu_baseline": cpu,
     }
+    if args.gemm_diag and rank == 0:
+        line["gemm_vs_cublas"] = gemm_vs_library(w.cfg, w.B * w.T, stage_ms)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -395,6 +508,8 @@ def main():
     ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--precision", default="fp16", choices=["fp16", "bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gemm-diag", action="store_true",
+                    help="add each GEMM site's time beside cuBLAS at the same shape (diagnostic)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")
