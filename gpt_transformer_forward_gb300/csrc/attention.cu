@@ -331,13 +331,26 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __re
   const int chunk = split * kDecWarps + warp;
   const int j = chunk * kDecPos + lane;
   const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
+  // score of position j: this lane's K row in 16-byte loads (all in flight
+  // together)
+  constexpr int kPer16 = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte load
   float sc = -INFINITY;
   if (j <= pos) {
-    const E* krow = kcache + (head + j) * HS;
-    float dot = 0.f;
+    const uint4* krow = reinterpret_cast<const uint4*>(kcache + (head + j) * HS);
+    uint4 kv[HS / kPer16];
 #pragma unroll
-    for (int d = 0; d < HS; ++d) dot = fmaf(q_s[d], to_f32(krow[d]), dot);
-    sc = dot * scale;
+    for (int i = 0; i < HS / kPer16; ++i) kv[i] = __ldg(krow + i);
+    float dot0 = 0.f, dot1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < HS / kPer16; ++i) {
+      const E* e = reinterpret_cast<const E*>(&kv[i]);
+#pragma unroll
+      for (int k = 0; k < kPer16; k += 2) {
+        dot0 = fmaf(q_s[kPer16 * i + k], to_f32(e[k]), dot0);
+        dot1 = fmaf(q_s[kPer16 * i + k + 1], to_f32(e[k + 1]), dot1);
+      }
+    }
+    sc = (dot0 + dot1) * scale;
   }
   const float mx = warp_max(sc);
   const float p = (j <= pos) ? __expf(sc - mx) : 0.f;
@@ -347,11 +360,26 @@ __global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __re
   const int nchunks = gridDim.x * kDecWarps;
   float* part = scratch + ((static_cast<size_t>(b) * NH + h) * nchunks + chunk) * (HS + 2);
   const int jmax = min(kDecPos, pos + 1 - chunk * kDecPos);  // valid positions in this chunk (may be <= 0)
-  for (int d = lane; d < HS; d += 32) {
-    float acc = 0.f;
-    for (int r = 0; r < jmax; ++r)
-      acc = fmaf(p_s[warp][r], to_f32(vcache[(head + chunk * kDecPos + r) * HS + d]), acc);
-    part[2 + d] = acc;
+  // P V over the chunk: lane l owns dimensions kDPL l .. kDPL l + kDPL - 1
+  // (a warp reads whole V rows); the position loop is unrolled so that its
+  // loads are all in flight at once
+  constexpr int kDPL = HS >= 32 ? HS / 32 : 1;
+  const bool owns = lane * kDPL < HS;
+  const E* vbase = vcache + (head + chunk * kDecPos) * HS + lane * kDPL;
+  float acc[kDPL];
+#pragma unroll
+  for (int k = 0; k < kDPL; ++k) acc[k] = 0.f;
+#pragma unroll
+  for (int r = 0; r < kDecPos; ++r) {
+    if (r < jmax && owns) {
+      const float pr = p_s[warp][r];
+#pragma unroll
+      for (int k = 0; k < kDPL; ++k) acc[k] = fmaf(pr, to_f32(__ldg(vbase + static_cast<size_t>(r) * HS + k)), acc[k]);
+    }
+  }
+  if (owns) {
+#pragma unroll
+    for (int k = 0; k < kDPL; ++k) part[2 + lane * kDPL + k] = acc[k];
   }
   if (lane == 0) {
     part[0] = (jmax > 0) ? mx : -INFINITY;

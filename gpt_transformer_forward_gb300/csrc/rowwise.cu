@@ -453,13 +453,36 @@ __global__ void __launch_bounds__(512) argmax_kernel(int* __restrict__ next, con
   const float* row = logits + static_cast<size_t>(blockIdx.x) * Vp;
   float best = -INFINITY;
   int bi = 0x7fffffff;
-  for (int c = threadIdx.x; c < V; c += blockDim.x) {
-    const float x = row[c];
+  auto take = [&](float x, int c) {
     if (x > best) {  // strictly greater: within a thread indices increase
       best = x;
       bi = c;
     }
+  };
+  int c0 = 0;  // columns below c0 are done by the vector loop
+  if ((Vp & 3) == 0) {
+    // 16-byte loads, four per thread per round so that they are in flight
+    // together; a thread still visits its columns in increasing order
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    const int n4 = V / 4, stride = blockDim.x;
+    for (int base = threadIdx.x; base < n4; base += 4 * stride) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (base + u * stride < n4) v[u] = __ldcs(row4 + base + u * stride);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (base + u * stride < n4) {
+          const int c = 4 * (base + u * stride);
+          take(v[u].x, c);
+          take(v[u].y, c + 1);
+          take(v[u].z, c + 2);
+          take(v[u].w, c + 3);
+        }
+    }
+    c0 = 4 * n4;
   }
+  for (int c = c0 + threadIdx.x; c < V; c += blockDim.x) take(row[c], c);
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

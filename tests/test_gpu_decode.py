@@ -50,6 +50,20 @@ def test_tiny_decode_matches_oracle(precision):
     assert_close(steps, full[:, 20:40], atol=LOGIT_TOL[precision], what="decode vs recompute")
 
 
+@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_FP32])
+def test_decode_head_size_32(precision):
+    # head size 32 (C=128, 4 heads): one dimension per lane in the decode
+    # kernel's P V; positions 40..89 span several 32-position chunks
+    cfg = inputs.GPT2Config(max_seq_len=128, vocab_size=300, padded_vocab_size=304, num_layers=2, num_heads=4,
+                            channels=128)
+    params = inputs.make_params(cfg, 94, "perturbed")
+    tok = inputs.make_tokens(95, 2, 90, cfg.vocab_size)
+    m = GPT2Model(cfg, params, 2, 90, precision)
+    _, steps = teacher_forced(m, cfg, tok, 40, 50)
+    full, _ = oracle.forward(cfg, params, tok, want_probs=False)
+    assert_close(steps, full[:, 40:90], atol=LOGIT_TOL[precision], what="head-size-32 decode vs recompute")
+
+
 def test_tiny_decode_from_position_zero():
     cfg = inputs.TINY
     params = inputs.make_params(cfg, 92, "perturbed")
