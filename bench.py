@@ -342,9 +342,9 @@ def run_decode(args, w, precision):
         "config": {"workload": w.name, "B": B, "prompt": T, "decode_steps": n, "layers": cfg.num_layers,
                    "outputs": "logits+probs per step, greedy argmax", "parallelism": f"replicas{world}"},
         "prefill_ms": prefill_ms / args.steps,
-        # per step: argmax, encoder, 9 per layer (LN, QKV, cache store, attention
-        # partials + combine, projection, LN, FC, FC-proj), LN_f, LM head, softmax
-        "gpu_launches": (9 * cfg.num_layers + 5) * n * args.steps,
+        # per step: argmax, encoder, 7 per layer (LN, QKV, attention with the
+        # cache append, projection, LN, FC, FC-proj), LN_f, LM head, softmax
+        "gpu_launches": (7 * cfg.num_layers + 5) * n * args.steps,
         "device_error_word": err,
     }
     if rank == 0:

@@ -152,7 +152,7 @@ PackedOffsets packed_offsets(const GPT2Config* c) {
 
 // ---------------------------------------------------------- workspace
 struct Workspace {
-  size_t x, ln, qkv, qkv16, att, fch, dec, stats, total;  // byte offsets
+  size_t x, ln, qkv, qkv16, att, fch, stats, total;  // byte offsets
 };
 
 Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
@@ -167,7 +167,6 @@ Workspace workspace_layout(const GPT2Config* c, int B, int T, int precision) {
   if (precision == GPT2_TF32) p = round_up(p + N * 3 * C * 2, 256);  // bf16 copy for the attention kernel
   w.att = p; p = round_up(p + N * C * act, 256);
   w.fch = p; p = round_up(p + N * 4 * C * act, 256);
-  w.dec = p; p = round_up(p + decode_attention_scratch_floats(B, c->channels, c->num_heads, c->max_seq_len) * 4, 256);
   w.stats = p; p = round_up(p + N * logits_stat_blocks(c->padded_vocab_size) * sizeof(float2), 256);  // softmax statistics
   w.total = p;
   return w;
@@ -405,7 +404,6 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
   void* qkv = ws + wl.qkv;
   void* att = ws + wl.att;
   void* fch = ws + wl.fch;
-  float* dec_scratch = reinterpret_cast<float*>(ws + wl.dec);
   const bool bf16 = is16(precision);  // 16-bit operand buffers (bf16 or fp16)
   const int op = op_of(precision);
   const PackedOffsets ko = packed_offsets(cfg);
@@ -457,14 +455,13 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     TRY(mark(GPT2_STAGE_LN1));
     TRY(gemm(precision, qkv, ln, wmat(po.qkvw, ko.qkvw, 3 * CC, l), params + po.qkvb + static_cast<size_t>(l) * 3 * C,
              N, 3 * C, C, bf16 ? kEpiOut16 : kEpiF32, s));
-    if (kvcache != nullptr) {
-      const int pos0 = decode_pos < 0 ? 0 : decode_pos;
+    if (kvcache != nullptr && decode_pos < 0) {  // a decode step appends in its attention kernel
       if (bf16)
         launch_kv_store_16(static_cast<uint16_t*>(kvcache) + l * kv_slab, static_cast<const uint16_t*>(qkv), B, T,
-                           C, NH, maxT, pos0, s);
+                           C, NH, maxT, 0, s);
       else
         launch_kv_store_f32(static_cast<float*>(kvcache) + l * kv_slab, static_cast<const float*>(qkv), B, T, C, NH,
-                            maxT, pos0, s);
+                            maxT, 0, s);
     }
     TRY(mark(GPT2_STAGE_QKV));
     if (decode_pos < 0) {
@@ -479,12 +476,12 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
       }
     } else {
       if (bf16) {
-        const uint16_t* kc = static_cast<const uint16_t*>(kvcache) + l * kv_slab;
-        launch_decode_attention_16(att, true, qkv, kc, kc + kv_half, op, B, C, NH, maxT, decode_pos, dec_scratch, s);
+        uint16_t* kc = static_cast<uint16_t*>(kvcache) + l * kv_slab;
+        launch_decode_attention_16(att, true, qkv, kc, kc + kv_half, op, B, C, NH, maxT, decode_pos, s);
       } else {
-        const float* kc = static_cast<const float*>(kvcache) + l * kv_slab;
+        float* kc = static_cast<float*>(kvcache) + l * kv_slab;
         launch_decode_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), kc, kc + kv_half, B, C,
-                                    NH, maxT, decode_pos, dec_scratch, s);
+                                    NH, maxT, decode_pos, s);
       }
     }
     TRY(check_launch());

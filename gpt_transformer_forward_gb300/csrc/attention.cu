@@ -15,8 +15,8 @@
 //                       query rows per block (head size 64, GPT-2's, runs
 //                       on the tcgen05 kernel of attention_tc.cu);
 //   attn_f32_kernel     fp32 CUDA cores, reference-grade (GPT2_FP32 mode);
-//   decode kernels      one query per sequence against the KV cache, split
-//                       over positions, then a combine pass.
+//   decode_attn_kernel  one query per sequence against the KV cache, one
+//                       block per (head, sequence).
 #include "kernels.cuh"
 
 namespace gpt2 {
@@ -308,102 +308,136 @@ __global__ void __launch_bounds__(64) attn_f32_kernel(float* __restrict__ out, c
 }
 
 // ------------------------------------------------------------- decode
-// Phase 1: block (split, h, b) with 4 warps covers 128 cache positions of
-// one (sequence, head); each warp takes 32 of them.  Scores with one lane
-// per position, then the value sum with one lane per pair of dimensions.
-// Each warp leaves (max, sum, o[hs]) in scratch; phase 2 combines them.
-constexpr int kDecPos = 32;   // positions per warp
-constexpr int kDecWarps = 4;  // warps per block
+// One CTA of kDecWarps warps per (head, sequence).  A warp walks chunks of
+// the cache (chunk w, w + kDecWarps, ...) keeping a running maximum, sum and
+// unnormalised output (the online softmax of FlashAttention's Algorithm 1
+// with a single query row).  Each K or V row is read by kLPR lanes with
+// 16-byte loads, kRPI rows per warp instruction (coalesced), and a chunk's
+// K and V loads are all issued before any is used.  At the end the CTA
+// merges its warps' (maximum, sum, output) in shared memory and writes the
+// head's output row: one launch, no scratch.  The token's own key and value
+// (position pos) are read from the QKV row, and the block also appends them
+// to the cache for the steps that follow.
+constexpr int kDecWarps = 4;
 
-template <typename E, int HS>
-__global__ void __launch_bounds__(32 * kDecWarps) decode_attn_kernel(float* __restrict__ scratch,
-                                                                     const E* __restrict__ qkv,
-                                                                     const E* __restrict__ kcache,
-                                                                     const E* __restrict__ vcache, int B, int C,
-                                                                     int NH, int maxT, int pos, float scale) {
-  __shared__ float q_s[HS];
-  __shared__ float p_s[kDecWarps][kDecPos];
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+template <typename E, typename OutT, int HS>
+__global__ void __launch_bounds__(32 * kDecWarps)
+    decode_attn_kernel(OutT* __restrict__ out, const E* __restrict__ qkv, E* __restrict__ kcache,
+                       E* __restrict__ vcache, int C, int NH, int maxT, int pos, float scale_log2) {
+  constexpr int kPer = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte load
+  constexpr int kLPR = HS / kPer;                          // lanes per K or V row
+  constexpr int kRPI = 32 / kLPR;                          // rows per warp instruction
+  constexpr int kIt = 8;                                   // instructions per chunk (each of K, V)
+  constexpr int kChunk = kIt * kRPI;                       // positions per chunk
+  static_assert(kLPR >= 1 && kLPR <= 32 && 32 % kLPR == 0, "head size and element type");
+  __shared__ float m_s[kDecWarps], l_s[kDecWarps];
+  __shared__ float o_s[kDecWarps][HS];
+  const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int d = threadIdx.x; d < HS; d += blockDim.x)
-    q_s[d] = to_f32(qkv[static_cast<size_t>(b) * 3 * C + h * HS + d]);
-  __syncthreads();
-  const int chunk = split * kDecWarps + warp;
-  const int j = chunk * kDecPos + lane;
+  const int g = lane / kLPR;   // row of an instruction this lane reads
+  const int dg = lane % kLPR;  // its dimensions dg * kPer .. dg * kPer + kPer - 1
+  // the query's dimensions of this lane, scaled by log2(e) / sqrt(hs)
+  float q[kPer];
+  {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + h * HS) + dg);
+    const E* e = reinterpret_cast<const E*>(&raw);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) q[k] = to_f32(e[k]) * scale_log2;
+  }
   const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
-  // score of position j: this lane's K row in 16-byte loads (all in flight
-  // together)
-  constexpr int kPer16 = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte load
-  float sc = -INFINITY;
-  if (j <= pos) {
-    const uint4* krow = reinterpret_cast<const uint4*>(kcache + (head + j) * HS);
-    uint4 kv[HS / kPer16];
+  const uint4* kb = reinterpret_cast<const uint4*>(kcache + head * HS) + dg;
+  const uint4* vb = reinterpret_cast<const uint4*>(vcache + head * HS) + dg;
+  // this token's key and value: used for position pos, and appended
+  const uint4* kq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + C + h * HS) + dg;
+  const uint4* vq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + 2 * C + h * HS) + dg;
+  if (threadIdx.x < kLPR) {
+    reinterpret_cast<uint4*>(kcache + (head + pos) * HS)[dg] = __ldg(kq);
+    reinterpret_cast<uint4*>(vcache + (head + pos) * HS)[dg] = __ldg(vq);
+  }
+  float m = -INFINITY, l = 0.f, acc[kPer];
 #pragma unroll
-    for (int i = 0; i < HS / kPer16; ++i) kv[i] = __ldg(krow + i);
-    float dot0 = 0.f, dot1 = 0.f;
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  const int nchunk = pos / kChunk + 1;  // chunks covering positions 0 .. pos
+  for (int c = warp; c < nchunk; c += kDecWarps) {
+    const int j0 = c * kChunk + g;
+    uint4 kr[kIt], vr[kIt];
 #pragma unroll
-    for (int i = 0; i < HS / kPer16; ++i) {
-      const E* e = reinterpret_cast<const E*>(&kv[i]);
-#pragma unroll
-      for (int k = 0; k < kPer16; k += 2) {
-        dot0 = fmaf(q_s[kPer16 * i + k], to_f32(e[k]), dot0);
-        dot1 = fmaf(q_s[kPer16 * i + k + 1], to_f32(e[k + 1]), dot1);
+    for (int i = 0; i < kIt; ++i) {
+      const int j = j0 + i * kRPI;
+      if (j < pos) {
+        kr[i] = __ldg(kb + static_cast<size_t>(j) * kLPR);
+        vr[i] = __ldg(vb + static_cast<size_t>(j) * kLPR);
+      } else if (j == pos) {
+        kr[i] = __ldg(kq);
+        vr[i] = __ldg(vq);
+      } else {
+        kr[i] = make_uint4(0u, 0u, 0u, 0u);
+        vr[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    sc = (dot0 + dot1) * scale;
-  }
-  const float mx = warp_max(sc);
-  const float p = (j <= pos) ? __expf(sc - mx) : 0.f;
-  const float sum = warp_sum(p);
-  p_s[warp][lane] = p;
-  __syncwarp();
-  const int nchunks = gridDim.x * kDecWarps;
-  float* part = scratch + ((static_cast<size_t>(b) * NH + h) * nchunks + chunk) * (HS + 2);
-  const int jmax = min(kDecPos, pos + 1 - chunk * kDecPos);  // valid positions in this chunk (may be <= 0)
-  // P V over the chunk: lane l owns dimensions kDPL l .. kDPL l + kDPL - 1
-  // (a warp reads whole V rows); the position loop is unrolled so that its
-  // loads are all in flight at once
-  constexpr int kDPL = HS >= 32 ? HS / 32 : 1;
-  const bool owns = lane * kDPL < HS;
-  const E* vbase = vcache + (head + chunk * kDecPos) * HS + lane * kDPL;
-  float acc[kDPL];
+    // scores (log2 units) of this lane's kIt rows; the row's kLPR lanes
+    // each hold a partial dot product and sum it by shuffles
+    float sc[kIt];
+    float cmax = -INFINITY;
 #pragma unroll
-  for (int k = 0; k < kDPL; ++k) acc[k] = 0.f;
+    for (int i = 0; i < kIt; ++i) {
+      const E* e = reinterpret_cast<const E*>(&kr[i]);
+      float d = 0.f;
 #pragma unroll
-  for (int r = 0; r < kDecPos; ++r) {
-    if (r < jmax && owns) {
-      const float pr = p_s[warp][r];
+      for (int k = 0; k < kPer; ++k) d = fmaf(q[k], to_f32(e[k]), d);
 #pragma unroll
-      for (int k = 0; k < kDPL; ++k) acc[k] = fmaf(pr, to_f32(__ldg(vbase + static_cast<size_t>(r) * HS + k)), acc[k]);
+      for (int o = kLPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      sc[i] = (j0 + i * kRPI <= pos) ? d : -INFINITY;
+      cmax = fmaxf(cmax, sc[i]);
     }
-  }
-  if (owns) {
 #pragma unroll
-    for (int k = 0; k < kDPL; ++k) part[2 + lane * kDPL + k] = acc[k];
+    for (int o = 16; o >= kLPR; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    // position c * kChunk <= pos is in the chunk, so cmax is finite
+    const float m_new = fmaxf(m, cmax);
+    const float alpha = exp2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
+    l *= alpha;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] *= alpha;
+#pragma unroll
+    for (int i = 0; i < kIt; ++i) {
+      const float p = exp2_approx(sc[i] - m_new);  // 0 past pos
+      l += p;
+      const E* e = reinterpret_cast<const E*>(&vr[i]);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) acc[k] = fmaf(p, to_f32(e[k]), acc[k]);
+    }
+    m = m_new;
+  }
+  // sum over the rows of an instruction: every lane then holds the warp's
+  // sum and its dimensions' output
+#pragma unroll
+  for (int o = 16; o >= kLPR; o >>= 1) {
+    l += __shfl_xor_sync(0xffffffffu, l, o);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
   }
   if (lane == 0) {
-    part[0] = (jmax > 0) ? mx : -INFINITY;
-    part[1] = sum;
+    m_s[warp] = m;
+    l_s[warp] = l;
   }
-}
-
-template <typename OutT, int HS>
-__global__ void decode_combine_kernel(OutT* __restrict__ out, const float* __restrict__ scratch, int C, int NH,
-                                      int nchunks) {
-  const int h = blockIdx.x, b = blockIdx.y;
-  const float* part = scratch + (static_cast<size_t>(b) * NH + h) * nchunks * (HS + 2);
-  float M = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, part[c * (HS + 2)]);
+  if (g == 0) {
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) o_s[warp][dg * kPer + k] = acc[k];
+  }
+  __syncthreads();
   for (int d = threadIdx.x; d < HS; d += blockDim.x) {
-    float L = 0.f, acc = 0.f;
-    for (int c = 0; c < nchunks; ++c) {
-      const float m = part[c * (HS + 2)];
-      if (m == -INFINITY) continue;
-      const float w = __expf(m - M);
-      L += part[c * (HS + 2) + 1] * w;
-      acc += part[c * (HS + 2) + 2 + d] * w;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) M = fmaxf(M, m_s[w]);
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      if (m_s[w] == -INFINITY) continue;  // a warp that had no chunk
+      const float f = exp2_approx(m_s[w] - M);
+      L = fmaf(l_s[w], f, L);
+      O = fmaf(o_s[w][d], f, O);
     }
-    out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(acc / L);
+    out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(O / L);
   }
 }
 
@@ -448,60 +482,52 @@ int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int 
   return GPT2_ERR_UNSUPPORTED;
 }
 
-size_t decode_attention_scratch_floats(int B, int C, int NH, int maxT) {
-  const int hs = C / NH;
-  const int nsplit = (maxT + kDecPos * kDecWarps - 1) / (kDecPos * kDecWarps);
-  return static_cast<size_t>(B) * NH * nsplit * kDecWarps * (hs + 2);
-}
-
 template <typename E, typename OutT, int HS>
-static void decode_typed(OutT* out, const E* qkv, const E* kc, const E* vc, int B, int C, int NH, int maxT, int pos,
-                         float* scratch, cudaStream_t s) {
-  const int nsplit = (pos + 1 + kDecPos * kDecWarps - 1) / (kDecPos * kDecWarps);
-  const float scale = 1.0f / sqrtf(static_cast<float>(HS));
-  decode_attn_kernel<E, HS><<<dim3(nsplit, NH, B), 32 * kDecWarps, 0, s>>>(scratch, qkv, kc, vc, B, C, NH, maxT,
-                                                                           pos, scale);
-  decode_combine_kernel<OutT, HS><<<dim3(NH, B), 64, 0, s>>>(out, scratch, C, NH, nsplit * kDecWarps);
+static void decode_typed(OutT* out, const E* qkv, E* kc, E* vc, int B, int C, int NH, int maxT, int pos,
+                         cudaStream_t s) {
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
+  decode_attn_kernel<E, OutT, HS><<<dim3(NH, B), 32 * kDecWarps, 0, s>>>(out, qkv, kc, vc, C, NH, maxT, pos,
+                                                                         scale_log2);
 }
 
 template <typename E>
-static void decode_16(void* out, bool out16, const void* qkv, const void* kcache, const void* vcache, int B, int C,
-                      int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+static void decode_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int B, int C, int NH,
+                      int maxT, int pos, cudaStream_t s) {
   const E* q = static_cast<const E*>(qkv);
-  const E* kc = static_cast<const E*>(kcache);
-  const E* vc = static_cast<const E*>(vcache);
+  E* kc = static_cast<E*>(kcache);
+  E* vc = static_cast<E*>(vcache);
   E* o16 = static_cast<E*>(out);
   float* o32 = static_cast<float*>(out);
   switch (C / NH) {
     case 16:
-      if (out16) decode_typed<E, E, 16>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<E, float, 16>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 16>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
+      else decode_typed<E, float, 16>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
       break;
     case 32:
-      if (out16) decode_typed<E, E, 32>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<E, float, 32>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 32>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
+      else decode_typed<E, float, 32>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
       break;
     default:
-      if (out16) decode_typed<E, E, 64>(o16, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
-      else decode_typed<E, float, 64>(o32, q, kc, vc, B, C, NH, maxT, pos, scratch, s);
+      if (out16) decode_typed<E, E, 64>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
+      else decode_typed<E, float, 64>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
       break;
   }
 }
 
-void launch_decode_attention_16(void* out, bool out16, const void* qkv, const void* kcache, const void* vcache,
-                                int op, int B, int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+void launch_decode_attention_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int op, int B,
+                                int C, int NH, int maxT, int pos, cudaStream_t s) {
   if (op == kOpF16)
-    decode_16<__half>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+    decode_16<__half>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, s);
   else
-    decode_16<__nv_bfloat16>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s);
+    decode_16<__nv_bfloat16>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, s);
 }
 
-void launch_decode_attention_f32(float* out, const float* qkv, const float* kcache, const float* vcache, int B,
-                                 int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s) {
+void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, float* vcache, int B, int C, int NH,
+                                 int maxT, int pos, cudaStream_t s) {
   switch (C / NH) {
-    case 16: decode_typed<float, float, 16>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
-    case 32: decode_typed<float, float, 32>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
-    default: decode_typed<float, float, 64>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, scratch, s); break;
+    case 16: decode_typed<float, float, 16>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
+    case 32: decode_typed<float, float, 32>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
+    default: decode_typed<float, float, 64>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
   }
 }
 

@@ -588,6 +588,7 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s) {
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
+  if (M <= kSkinnyMaxRows) return launch_gemm_skinny(out, A, B, bias, M, N, K, epi, op, s);
   switch (op) {
     case kOpBF16:
       switch (epi) {

@@ -63,6 +63,14 @@ enum OperandType { kOpBF16 = 0, kOpF16 = 1, kOpTF32 = 2 };
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s);
 
+// gemm_skinny.cu: the same product for M <= 64 rows (not the LM-head
+// epilogue): weight blocks of 128 rows, K split over the CTAs of a cluster,
+// reduced through distributed shared memory.  launch_gemm_tc routes small M
+// here.
+int launch_gemm_skinny(void* out, const void* A, const void* W, const float* bias, int M, int N, int K, int epi,
+                       int op, cudaStream_t s);
+constexpr int kSkinnyMaxRows = 64;
+
 // The LM head: logits = A B^T (no bias) and row_stats[row * blocks + i] =
 // (max, sum of exp(x - max)) over the columns < V of column block i (128
 // columns), blocks = logits_stat_blocks(N) (a block past V holds (-inf, 0)).
@@ -90,11 +98,11 @@ int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B,
 // fp32 CUDA-core causal attention (head size 16, 32 or 64).
 int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s);
 // Decode attention: one query per sequence (row b of qkv [B,3C]) against the
-// cache positions [0, pos]; output [B,C].
-void launch_decode_attention_16(void* out, bool out16, const void* qkv, const void* kcache, const void* vcache,
-                                int op, int B, int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s);
-void launch_decode_attention_f32(float* out, const float* qkv, const float* kcache, const float* vcache, int B,
-                                 int C, int NH, int maxT, int pos, float* scratch, cudaStream_t s);
-size_t decode_attention_scratch_floats(int B, int C, int NH, int maxT);
+// cache positions [0, pos], the key and value of position pos taken from
+// qkv and appended to the cache; output [B,C].
+void launch_decode_attention_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int op, int B,
+                                int C, int NH, int maxT, int pos, cudaStream_t s);
+void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, float* vcache, int B, int C, int NH,
+                                 int maxT, int pos, cudaStream_t s);
 
 }  // namespace gpt2

@@ -373,8 +373,8 @@ __device__ __forceinline__ float2 block_merge_stats(float m, float s) {
 
 // Writes probs for one row given its max and 1/sum: float4 streaming.
 __device__ __forceinline__ void softmax_write_row(float4* __restrict__ prow, const float4* __restrict__ lrow, int V,
-                                                  int Vp4, float mx, float inv) {
-  for (int c4 = threadIdx.x; c4 < Vp4; c4 += blockDim.x) {
+                                                  int c4_lo, int c4_hi, float mx, float inv) {
+  for (int c4 = c4_lo + static_cast<int>(threadIdx.x); c4 < c4_hi; c4 += blockDim.x) {
     const float4 x = __ldcs(lrow + c4);
     const int c = c4 * 4;
     float4 p;
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float4* 
     }
   }
   const float2 r = block_merge_stats(m, s);
-  softmax_write_row(probs + row * Vp4, lrow, V, Vp4, r.x, 1.0f / r.y);
+  softmax_write_row(probs + row * Vp4, lrow, V, 0, Vp4, r.x, 1.0f / r.y);
 }
 
 void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s) {
@@ -434,12 +434,20 @@ __global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(float
     merge_stats(m, s, p.x, p.y);
   }
   const float2 r = block_merge_stats(m, s);
-  softmax_write_row(probs + row * Vp4, logits + row * Vp4, V, Vp4, r.x, 1.0f / r.y);
+  // blockIdx.y: this block's share of the row's columns (one share unless
+  // there are too few rows to fill the GPU)
+  const int per = (Vp4 + static_cast<int>(gridDim.y) - 1) / static_cast<int>(gridDim.y);
+  const int lo = static_cast<int>(blockIdx.y) * per;
+  softmax_write_row(probs + row * Vp4, logits + row * Vp4, V, lo, min(Vp4, lo + per), r.x, 1.0f / r.y);
 }
 
 void launch_softmax_from_stats(float* probs, const float* logits, const float2* row_stats, int tiles, int N, int V,
                                int Vp, cudaStream_t s) {
-  softmax_from_stats_kernel<<<N, kStatsThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
+  // a few rows (a decode step): split each row over blocks, about four
+  // blocks per SM in all
+  int split = N >= 4 * num_sms() ? 1 : (4 * num_sms() + N - 1) / N;
+  if (split > 64) split = 64;
+  softmax_from_stats_kernel<<<dim3(N, split), kStatsThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
                                                         reinterpret_cast<const float4*>(logits), row_stats, tiles, V,
                                                         Vp / 4);
 }

@@ -52,8 +52,8 @@ def test_tiny_decode_matches_oracle(precision):
 
 @pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_FP32])
 def test_decode_head_size_32(precision):
-    # head size 32 (C=128, 4 heads): one dimension per lane in the decode
-    # kernel's P V; positions 40..89 span several 32-position chunks
+    # head size 32 (C=128, 4 heads): in the decode kernel four (fp16) or
+    # eight (fp32) lanes per cache row; positions 40..89 cross chunk edges
     cfg = inputs.GPT2Config(max_seq_len=128, vocab_size=300, padded_vocab_size=304, num_layers=2, num_heads=4,
                             channels=128)
     params = inputs.make_params(cfg, 94, "perturbed")
@@ -70,11 +70,13 @@ def test_tiny_decode_from_position_zero():
     tok = inputs.make_tokens(93, 2, 64, cfg.vocab_size)
     m = GPT2Model(cfg, params, 2, 64, ab.GPT2_BF16)
     cache = m.new_kvcache(2)
-    full, _ = oracle.forward(cfg, params, tok, want_probs=False)
+    full, full_p = oracle.forward(cfg, params, tok)
     for pos in range(64):  # up to the last position maxT - 1
         lg, pr = m.new_outputs(2, None)
         m.decode_step(cache, dev(tok[:, pos]), pos, lg, pr)
         assert_close(host(lg), full[:, pos], atol=2e-2, what=f"pos {pos}")
+        # two rows: the softmax splits each row's columns over many blocks
+        assert_close(host(pr), full_p[:, pos], atol=1e-3, what=f"probs pos {pos}")
         np.testing.assert_allclose(host(pr).sum(-1), 1.0, atol=1e-4)
 
 

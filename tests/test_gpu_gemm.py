@@ -54,6 +54,14 @@ SHAPES = [
     (5, 64, 40),         # tiny, ragged N inside one tile
     (32, 768, 2304),     # decode-sized M
     (1, 8, 4),           # smallest legal shape
+    # M <= 64 (the small-M kernel: K split over a cluster, reduced in
+    # distributed shared memory): padded activation rows 16/32/48/64, 16-way
+    # splits at K = 3072, a ragged K (200 = 3 blocks + 8) and N tail
+    (33, 768, 2304),
+    (64, 3072, 768),
+    (17, 768, 3072),
+    (2, 3072, 768),
+    (48, 200, 200),
 ]
 
 
@@ -69,7 +77,8 @@ def test_matmul(N, C, OC, precision):
 
 @pytest.mark.parametrize("precision,grid", [(ab.GPT2_BF16, "bf16"), (ab.GPT2_FP16, "fp16"),
                                             (ab.GPT2_TF32, "tf32")])
-@pytest.mark.parametrize("N,C,OC", [(300, 768, 2304), (128 * 20, 256, 256 * 20), (64, 3072, 50304), (7, 64, 40)])
+@pytest.mark.parametrize("N,C,OC", [(300, 768, 2304), (128 * 20, 256, 256 * 20), (64, 3072, 50304), (7, 64, 40),
+                                    (32, 3072, 768), (3, 768, 2304)])
 def test_matmul_on_grid_is_exact_to_fp32_accumulation(N, C, OC, precision, grid):
     got, ref = run_matmul(N, C, OC, precision, seed=9, grid=grid)
     assert_close(got, ref, atol=1e-4, what=f"on-grid matmul {N}x{C}x{OC} {grid}")
@@ -80,6 +89,15 @@ def test_matmul_no_bias_and_persistent_tiles(precision):
     # 2 * 148 + tiles: every CTA walks several tiles through both TMEM buffers
     got, ref = run_matmul(128 * 20, 256, 256 * 20, precision, bias=False, seed=5)
     assert_close(got, ref, atol=TOL[precision], what="persistent")
+
+
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16, ab.GPT2_TF32])
+def test_small_m_split_sum_is_run_to_run_identical(precision):
+    # the K-split partials are summed in a fixed order: repeated calls agree bit for bit
+    a, ref = run_matmul(32, 3072, 768, precision, seed=11)
+    b, _ = run_matmul(32, 3072, 768, precision, seed=11)
+    np.testing.assert_array_equal(a, b)
+    assert_close(a, ref, atol=TOL[precision], what="split-K small M")
 
 
 def test_matmul_bf16_is_bf16_rounded():
