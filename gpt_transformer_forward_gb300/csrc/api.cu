@@ -39,6 +39,13 @@ namespace {
 thread_local std::string g_last_cuda_error;
 }  // namespace
 
+namespace {
+thread_local bool t_pdl = false;
+}
+bool pdl_on() { return t_pdl; }
+PdlScope::PdlScope(bool on) : prev_(t_pdl) { t_pdl = on; }
+PdlScope::~PdlScope() { t_pdl = prev_; }
+
 int note_cuda_error(cudaError_t e) {
   g_last_cuda_error = cudaGetErrorString(e);
   cudaGetLastError();
@@ -337,6 +344,7 @@ int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, voi
 int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, void* stream) {
   RETURN_IF(!next || !logits || B < 0 || V <= 0 || Vp < V, GPT2_ERR_ARG);
   if (B == 0) return GPT2_OK;
+  PdlScope pdl(true);  // the argmax kernel waits for its predecessor itself
   launch_argmax(next, logits, B, V, Vp, as_stream(stream));
   return check_launch();
 }
@@ -576,6 +584,7 @@ int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* pac
                 (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
             GPT2_ERR_ALIGN);
+  PdlScope pdl(is16(precision));  // every kernel of the 16-bit step waits for its predecessor itself
   return run_forward(cfg, params, packed, tok, B, 1, pos, logits, probs, kvcache, workspace, ws_bytes, precision,
                      as_stream(stream));
 }

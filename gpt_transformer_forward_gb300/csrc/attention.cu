@@ -336,6 +336,19 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane / kLPR;   // row of an instruction this lane reads
   const int dg = lane % kLPR;  // its dimensions dg * kPer .. dg * kPer + kPer - 1
+  const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
+  // The cache rows before pos were written by earlier steps: this warp's
+  // first chunk of them is fetched into L2 while the QKV projection before
+  // this kernel finishes (a prefetch has no other effect).
+  for (int i = 0; i < kIt; ++i) {
+    const int j = warp * kChunk + i * kRPI + g;
+    if (j < pos && dg == 0) {
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(kcache + (head + j) * HS));
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(vcache + (head + j) * HS));
+    }
+  }
+  pdl_wait();  // q and this token's key and value come from the QKV projection
+  pdl_trigger();
   // the query's dimensions of this lane, scaled by log2(e) / sqrt(hs)
   float q[kPer];
   {
@@ -344,7 +357,6 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) q[k] = to_f32(e[k]) * scale_log2;
   }
-  const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
   const uint4* kb = reinterpret_cast<const uint4*>(kcache + head * HS) + dg;
   const uint4* vb = reinterpret_cast<const uint4*>(vcache + head * HS) + dg;
   // this token's key and value: used for position pos, and appended
@@ -486,8 +498,8 @@ template <typename E, typename OutT, int HS>
 static void decode_typed(OutT* out, const E* qkv, E* kc, E* vc, int B, int C, int NH, int maxT, int pos,
                          cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
-  decode_attn_kernel<E, OutT, HS><<<dim3(NH, B), 32 * kDecWarps, 0, s>>>(out, qkv, kc, vc, C, NH, maxT, pos,
-                                                                         scale_log2);
+  launch_pdl(decode_attn_kernel<E, OutT, HS>, dim3(NH, B), dim3(32 * kDecWarps), 0, s, out, qkv, kc, vc, C, NH, maxT,
+             pos, scale_log2);
 }
 
 template <typename E>

@@ -23,6 +23,9 @@
 // result does not depend on timing), adds the bias, applies the epilogue and
 // stores with plain vector stores; a second cluster barrier keeps every
 // CTA's shared memory alive until its peers have read it.
+// Launched as a programmatic dependent launch (in a decode step), a CTA
+// sets up and requests its first weight tiles before it waits for the
+// kernel ahead of it.
 // Every mbarrier wait is bounded; on a timeout the CTA records
 // GPT2_DEVERR_TIMEOUT and still reaches both cluster barriers.
 #include "kernels.cuh"
@@ -96,19 +99,33 @@ __global__ void __launch_bounds__(kSkThreads)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The weights are never written by the kernel before this one, so the
+  // first stages' weight tiles are requested before waiting for it; the
+  // activations (its output) after.
+  const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
+  const int early = count < kSkStages ? count : kSkStages;
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < early; ++i) {
+      mbar_arrive_expect_tx(&full[i], kSkWStage + x_bytes);
+      tma_load_2d_hint(smem + i * kSkWStage, &tmap_w, &full[i], (kb0 + i) * kBK, n_blk * kSkRowsW, pol_w);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_w = policy_evict_first();  // each weight byte is read once
       int issued = 0;
       for (int i = 0; i < count; ++i) {
         const int stage = i % kSkStages;
         const uint32_t phase = static_cast<uint32_t>(i / kSkStages) & 1u;
-        if (!mbar_wait(&empty[stage], phase ^ 1u)) break;
-        mbar_arrive_expect_tx(&full[stage], kSkWStage + x_bytes);
         const int kx = (kb0 + i) * kBK;
-        tma_load_2d_hint(smem + stage * kSkWStage, &tmap_w, &full[stage], kx, n_blk * kSkRowsW, pol_w);
+        if (i >= early) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u)) break;
+          mbar_arrive_expect_tx(&full[stage], kSkWStage + x_bytes);
+          tma_load_2d_hint(smem + stage * kSkWStage, &tmap_w, &full[stage], kx, n_blk * kSkRowsW, pol_w);
+        }
         tma_load_2d(smem + kSkXOff + stage * kSkXStage, &tmap_x, &full[stage], kx, 0);
         ++issued;
       }
@@ -251,10 +268,12 @@ int launch_skinny_impl(void* out, const void* A, const void* W, const float* bia
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits for its predecessor itself
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kSkThreads);
   cfg.dynamicSmemBytes = kSkAlloc;
   cfg.stream = s;
@@ -281,6 +300,7 @@ int launch_skinny_impl(void* out, const void* A, const void* W, const float* bia
   while (splits * 2 <= max_splits[dev] && splits * 2 <= num_kb && n_blocks * splits < num_sms()) splits *= 2;
   attr[0].val.clusterDim.x = splits;
   cfg.gridDim = dim3(n_blocks * splits);
+  cfg.numAttrs = pdl_on() ? 2 : 1;
   const uint32_t idesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kSkRowsW, n_mma);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, tx, out, bias, M, N, K, n_mma, idesc);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);

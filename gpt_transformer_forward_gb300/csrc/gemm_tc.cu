@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // a programmatic dependent launch: the kernel ahead has finished
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -544,11 +546,13 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::alloc;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kPair ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits for its predecessor itself
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // per template instance and device: the shared-memory attribute and how
@@ -571,6 +575,7 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   }
   const int units = num_tiles < resident[dev] ? num_tiles : resident[dev];
   cfg.gridDim = dim3(kPair ? 2 * units : units);
+  cfg.numAttrs = pdl_on() ? 2 : 1;
   const cudaError_t e =
       cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, n_fast, row_stats, V);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);

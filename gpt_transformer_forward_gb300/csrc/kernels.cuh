@@ -11,6 +11,40 @@ int num_sms();  // SM count of the current device (cached)
 // runtime, and returns GPT2_ERR_CUDA.
 int note_cuda_error(cudaError_t e);
 
+// Programmatic dependent launch.  Inside a PdlScope(true) on the calling
+// thread (a 16-bit decode step, greedy argmax) the kernels below that call
+// pdl_wait() before touching dependent memory are launched with the
+// programmatic-stream-serialization attribute, so that each one's launch and
+// prologue overlap the tail of the kernel before it.
+bool pdl_on();
+class PdlScope {
+ public:
+  explicit PdlScope(bool on);
+  ~PdlScope();
+  PdlScope(const PdlScope&) = delete;
+  PdlScope& operator=(const PdlScope&) = delete;
+
+ private:
+  bool prev_;
+};
+
+// Launches a kernel whose body begins with pdl_wait() (or waits before its
+// first dependent access), with the attribute when pdl_on().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_on() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // rowwise.cu
 void launch_encoder(float* out, const int* tok, const float* wte, const float* wpe, int N, int T, int C, int V,
                     cudaStream_t s);

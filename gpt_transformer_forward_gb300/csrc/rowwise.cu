@@ -36,6 +36,8 @@ __global__ void encoder_kernel(float4* __restrict__ out, const int* __restrict__
 __global__ void encoder_pos_kernel(float4* __restrict__ out, const int* __restrict__ tok,
                                    const float4* __restrict__ wte, const float4* __restrict__ wpe, int B, int pos,
                                    int C4, int V) {
+  pdl_wait();  // tok comes from the argmax before it
+  pdl_trigger();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= B * C4) return;
   const int b = idx / C4, c = idx % C4;
@@ -64,9 +66,9 @@ void launch_encoder_pos(float* out, const int* tok, const float* wte, const floa
                         cudaStream_t s) {
   const int C4 = C / 4;
   const int threads = 256;
-  encoder_pos_kernel<<<(B * C4 + threads - 1) / threads, threads, 0, s>>>(
-      reinterpret_cast<float4*>(out), tok, reinterpret_cast<const float4*>(wte),
-      reinterpret_cast<const float4*>(wpe), B, pos, C4, V);
+  launch_pdl(encoder_pos_kernel, dim3((B * C4 + threads - 1) / threads), dim3(threads), 0, s,
+             reinterpret_cast<float4*>(out), tok, reinterpret_cast<const float4*>(wte),
+             reinterpret_cast<const float4*>(wpe), B, pos, C4, V);
 }
 
 // -------------------------------------------------------------- LayerNorm
@@ -79,6 +81,8 @@ __global__ void __launch_bounds__(256) layernorm_warp_kernel(OutT* __restrict__ 
                                                              const float* __restrict__ inp,
                                                              const float* __restrict__ w,
                                                              const float* __restrict__ b, int N) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int C = 128 * kVec;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -169,12 +173,12 @@ static void layernorm_dispatch(OutT* out, float* mean, float* rstd, const float*
   const int rows_per_block = 8;
   const unsigned grid = static_cast<unsigned>((N + rows_per_block - 1) / rows_per_block);
   switch (C) {
-    case 256: layernorm_warp_kernel<2, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
-    case 512: layernorm_warp_kernel<4, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
-    case 768: layernorm_warp_kernel<6, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
-    case 1024: layernorm_warp_kernel<8, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
-    case 1280: layernorm_warp_kernel<10, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
-    case 1536: layernorm_warp_kernel<12, OutT><<<grid, 256, 0, s>>>(out, mean, rstd, inp, w, b, N); return;
+    case 256: launch_pdl(layernorm_warp_kernel<2, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
+    case 512: launch_pdl(layernorm_warp_kernel<4, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
+    case 768: launch_pdl(layernorm_warp_kernel<6, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
+    case 1024: launch_pdl(layernorm_warp_kernel<8, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
+    case 1280: launch_pdl(layernorm_warp_kernel<10, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
+    case 1536: launch_pdl(layernorm_warp_kernel<12, OutT>, dim3(grid), dim3(256), 0, s, out, mean, rstd, inp, w, b, N); return;
     default: layernorm_block_kernel<OutT><<<N, 256, 0, s>>>(out, mean, rstd, inp, w, b, C); return;
   }
 }
@@ -210,6 +214,8 @@ template <int kVec, typename T16>
 __global__ void __launch_bounds__(256) residual_layernorm_kernel(float* __restrict__ x, const T16* __restrict__ y,
                                                                  T16* __restrict__ out, const float* __restrict__ w,
                                                                  const float* __restrict__ b, int N, int write_x) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int C = 128 * kVec;
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -271,12 +277,12 @@ void launch_residual_layernorm_16(float* x, const T16* y, T16* out, const float*
   const unsigned grid = static_cast<unsigned>((N + rows_per_block - 1) / rows_per_block);
   const int wx = write_x ? 1 : 0;
   switch (C) {
-    case 256: residual_layernorm_kernel<2, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
-    case 512: residual_layernorm_kernel<4, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
-    case 768: residual_layernorm_kernel<6, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
-    case 1024: residual_layernorm_kernel<8, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
-    case 1280: residual_layernorm_kernel<10, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
-    case 1536: residual_layernorm_kernel<12, T16><<<grid, 256, 0, s>>>(x, y, out, w, b, N, wx); return;
+    case 256: launch_pdl(residual_layernorm_kernel<2, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
+    case 512: launch_pdl(residual_layernorm_kernel<4, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
+    case 768: launch_pdl(residual_layernorm_kernel<6, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
+    case 1024: launch_pdl(residual_layernorm_kernel<8, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
+    case 1280: launch_pdl(residual_layernorm_kernel<10, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
+    case 1536: launch_pdl(residual_layernorm_kernel<12, T16>, dim3(grid), dim3(256), 0, s, x, y, out, w, b, N, wx); return;
     default: {
       const long long n = static_cast<long long>(N) * C;
       add16_kernel<T16><<<stream_grid(n, 256), 256, 0, s>>>(x, y, n);
@@ -427,6 +433,8 @@ __global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(float
                                                                            const float4* __restrict__ logits,
                                                                            const float2* __restrict__ stats,
                                                                            int tiles, int V, int Vp4) {
+  pdl_wait();
+  pdl_trigger();
   const size_t row = blockIdx.x;
   float m = -INFINITY, s = 0.f;
   for (int i = threadIdx.x; i < tiles; i += blockDim.x) {
@@ -447,15 +455,16 @@ void launch_softmax_from_stats(float* probs, const float* logits, const float2* 
   // blocks per SM in all
   int split = N >= 4 * num_sms() ? 1 : (4 * num_sms() + N - 1) / N;
   if (split > 64) split = 64;
-  softmax_from_stats_kernel<<<dim3(N, split), kStatsThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
-                                                        reinterpret_cast<const float4*>(logits), row_stats, tiles, V,
-                                                        Vp / 4);
+  launch_pdl(softmax_from_stats_kernel, dim3(N, split), dim3(kStatsThreads), 0, s, reinterpret_cast<float4*>(probs),
+             reinterpret_cast<const float4*>(logits), row_stats, tiles, V, Vp / 4);
 }
 
 // ----------------------------------------------------------------- argmax
 // One block per row; ties go to the smallest index.
 __global__ void __launch_bounds__(512) argmax_kernel(int* __restrict__ next, const float* __restrict__ logits, int V,
                                                      int Vp) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sv[32];
   __shared__ int si[32];
   const float* row = logits + static_cast<size_t>(blockIdx.x) * Vp;
@@ -524,7 +533,7 @@ __global__ void __launch_bounds__(512) argmax_kernel(int* __restrict__ next, con
 }
 
 void launch_argmax(int* next, const float* logits, int B, int V, int Vp, cudaStream_t s) {
-  argmax_kernel<<<B, 512, 0, s>>>(next, logits, V, Vp);
+  launch_pdl(argmax_kernel, dim3(B), dim3(512), 0, s, next, logits, V, Vp);
 }
 
 // ------------------------------------------------------------ conversions
