@@ -234,7 +234,12 @@ GPT2_API int gpt2_forward(const GPT2Config* cfg, const float* params, const void
  * tok[b] at position pos.  Writes this position's keys and values into the
  * cache and computes logits [B,Vp] (and probs [B,Vp] when non-null) exactly
  * as row `pos` of gpt2_forward over the whole sequence would.  Requires
- * 0 <= pos < maxT; workspace of gpt2_workspace_size(cfg, B, 1, precision). */
+ * 0 <= pos < maxT; workspace of gpt2_workspace_size(cfg, B, 1, precision).
+ * The new keys and values are appended by the attention kernel.  In the
+ * 16-bit modes the step's kernels are programmatic dependent launches: each
+ * may begin (set up, request weights) while the kernel ahead of it on the
+ * stream runs, and waits for it before touching what it writes, so stream
+ * order holds for the caller's own work before and after the call. */
 GPT2_API int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* packed, void* kvcache, const int* tok,
                      int B, int pos, float* logits, float* probs, void* workspace, size_t ws_bytes, int precision,
                      void* stream);
@@ -248,7 +253,7 @@ enum {
                                16-bit modes LN1 of layers 1.. and LN2 and
                                LN_f also add the preceding projection's
                                output into the residual stream */
-  GPT2_STAGE_QKV = 2,       /* QKV GEMM (+ cache store when caching) */
+  GPT2_STAGE_QKV = 2,       /* QKV GEMM (+ cache store when a prefill fills a cache) */
   GPT2_STAGE_ATTENTION = 3,
   GPT2_STAGE_ATTPROJ = 4,   /* attention projection GEMM (+ residual in the fp32 and tf32 modes) */
   GPT2_STAGE_LN2 = 5,
