@@ -81,6 +81,23 @@ def stage_costs(cfg, B, T, act_bytes=2):
     }
 
 
+def decode_step_bytes(cfg, B, pos, act_bytes=2):
+    """Algorithmic HBM bytes of one KV-cached decode step at position pos:
+    the weights of the blocks and of the tied LM head (16-bit, or fp32 when
+    act_bytes is 4), the fp32 biases and LayerNorm parameters, the cache
+    read of positions 0..pos-1 and the append at pos (keys and values,
+    act_bytes each), the token ids, embedding rows, and the B rows of
+    logits (written, then read by the softmax) and probabilities, as the
+    forward pass's stage sum counts them.  The activations passed between
+    kernels (a few B x C rows, under 0.1 % here) are left out."""
+    C, L, Vp = cfg.channels, cfg.num_layers, cfg.padded_vocab_size
+    weights = (L * 12 * C * C + Vp * C) * act_bytes
+    small = (L * 13 * C + 2 * C) * 4  # per layer 9C of biases and 4C of LayerNorm; LN_f
+    kv = 2 * L * B * C * act_bytes * (pos + 1)  # pos rows read, one row written
+    rows = B * 4 + (B + 1) * C * 4 + 3 * B * Vp * 4
+    return weights + small + kv + rows
+
+
 def measured_traffic(stage):
     """DRAM bytes per launch of a stage's kernel from the committed ncu
     record, or None when absent or taken on a different kernel source."""
@@ -334,14 +351,23 @@ def run_decode(args, w, precision):
     err = ab.gpt2_get_error()
     decode_ms = max_over_ranks(decode_ms, pg, "cuda")
     tokens = B * n * args.steps
+    # HBM floor of the timed steps (positions T .. T + n - 1) at the measured
+    # copy bandwidth
+    peaks, peak_src = load_peaks()
+    act = 2 if precision in (ab.GPT2_BF16, ab.GPT2_FP16) else 4
+    step_bytes = sum(decode_step_bytes(cfg, B, T + i, act) for i in range(n)) / n
+    ms_step = decode_ms / (args.steps * n)
+    floor_ms = step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
     line = {
         "metric": DECODE_METRIC, "value": job_tokens_per_s(world, tokens, decode_ms), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": decode_ms / (args.steps * n),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.precision,
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "prompt": T, "decode_steps": n, "layers": cfg.num_layers,
                    "outputs": "logits+probs per step, greedy argmax", "parallelism": f"replicas{world}"},
         "prefill_ms": prefill_ms / args.steps,
+        "step_roofline": {"bound": "hbm", "bytes_per_step": step_bytes, "floor_ms": floor_ms, "measured_ms": ms_step,
+                          "frac": floor_ms / ms_step, "peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src},
         # per step: argmax, encoder, 7 per layer (LN, QKV, attention with the
         # cache append, projection, LN, FC, FC-proj), LN_f, LM head, softmax
         "gpu_launches": (7 * cfg.num_layers + 5) * n * args.steps,
