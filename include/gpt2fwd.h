@@ -122,7 +122,11 @@ GPT2_API size_t matmul_workspace_size(int N, int C, int OC, int precision);
  * out [N,OC], inp [N,C], W [OC,C] (PyTorch Linear layout), bias [OC].
  * Tensor-core modes need C % 8 == 0 and OC % 4 == 0.  `workspace` of
  * matmul_workspace_size() bytes is caller-owned scratch (may be NULL when
- * that size is 0).  out must not alias inp or W. */
+ * that size is 0).  out must not alias inp or W.  In the tensor-core modes
+ * N <= 64 rows (a decode step's shape) run on a kernel that splits C over
+ * the CTAs of a cluster and adds the parts in a fixed order: repeated calls
+ * give identical results, which may differ in the last bits from the same
+ * rows computed inside a larger N. */
 GPT2_API int matmul_forward(float* out, const float* inp, const float* W, const float* bias, int N, int C, int OC,
                    int precision, void* workspace, size_t ws_bytes, void* stream);
 
