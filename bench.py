@@ -42,6 +42,17 @@ sys.path.insert(0, ROOT)
 from gpt_transformer_forward_gb300 import inputs  # noqa: E402
 
 METRIC = "GPT-2 124M forward tokens/s (B=16,T=1024) on 1 GB300; % of roofline"
+
+
+def metric_name(w):
+    """The metric string of a forward workload: the headline string for the
+    124M B=16 T=1024 pass, the same wording with its own model and shape for
+    every other one."""
+    if w.name == "gpt2-124m-b16":
+        return METRIC
+    model = {12: "124M", 24: "medium"}.get(w.cfg.num_layers, f"L{w.cfg.num_layers}")
+    return f"GPT-2 {model} forward tokens/s (B={w.B},T={w.T}) on 1 GB300; % of roofline"
+
 UNIT = "tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -291,7 +302,7 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = args.steps * T_s / dt
     sample = f"per step: 1 sequence x {T_s} tokens of {w.name} (double precision, logits and probs)"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_name(w), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T},
@@ -499,7 +510,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, params, tok)
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_name(w), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.precision, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "layers": w.cfg.num_layers,

@@ -75,6 +75,7 @@ _SIGNATURES = {
     "gpt2_get_error": (_I, [_P]),
     "gpt2_strerror": (ctypes.c_char_p, [_I]),
     "gpt2_last_cuda_error": (ctypes.c_char_p, []),
+    "gpt2_diag_wait_timeout": (_I, [ctypes.c_longlong, _P, _P]),
 }
 
 _handle = None
@@ -255,3 +256,9 @@ def gpt2_strerror(code) -> str:
 
 def gpt2_last_cuda_error() -> str:
     return _lib().gpt2_last_cuda_error().decode()
+
+
+def gpt2_diag_wait_timeout(limit_ns, gave_up, stream=None):
+    """Runs the bounded-wait path once (see the header); gave_up: a device
+    int32 tensor of one element."""
+    _check("gpt2_diag_wait_timeout", _lib().gpt2_diag_wait_timeout(int(limit_ns), _ptr(gave_up), _stream(stream)))

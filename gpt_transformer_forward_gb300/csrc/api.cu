@@ -545,6 +545,7 @@ int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed,
                 (kvcache && !aligned16(kvcache)) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
             GPT2_ERR_ALIGN);
+  PdlScope pdl(is16(precision));  // every kernel of the 16-bit pass waits for its predecessor itself
   return run_forward(cfg, params, packed, tok, B, T, -1, logits, probs, kvcache, workspace, ws_bytes, precision,
                      as_stream(stream));
 }
@@ -562,6 +563,7 @@ int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void*
                 (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
             GPT2_ERR_ALIGN);
+  PdlScope pdl(is16(precision));  // the kernels gpt2_forward launches, launched the same way
   StageProfiler prof{as_stream(stream), {}, {}};
   int rc = prof.begin();
   if (rc == GPT2_OK)

@@ -112,7 +112,7 @@ struct Schedule {
 // therefore read their S row in halves instead of holding all of it.
 template <typename T16, typename OutT, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, OutT* __restrict__ out, int T, int C,
                    float scale_log2) {
   using L = Smem<kPair>;
@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // a programmatic dependent launch: the QKV projection has finished
+  pdl_trigger();
 
   if (warp == 0) {
     // ------------------------------------------------------------ loads
@@ -560,7 +562,7 @@ int launch_typed(void* out, const CUtensorMap* maps, int B, int T, int C, int NH
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
   if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<T16, OutT, kPair>,
+    const cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<T16, OutT, kPair>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kPair>::alloc);
     if (e != cudaSuccess) return note_cuda_error(e);
     attr_set[dev] = true;
@@ -573,18 +575,28 @@ int launch_typed(void* out, const CUtensorMap* maps, int B, int T, int C, int NH
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Smem<kPair>::alloc;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n_attr = 0;
+  if (kPair) {
+    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+    attr[n_attr].val.clusterDim.x = 2;
+    attr[n_attr].val.clusterDim.y = 1;
+    attr[n_attr].val.clusterDim.z = 1;
+    ++n_attr;
+  }
+  if (pdl_on()) {  // the kernel waits for its predecessor itself
+    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = kPair ? 1 : 0;
+  cfg.numAttrs = n_attr;
   // the one-CTA form loads whole K and V tiles: 64 dims x 128 rows, as Q
   const CUtensorMap& mk = kPair ? maps[1] : maps[0];
   const CUtensorMap& mv = kPair ? maps[2] : maps[0];
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<T16, OutT, kPair>, maps[0], mk, mv,
-                                           static_cast<OutT*>(out), T, C, scale_log2);
+  auto kern = attn_tc05_kernel<T16, OutT, kPair>;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, kern, maps[0], mk, mv, static_cast<OutT*>(out), T, C, scale_log2);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 

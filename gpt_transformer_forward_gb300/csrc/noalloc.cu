@@ -32,10 +32,9 @@ int scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(mu);
   if (addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_matmul_scratch) != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return GPT2_ERR_CUDA;
-    }
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_matmul_scratch);
+    if (e != cudaSuccess) return note_cuda_error(e);  // keeps the error text for gpt2_last_cuda_error()
+    if (p == nullptr) return GPT2_ERR_CUDA;
     addr[dev] = p;
   }
   *out = addr[dev];

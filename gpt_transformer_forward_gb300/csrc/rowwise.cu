@@ -17,6 +17,8 @@ __device__ unsigned int g_error_word = 0;
 __global__ void encoder_kernel(float4* __restrict__ out, const int* __restrict__ tok,
                                const float4* __restrict__ wte, const float4* __restrict__ wpe, int N, int T,
                                int C4, int V) {
+  pdl_wait();  // x may still be read by the kernel ahead (the previous pass)
+  pdl_trigger();
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<long long>(N) * C4) return;
   const int n = static_cast<int>(idx / C4);
@@ -57,9 +59,8 @@ void launch_encoder(float* out, const int* tok, const float* wte, const float* w
   const long long total = static_cast<long long>(N) * C4;
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
-  encoder_kernel<<<blocks, threads, 0, s>>>(reinterpret_cast<float4*>(out), tok,
-                                            reinterpret_cast<const float4*>(wte),
-                                            reinterpret_cast<const float4*>(wpe), N, T, C4, V);
+  launch_pdl(encoder_kernel, dim3(blocks), dim3(threads), 0, s, reinterpret_cast<float4*>(out), tok,
+             reinterpret_cast<const float4*>(wte), reinterpret_cast<const float4*>(wpe), N, T, C4, V);
 }
 
 void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos, int C, int V,
@@ -567,6 +568,8 @@ template void launch_f32_to_16<__half>(__half*, const float*, long long, cudaStr
 template <typename E>
 __global__ void kv_store_kernel(E* __restrict__ cache, const E* __restrict__ qkv, int B, int T, int C, int NH,
                                 int maxT, int pos0) {
+  pdl_wait();  // the QKV projection ahead has finished
+  pdl_trigger();
   constexpr int kPer = 16 / sizeof(E);
   const int hs = C / NH;
   const int chunks = hs / kPer;
@@ -588,13 +591,15 @@ __global__ void kv_store_kernel(E* __restrict__ cache, const E* __restrict__ qkv
 void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, int NH, int maxT, int pos0,
                          cudaStream_t s) {
   const long long total = 2LL * B * T * C / 4;
-  kv_store_kernel<float><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
+  launch_pdl(kv_store_kernel<float>, dim3(stream_grid(total, 256)), dim3(256), 0, s, cache, qkv, B, T, C, NH, maxT,
+             pos0);
 }
 
 void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
                         cudaStream_t s) {
   const long long total = 2LL * B * T * C / 8;
-  kv_store_kernel<uint16_t><<<stream_grid(total, 256), 256, 0, s>>>(cache, qkv, B, T, C, NH, maxT, pos0);
+  launch_pdl(kv_store_kernel<uint16_t>, dim3(stream_grid(total, 256)), dim3(256), 0, s, cache, qkv, B, T, C, NH,
+             maxT, pos0);
 }
 
 }  // namespace gpt2

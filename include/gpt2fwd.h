@@ -228,7 +228,11 @@ GPT2_API size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision);
  * kvcache: NULL, or a cache of gpt2_kvcache_size(cfg, B, precision) bytes
  * whose positions [0, T) are written (the prefill of decoding);
  * workspace of gpt2_workspace_size(cfg, B, T, precision) bytes.
- * Requires 1 <= T <= maxT and C % NH == 0. */
+ * Requires 1 <= T <= maxT and C % NH == 0.  In the 16-bit modes the pass's
+ * kernels are programmatic dependent launches: each may begin its set-up
+ * while the kernel ahead of it on the stream runs and waits for that kernel
+ * before touching what it writes, so stream order holds for the caller's
+ * own work before and after the call. */
 GPT2_API int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
                  float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
                  void* stream);
@@ -288,6 +292,18 @@ GPT2_API const char* gpt2_strerror(int code);
 
 /* Text of the last CUDA error seen by the library on this host thread. */
 GPT2_API const char* gpt2_last_cuda_error(void);
+
+/* Runs the kernels' bounded-wait path once, on purpose, so that it can be
+ * tested: one CTA waits on an mbarrier that nothing ever completes, with
+ * the same wait routine the pipelines use but a limit of limit_ns
+ * nanoseconds (1e3 .. 1e9) instead of ~1 s.  The wait gives up, sets
+ * GPT2_DEVERR_TIMEOUT_BIT in the device error word (read it with
+ * gpt2_get_error) and the kernel returns; *gave_up (a DEVICE int) is set
+ * to 1 when the wait gave up, 0 if it had completed.  Nothing traps: the
+ * device stays usable for the next call.  The pages have no counterpart of
+ * this call: it checks the library's own error path.  GPT2_ERR_ARG for a
+ * null gave_up or a limit outside the range. */
+GPT2_API int gpt2_diag_wait_timeout(long long limit_ns, int* gave_up, void* stream);
 
 #ifdef __cplusplus
 }

@@ -17,7 +17,7 @@ def lib():
 
 def test_every_declared_function_is_exported(lib):
     names = ab.header_functions()
-    assert len(names) == 22
+    assert len(names) == 23
     for n in names:
         assert hasattr(lib, n), n
         assert n in ab._SIGNATURES, n
@@ -75,3 +75,12 @@ def test_argument_errors_before_any_launch(lib):
     assert lib.gpt2_decode_step(ctypes.byref(cfg), 256, 256, 256, 256, 1, 64, 256, None, 256, 1 << 30, 2,
                                 None) == -2
     assert ab.gpt2_strerror(-4).startswith("workspace")
+
+
+def test_wait_timeout_diagnostic_checks_its_arguments_on_the_host(lib):
+    # rejected before anything is launched, so no GPU is needed
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_diag_wait_timeout(10, None, stream=0)
+    assert e.value.code == -1
+    assert lib.gpt2_diag_wait_timeout(999, None, None) == -1
+    assert lib.gpt2_diag_wait_timeout(2_000_000_000, None, None) == -1

@@ -9,11 +9,17 @@ rows of the full-size run.  Properties that hold at any size (row sums,
 padding, causality, batch permutation) are checked on every row.
 
 Tolerances: logits 2e-2 absolute and probabilities 1e-3 absolute with
-tensor-core operands (fp16, bf16, tf32); 1e-4 / 1e-6 in fp32 mode.  One
-derived exception: at 124M depth and beyond, bf16 operands (unit roundoff
-2^-8) put the largest logit error at about 2.1e-2, just over that bar, so
-bf16 is held to 3e-2 there; fp16 operands (2^-11) stay near 2.5e-3 and are
-held to the 2e-2 bar at every size."""
+tensor-core operands (fp16, bf16, tf32); 1e-4 / 1e-6 in fp32 mode.
+
+bf16 operands meet the 2e-2 logit bar up to 6 layers of 124M width (the
+tests below), not at 12 (124M) or 24 (medium) layers: there the largest
+logit error is 2.1e-2 (124M) and 2.7e-2 (medium) over tens of millions of
+compared logits, from bf16's 8-bit rounding of every operand, and keeping
+the projections' outputs in fp32 did not change that (measured).  So bf16
+at full depth is checked for the properties that hold at any precision,
+and the full-depth parity claims are fp16's and tf32's."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -27,7 +33,6 @@ from gpu_helpers import assert_close, dev, host, need_gpu, no_device_error
 
 pytestmark = pytest.mark.gpu
 LOGIT_TOL = {ab.GPT2_BF16: 2e-2, ab.GPT2_FP16: 2e-2, ab.GPT2_TF32: 2e-2, ab.GPT2_FP32: 1e-4}
-DEEP_BF16_LOGIT_TOL = 3e-2
 PROB_TOL = {ab.GPT2_BF16: 1e-3, ab.GPT2_FP16: 1e-3, ab.GPT2_TF32: 1e-3, ab.GPT2_FP32: 1e-6}
 
 
@@ -80,20 +85,23 @@ def test_forward_causal_and_batch_permutation_bitwise():
     np.testing.assert_array_equal(outs[2], outs[0][[3, 1, 0, 2]])
 
 
-def check_sampled(w, precision, logits, probs, params, tok, prefix_rows, full_seq, full_rows):
-    """Oracle rows: sequence 0's first prefix_rows positions (every column),
-    and rows full_rows of sequence full_seq (needs that whole sequence)."""
+def check_sampled(w, precision, logits, probs, params, tok, prefix_rows, full_seq):
+    """Oracle rows: sequence 0's first prefix_rows positions, and every row
+    of sequence full_seq (a whole-sequence oracle pass), each on every
+    column."""
     cfg = w.cfg
-    ltol = DEEP_BF16_LOGIT_TOL if precision == ab.GPT2_BF16 else LOGIT_TOL[precision]
+    ltol = LOGIT_TOL[precision]
     rl, rp = oracle.forward(cfg, params, tok[:1, :prefix_rows])
     assert_close(host(logits[:1, :prefix_rows]), rl, atol=ltol, what="prefix logits")
     assert_close(host(probs[:1, :prefix_rows]), rp, atol=PROB_TOL[precision], what="prefix probs")
     h = oracle.hidden(cfg, params, tok[full_seq:full_seq + 1])
-    rows = np.array(full_rows)
-    rl = oracle.lm_head(cfg, params, h[0, rows])
-    rp = oracle.softmax(rl, cfg.vocab_size)
-    assert_close(host(logits[full_seq, rows]), rl, atol=ltol, what="late-row logits")
-    assert_close(host(probs[full_seq, rows]), rp, atol=PROB_TOL[precision], what="late-row probs")
+    for r0 in range(0, w.T, 256):  # 256 rows of logits at a time bound the oracle's memory
+        rows = np.arange(r0, min(w.T, r0 + 256))
+        rl = oracle.lm_head(cfg, params, h[0, rows])
+        rp = oracle.softmax(rl, cfg.vocab_size)
+        assert_close(host(logits[full_seq, rows]), rl, atol=ltol, what=f"sequence {full_seq} logits rows {r0}..")
+        assert_close(host(probs[full_seq, rows]), rp, atol=PROB_TOL[precision],
+                     what=f"sequence {full_seq} probs rows {r0}..")
 
 
 def check_properties(cfg, logits, probs):
@@ -105,29 +113,53 @@ def check_properties(cfg, logits, probs):
     assert bool(torch.isfinite(logits).all())
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_BF16])
 @pytest.mark.parametrize("name", ["gpt2-124m-b4", "gpt2-124m-b16"])
-def test_gpt2_124m_sampled(name, precision):
+def test_gpt2_124m_sampled(name):
     w = inputs.WORKLOADS[name]
     params, tok = inputs.workload_inputs(w)
-    m = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_FP16)
     logits, probs = m.new_outputs(w.B, w.T)
     m.forward(dev(tok), logits, probs)
     no_device_error()
     check_properties(w.cfg, logits, probs)
-    check_sampled(w, precision, logits, probs, params, tok, 64, w.B - 1, [0, 511, 777, 1023])
+    check_sampled(w, ab.GPT2_FP16, logits, probs, params, tok, 64, w.B - 1)
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_BF16])
-def test_gpt2_medium_sampled(precision):
+def test_gpt2_medium_sampled():
     w = inputs.WORKLOADS["gpt2-medium-b8"]
     params, tok = inputs.workload_inputs(w)
-    m = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_FP16)
     logits, probs = m.new_outputs(w.B, w.T)
     m.forward(dev(tok), logits, probs)
     no_device_error()
     check_properties(w.cfg, logits, probs)
-    check_sampled(w, precision, logits, probs, params, tok, 32, w.B - 1, [1023])
+    check_sampled(w, ab.GPT2_FP16, logits, probs, params, tok, 32, w.B - 1)
+
+
+def test_bf16_at_124m_width_six_layers():
+    # the bf16 parity case: 124M width and vocabulary, half its depth
+    cfg = dataclasses.replace(inputs.GPT2_124M, num_layers=6)
+    w = inputs.Workload("gpt2-124m-width-L6-b2", cfg, B=2, T=1024, index=5)
+    params, tok = inputs.workload_inputs(w)
+    m = GPT2Model(cfg, params, w.B, w.T, ab.GPT2_BF16)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(cfg, logits, probs)
+    check_sampled(w, ab.GPT2_BF16, logits, probs, params, tok, 64, w.B - 1)
+
+
+@pytest.mark.parametrize("name", ["gpt2-124m-b16", "gpt2-medium-b8"])
+def test_bf16_full_depth_properties(name):
+    # full depth in bf16: the properties that hold at any precision (rows
+    # sum to 1, padding exactly 0, non-negative, finite)
+    w = inputs.WORKLOADS[name]
+    params, tok = inputs.workload_inputs(w)
+    m = GPT2Model(w.cfg, params, w.B, w.T, ab.GPT2_BF16)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(w.cfg, logits, probs)
 
 
 def test_gpt2_124m_tf32_sampled():
@@ -138,4 +170,4 @@ def test_gpt2_124m_tf32_sampled():
     m.forward(dev(tok), logits, probs)
     no_device_error()
     check_properties(w.cfg, logits, probs)
-    check_sampled(w, ab.GPT2_TF32, logits, probs, params, tok, 32, 0, [1023])
+    check_sampled(w, ab.GPT2_TF32, logits, probs, params, tok, 32, 0)
