@@ -21,7 +21,7 @@ PRECISIONS = {"fp32": GPT2_FP32, "tf32": GPT2_TF32, "bf16": GPT2_BF16, "fp16": G
 GPT2_OK = 0
 ERRORS = {-1: "GPT2_ERR_ARG", -2: "GPT2_ERR_SHAPE", -3: "GPT2_ERR_ALIGN", -4: "GPT2_ERR_WORKSPACE",
           -5: "GPT2_ERR_CUDA", -6: "GPT2_ERR_DEVICE", -7: "GPT2_ERR_UNSUPPORTED"}
-DEVERR_TOKEN, DEVERR_TIMEOUT, DEVERR_POSITION = 1, 2, 4
+DEVERR_TOKEN, DEVERR_TIMEOUT, DEVERR_POSITION, DEVERR_BLOCK = 1, 2, 4, 8
 
 
 class GPT2Error(RuntimeError):
@@ -46,10 +46,16 @@ class GPT2Config(ctypes.Structure):
                    cfg.num_heads, cfg.channels)
 
 
+class GPT2PagedKVCache(ctypes.Structure):
+    _fields_ = [("pool", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("num_blocks", ctypes.c_int),
+                ("block_size", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _Z = ctypes.c_size_t
 _CFG = ctypes.POINTER(GPT2Config)
+_PKV = ctypes.POINTER(GPT2PagedKVCache)
 
 # name -> (restype, argtypes), in the order of include/gpt2fwd.h
 _SIGNATURES = {
@@ -71,6 +77,9 @@ _SIGNATURES = {
     "gpt2_kvcache_size": (_Z, [_CFG, _I, _I]),
     "gpt2_forward": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _P, _P, _Z, _I, _P]),
     "gpt2_decode_step": (_I, [_CFG, _P, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _I, _P]),
+    "gpt2_paged_kvcache_size": (_Z, [_CFG, _I, _I, _I]),
+    "gpt2_prefill_paged": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _PKV, _P, _Z, _I, _P]),
+    "gpt2_decode_step_paged": (_I, [_CFG, _P, _P, _PKV, _P, _P, _I, _P, _P, _P, _Z, _I, _P]),
     "gpt2_forward_profile": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _I, _P, _P, _I]),
     "gpt2_get_error": (_I, [_P]),
     "gpt2_strerror": (ctypes.c_char_p, [_I]),
@@ -234,6 +243,30 @@ def gpt2_decode_step(cfg, params, packed, kvcache, tok, B, pos, logits, probs, w
 
 
 STAGES = ["encoder", "ln1", "qkv", "attention", "attproj", "ln2", "fc", "fcproj", "lnf", "lm_head", "softmax"]
+
+
+def paged_kv(pool, block_table, num_blocks, block_size, max_blocks_per_seq) -> GPT2PagedKVCache:
+    """The C struct describing a paged cache (pool and block_table: device
+    tensors or addresses)."""
+    return GPT2PagedKVCache(_ptr(pool), _ptr(block_table), num_blocks, block_size, max_blocks_per_seq)
+
+
+def gpt2_paged_kvcache_size(cfg, num_blocks, block_size, precision) -> int:
+    return _lib().gpt2_paged_kvcache_size(_cfg(cfg), num_blocks, block_size, precision)
+
+
+def gpt2_prefill_paged(cfg, params, packed, tok, B, T, logits, probs, kv, workspace, ws_bytes, precision,
+                       stream=None):
+    _check("gpt2_prefill_paged", _lib().gpt2_prefill_paged(
+        _cfg(cfg), _ptr(params), _ptr(packed), _ptr(tok), B, T, _ptr(logits), _ptr(probs),
+        ctypes.byref(kv) if kv is not None else None, _ptr(workspace), ws_bytes, precision, _stream(stream)))
+
+
+def gpt2_decode_step_paged(cfg, params, packed, kv, tok, pos, B, logits, probs, workspace, ws_bytes, precision,
+                           stream=None):
+    _check("gpt2_decode_step_paged", _lib().gpt2_decode_step_paged(
+        _cfg(cfg), _ptr(params), _ptr(packed), ctypes.byref(kv) if kv is not None else None, _ptr(tok), _ptr(pos), B,
+        _ptr(logits), _ptr(probs), _ptr(workspace), ws_bytes, precision, _stream(stream)))
 
 
 def gpt2_forward_profile(cfg, params, packed, tok, B, T, logits, probs, workspace, ws_bytes, precision,

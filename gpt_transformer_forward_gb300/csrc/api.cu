@@ -15,6 +15,7 @@
 // the residual stream x, the logits and the probabilities stay fp32.
 #include <stdio.h>
 
+#include <algorithm>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -184,6 +185,53 @@ size_t kv_elem_bytes(int precision) { return is16(precision) ? 2 : 4; }
 // elements of one layer's cache slab [2][B][NH][maxT][hs]
 size_t kv_layer_elems(const GPT2Config* c, int B) {
   return 2ull * B * c->num_heads * c->max_seq_len * (c->channels / c->num_heads);
+}
+
+// elements of one layer's slab of a paged pool [2][num_blocks][NH][block][hs]
+size_t paged_layer_elems(const GPT2Config* c, int num_blocks, int block_size) {
+  return 2ull * num_blocks * c->num_heads * block_size * (c->channels / c->num_heads);
+}
+
+// A KV cache as the forward pass and the decode step address it: the base
+// of layer 0's slab, the row layout inside one K or V half, and the
+// elements of a layer's slab (its K half, then its V half).
+struct KVLayout {
+  void* base;
+  KVRows rows;
+  size_t layer_elems;
+};
+
+KVLayout dense_kv(const GPT2Config* c, void* cache, int B) {
+  KVLayout k;
+  k.base = cache;
+  k.rows = KVRows{nullptr, 0, 1, B, c->max_seq_len, c->max_seq_len};
+  k.layer_elems = kv_layer_elems(c, B);
+  return k;
+}
+
+int log2_exact(int v) {  // -1 unless v is a power of two
+  if (v <= 0 || (v & (v - 1)) != 0) return -1;
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return l;
+}
+
+// Checks a caller's paged cache description on the host and builds its
+// layout; positions [0, T) must fit one sequence's blocks when T > 0.
+int paged_kv(const GPT2Config* c, const GPT2PagedKVCache* p, int T, KVLayout* out) {
+  RETURN_IF(p == nullptr || p->pool == nullptr || p->block_table == nullptr, GPT2_ERR_ARG);
+  const int lbs = log2_exact(p->block_size);
+  RETURN_IF(lbs < 0 || p->num_blocks <= 0 || p->max_blocks_per_seq <= 0, GPT2_ERR_ARG);
+  RETURN_IF(p->max_blocks_per_seq > kMaxBlocksPerSeq, GPT2_ERR_SHAPE);
+  RETURN_IF((reinterpret_cast<uintptr_t>(p->pool) & 15u) != 0 ||
+                (reinterpret_cast<uintptr_t>(p->block_table) & 3u) != 0,
+            GPT2_ERR_ALIGN);
+  const long long cap = std::min<long long>(c->max_seq_len, static_cast<long long>(p->max_blocks_per_seq) << lbs);
+  RETURN_IF(T > cap, GPT2_ERR_SHAPE);
+  out->base = p->pool;
+  out->rows = KVRows{p->block_table, lbs, p->max_blocks_per_seq, p->num_blocks, c->max_seq_len, static_cast<int>(cap)};
+  out->layer_elems = paged_layer_elems(c, p->num_blocks, p->block_size);
+  return GPT2_OK;
 }
 
 // One GEMM site: picks the kernel for the precision mode.
@@ -393,12 +441,15 @@ size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision) {
   return static_cast<size_t>(cfg->num_layers) * kv_layer_elems(cfg, B) * kv_elem_bytes(precision);
 }
 
-// The body shared by the full forward pass and the decode step.  decode_pos
-// < 0: rows are B sequences x T tokens at positions 0..T-1; otherwise rows
-// are the B sequences' tokens at position decode_pos (T == 1).
+// The body shared by the full forward pass and the decode step.  decode
+// false: rows are B sequences x T tokens at positions 0..T-1 (their keys and
+// values written into kv when it is given: a prefill); decode true: rows are
+// the B sequences' tokens at position decode_pos, or pos_arr[b] when pos_arr
+// is given (T == 1), attending over and appending to kv.
 static int run_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
-                       int decode_pos, float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes,
-                       int precision, cudaStream_t s, StageProfiler* prof = nullptr) {
+                       bool decode, int decode_pos, const int* pos_arr, float* logits, float* probs,
+                       const KVLayout* kv, void* workspace, size_t ws_bytes, int precision, cudaStream_t s,
+                       StageProfiler* prof = nullptr) {
   auto mark = [&](int stage) { return prof ? prof->record(stage) : GPT2_OK; };
   const int C = cfg->channels, L = cfg->num_layers, NH = cfg->num_heads, V = cfg->vocab_size;
   const int Vp = cfg->padded_vocab_size, maxT = cfg->max_seq_len;
@@ -416,7 +467,7 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
   const int op = op_of(precision);
   const PackedOffsets ko = packed_offsets(cfg);
   const uint8_t* pk = static_cast<const uint8_t*>(packed);
-  const size_t kv_slab = kv_layer_elems(cfg, B);
+  const size_t kv_slab = kv != nullptr ? kv->layer_elems : 0;
   const size_t kv_half = kv_slab / 2;
 
   // weight matrix of a GEMM site for layer l
@@ -447,10 +498,10 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
                                    params + w_off, params + b_off, N, C, write_x, s);
   };
 
-  if (decode_pos < 0)
+  if (!decode)
     launch_encoder(x, tok, params + po.wte, params + po.wpe, N, T, C, V, s);
   else
-    launch_encoder_pos(x, tok, params + po.wte, params + po.wpe, B, decode_pos, C, V, s);
+    launch_encoder_pos(x, tok, params + po.wte, params + po.wpe, B, decode_pos, pos_arr, maxT, C, V, s);
   TRY(check_launch());
   TRY(mark(GPT2_STAGE_ENCODER));
 
@@ -463,16 +514,17 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
     TRY(mark(GPT2_STAGE_LN1));
     TRY(gemm(precision, qkv, ln, wmat(po.qkvw, ko.qkvw, 3 * CC, l), params + po.qkvb + static_cast<size_t>(l) * 3 * C,
              N, 3 * C, C, bf16 ? kEpiOut16 : kEpiF32, s));
-    if (kvcache != nullptr && decode_pos < 0) {  // a decode step appends in its attention kernel
-      if (bf16)
-        launch_kv_store_16(static_cast<uint16_t*>(kvcache) + l * kv_slab, static_cast<const uint16_t*>(qkv), B, T,
-                           C, NH, maxT, 0, s);
-      else
-        launch_kv_store_f32(static_cast<float*>(kvcache) + l * kv_slab, static_cast<const float*>(qkv), B, T, C, NH,
-                            maxT, 0, s);
+    if (kv != nullptr && !decode) {  // a decode step appends in its attention kernel
+      if (bf16) {
+        uint16_t* kc = static_cast<uint16_t*>(kv->base) + l * kv_slab;
+        launch_kv_store_16(kc, kc + kv_half, static_cast<const uint16_t*>(qkv), B, T, C, NH, kv->rows, s);
+      } else {
+        float* kc = static_cast<float*>(kv->base) + l * kv_slab;
+        launch_kv_store_f32(kc, kc + kv_half, static_cast<const float*>(qkv), B, T, C, NH, kv->rows, s);
+      }
     }
     TRY(mark(GPT2_STAGE_QKV));
-    if (decode_pos < 0) {
+    if (!decode) {
       if (precision == GPT2_FP32) {
         TRY(launch_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), B, T, C, NH, s));
       } else if (precision == GPT2_TF32) {
@@ -484,12 +536,12 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
       }
     } else {
       if (bf16) {
-        uint16_t* kc = static_cast<uint16_t*>(kvcache) + l * kv_slab;
-        launch_decode_attention_16(att, true, qkv, kc, kc + kv_half, op, B, C, NH, maxT, decode_pos, s);
+        uint16_t* kc = static_cast<uint16_t*>(kv->base) + l * kv_slab;
+        launch_decode_attention_16(att, true, qkv, kc, kc + kv_half, op, B, C, NH, decode_pos, pos_arr, kv->rows, s);
       } else {
-        float* kc = static_cast<float*>(kvcache) + l * kv_slab;
+        float* kc = static_cast<float*>(kv->base) + l * kv_slab;
         launch_decode_attention_f32(static_cast<float*>(att), static_cast<const float*>(qkv), kc, kc + kv_half, B, C,
-                                    NH, maxT, decode_pos, s);
+                                    NH, decode_pos, pos_arr, kv->rows, s);
       }
     }
     TRY(check_launch());
@@ -546,8 +598,9 @@ int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed,
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
             GPT2_ERR_ALIGN);
   PdlScope pdl(is16(precision));  // every kernel of the 16-bit pass waits for its predecessor itself
-  return run_forward(cfg, params, packed, tok, B, T, -1, logits, probs, kvcache, workspace, ws_bytes, precision,
-                     as_stream(stream));
+  const KVLayout kv = dense_kv(cfg, kvcache, B);
+  return run_forward(cfg, params, packed, tok, B, T, false, 0, nullptr, logits, probs,
+                     kvcache != nullptr ? &kv : nullptr, workspace, ws_bytes, precision, as_stream(stream));
 }
 
 int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
@@ -567,8 +620,8 @@ int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void*
   StageProfiler prof{as_stream(stream), {}, {}};
   int rc = prof.begin();
   if (rc == GPT2_OK)
-    rc = run_forward(cfg, params, packed, tok, B, T, -1, logits, probs, nullptr, workspace, ws_bytes, precision,
-                     as_stream(stream), &prof);
+    rc = run_forward(cfg, params, packed, tok, B, T, false, 0, nullptr, logits, probs, nullptr, workspace, ws_bytes,
+                     precision, as_stream(stream), &prof);
   const int rc2 = prof.finish(stage_ms, n_stages);
   return rc != GPT2_OK ? rc : rc2;
 }
@@ -587,7 +640,54 @@ int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* pac
                 (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
             GPT2_ERR_ALIGN);
   PdlScope pdl(is16(precision));  // every kernel of the 16-bit step waits for its predecessor itself
-  return run_forward(cfg, params, packed, tok, B, 1, pos, logits, probs, kvcache, workspace, ws_bytes, precision,
+  const KVLayout kv = dense_kv(cfg, kvcache, B);
+  return run_forward(cfg, params, packed, tok, B, 1, true, pos, nullptr, logits, probs, &kv, workspace, ws_bytes,
+                     precision, as_stream(stream));
+}
+
+size_t gpt2_paged_kvcache_size(const GPT2Config* cfg, int num_blocks, int block_size, int precision) {
+  if (check_config(cfg) != GPT2_OK || num_blocks <= 0 || log2_exact(block_size) < 0 || !valid_precision(precision))
+    return 0;
+  return static_cast<size_t>(cfg->num_layers) * paged_layer_elems(cfg, num_blocks, block_size) *
+         kv_elem_bytes(precision);
+}
+
+int gpt2_prefill_paged(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                       float* logits, float* probs, const GPT2PagedKVCache* kvc, void* workspace, size_t ws_bytes,
+                       int precision, void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !tok || !logits || !workspace || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(B <= 0 || T <= 0, GPT2_ERR_ARG);
+  RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  RETURN_IF(is16(precision) && packed == nullptr, GPT2_ERR_ARG);
+  KVLayout kv;
+  TRY(paged_kv(cfg, kvc, T, &kv));
+  RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
+                (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
+            GPT2_ERR_ALIGN);
+  PdlScope pdl(is16(precision));
+  return run_forward(cfg, params, packed, tok, B, T, false, 0, nullptr, logits, probs, &kv, workspace, ws_bytes,
+                     precision, as_stream(stream));
+}
+
+int gpt2_decode_step_paged(const GPT2Config* cfg, const float* params, const void* packed,
+                           const GPT2PagedKVCache* kvc, const int* tok, const int* pos, int B, float* logits,
+                           float* probs, void* workspace, size_t ws_bytes, int precision, void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !tok || !pos || !logits || !workspace || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(B <= 0, GPT2_ERR_ARG);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  RETURN_IF(is16(precision) && packed == nullptr, GPT2_ERR_ARG);
+  KVLayout kv;
+  TRY(paged_kv(cfg, kvc, 0, &kv));
+  RETURN_IF(!aligned16(params) || !aligned16(logits) || (probs && !aligned16(probs)) ||
+                (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                (packed && (reinterpret_cast<uintptr_t>(packed) & 255u) != 0),
+            GPT2_ERR_ALIGN);
+  PdlScope pdl(is16(precision));
+  return run_forward(cfg, params, packed, tok, B, 1, true, 0, pos, logits, probs, &kv, workspace, ws_bytes, precision,
                      as_stream(stream));
 }
 

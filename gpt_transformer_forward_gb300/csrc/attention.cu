@@ -318,12 +318,19 @@ __global__ void __launch_bounds__(64) attn_f32_kernel(float* __restrict__ out, c
 // head's output row: one launch, no scratch.  The token's own key and value
 // (position pos) are read from the QKV row, and the block also appends them
 // to the cache for the steps that follow.
+//
+// Cache rows are found through KVRows: a dense cache [B][NH][maxT][hs] per
+// layer and K/V half, or a paged pool [num_blocks][NH][block][hs] whose
+// block of position p of sequence b is table[b][p / block] (the block-table
+// layout of a paged KV cache).  Positions come from `pos` (all sequences
+// at one position) or, when pos_arr is given, per sequence from it.
 constexpr int kDecWarps = 4;
 
 template <typename E, typename OutT, int HS>
 __global__ void __launch_bounds__(32 * kDecWarps)
     decode_attn_kernel(OutT* __restrict__ out, const E* __restrict__ qkv, E* __restrict__ kcache,
-                       E* __restrict__ vcache, int C, int NH, int maxT, int pos, float scale_log2) {
+                       E* __restrict__ vcache, int C, int NH, int pos_all, const int* __restrict__ pos_arr,
+                       KVRows rows, float scale_log2) {
   constexpr int kPer = 16 / static_cast<int>(sizeof(E));  // elements per 16-byte load
   constexpr int kLPR = HS / kPer;                          // lanes per K or V row
   constexpr int kRPI = 32 / kLPR;                          // rows per warp instruction
@@ -332,23 +339,50 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   static_assert(kLPR >= 1 && kLPR <= 32 && 32 % kLPR == 0, "head size and element type");
   __shared__ float m_s[kDecWarps], l_s[kDecWarps];
   __shared__ float o_s[kDecWarps][HS];
+  __shared__ int tbl_s[kMaxBlocksPerSeq];  // this sequence's block table (paged layout)
   const int h = blockIdx.x, b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane / kLPR;   // row of an instruction this lane reads
   const int dg = lane % kLPR;  // its dimensions dg * kPer .. dg * kPer + kPer - 1
-  const size_t head = (static_cast<size_t>(b) * NH + h) * maxT;
-  // The cache rows before pos were written by earlier steps: this warp's
-  // first chunk of them is fetched into L2 while the QKV projection before
-  // this kernel finishes (a prefetch has no other effect).
-  for (int i = 0; i < kIt; ++i) {
-    const int j = warp * kChunk + i * kRPI + g;
-    if (j < pos && dg == 0) {
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(kcache + (head + j) * HS));
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(vcache + (head + j) * HS));
+  // the caller's positions and block table are inputs of the step, written
+  // before its first kernel: they may be read before the wait below
+  const int pos = pos_arr != nullptr ? __ldg(pos_arr + b) : pos_all;
+  const bool pos_ok = pos >= 0 && pos < rows.capacity;
+  if (rows.table != nullptr && pos_ok) {
+    for (int i = threadIdx.x; i <= (pos >> rows.lbs); i += blockDim.x) {
+      int blk = __ldg(rows.table + static_cast<size_t>(b) * rows.max_blocks + i);
+      if (blk < 0 || blk >= rows.num_blocks) {
+        if (h == 0) set_error(GPT2_DEVERR_BLOCK);
+        blk = 0;
+      }
+      tbl_s[i] = blk;
+    }
+  }
+  __syncthreads();
+  // row index of cache position j of (b, h)
+  auto row = [&](int j) -> size_t {
+    if (rows.table == nullptr) return (static_cast<size_t>(b) * NH + h) * rows.maxT + j;
+    return ((static_cast<size_t>(tbl_s[j >> rows.lbs]) * NH + h) << rows.lbs) + (j & ((1 << rows.lbs) - 1));
+  };
+  if (pos_ok) {
+    // The cache rows before pos were written by earlier steps: this warp's
+    // first chunk of them is fetched into L2 while the QKV projection before
+    // this kernel finishes (a prefetch has no other effect).
+    for (int i = 0; i < kIt; ++i) {
+      const int j = warp * kChunk + i * kRPI + g;
+      if (j < pos && dg == 0) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(kcache + row(j) * HS));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(vcache + row(j) * HS));
+      }
     }
   }
   pdl_wait();  // q and this token's key and value come from the QKV projection
   pdl_trigger();
+  if (!pos_ok) {  // a position outside the cache: flagged, the row's output is zero
+    if (threadIdx.x == 0) set_error(GPT2_DEVERR_POSITION);
+    for (int d = threadIdx.x; d < HS; d += blockDim.x) out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(0.f);
+    return;
+  }
   // the query's dimensions of this lane, scaled by log2(e) / sqrt(hs)
   float q[kPer];
   {
@@ -357,14 +391,12 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) q[k] = to_f32(e[k]) * scale_log2;
   }
-  const uint4* kb = reinterpret_cast<const uint4*>(kcache + head * HS) + dg;
-  const uint4* vb = reinterpret_cast<const uint4*>(vcache + head * HS) + dg;
   // this token's key and value: used for position pos, and appended
   const uint4* kq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + C + h * HS) + dg;
   const uint4* vq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + 2 * C + h * HS) + dg;
   if (threadIdx.x < kLPR) {
-    reinterpret_cast<uint4*>(kcache + (head + pos) * HS)[dg] = __ldg(kq);
-    reinterpret_cast<uint4*>(vcache + (head + pos) * HS)[dg] = __ldg(vq);
+    reinterpret_cast<uint4*>(kcache + row(pos) * HS)[dg] = __ldg(kq);
+    reinterpret_cast<uint4*>(vcache + row(pos) * HS)[dg] = __ldg(vq);
   }
   float m = -INFINITY, l = 0.f, acc[kPer];
 #pragma unroll
@@ -377,8 +409,9 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     for (int i = 0; i < kIt; ++i) {
       const int j = j0 + i * kRPI;
       if (j < pos) {
-        kr[i] = __ldg(kb + static_cast<size_t>(j) * kLPR);
-        vr[i] = __ldg(vb + static_cast<size_t>(j) * kLPR);
+        const size_t rj = row(j) * HS;
+        kr[i] = __ldg(reinterpret_cast<const uint4*>(kcache + rj) + dg);
+        vr[i] = __ldg(reinterpret_cast<const uint4*>(vcache + rj) + dg);
       } else if (j == pos) {
         kr[i] = __ldg(kq);
         vr[i] = __ldg(vq);
@@ -495,16 +528,16 @@ int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int 
 }
 
 template <typename E, typename OutT, int HS>
-static void decode_typed(OutT* out, const E* qkv, E* kc, E* vc, int B, int C, int NH, int maxT, int pos,
-                         cudaStream_t s) {
+static void decode_typed(OutT* out, const E* qkv, E* kc, E* vc, int B, int C, int NH, int pos, const int* pos_arr,
+                         const KVRows& rows, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
-  launch_pdl(decode_attn_kernel<E, OutT, HS>, dim3(NH, B), dim3(32 * kDecWarps), 0, s, out, qkv, kc, vc, C, NH, maxT,
-             pos, scale_log2);
+  launch_pdl(decode_attn_kernel<E, OutT, HS>, dim3(NH, B), dim3(32 * kDecWarps), 0, s, out, qkv, kc, vc, C, NH, pos,
+             pos_arr, rows, scale_log2);
 }
 
 template <typename E>
 static void decode_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int B, int C, int NH,
-                      int maxT, int pos, cudaStream_t s) {
+                      int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s) {
   const E* q = static_cast<const E*>(qkv);
   E* kc = static_cast<E*>(kcache);
   E* vc = static_cast<E*>(vcache);
@@ -512,34 +545,34 @@ static void decode_16(void* out, bool out16, const void* qkv, void* kcache, void
   float* o32 = static_cast<float*>(out);
   switch (C / NH) {
     case 16:
-      if (out16) decode_typed<E, E, 16>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
-      else decode_typed<E, float, 16>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
+      if (out16) decode_typed<E, E, 16>(o16, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
+      else decode_typed<E, float, 16>(o32, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
       break;
     case 32:
-      if (out16) decode_typed<E, E, 32>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
-      else decode_typed<E, float, 32>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
+      if (out16) decode_typed<E, E, 32>(o16, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
+      else decode_typed<E, float, 32>(o32, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
       break;
     default:
-      if (out16) decode_typed<E, E, 64>(o16, q, kc, vc, B, C, NH, maxT, pos, s);
-      else decode_typed<E, float, 64>(o32, q, kc, vc, B, C, NH, maxT, pos, s);
+      if (out16) decode_typed<E, E, 64>(o16, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
+      else decode_typed<E, float, 64>(o32, q, kc, vc, B, C, NH, pos, pos_arr, rows, s);
       break;
   }
 }
 
 void launch_decode_attention_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int op, int B,
-                                int C, int NH, int maxT, int pos, cudaStream_t s) {
+                                int C, int NH, int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s) {
   if (op == kOpF16)
-    decode_16<__half>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, s);
+    decode_16<__half>(out, out16, qkv, kcache, vcache, B, C, NH, pos, pos_arr, rows, s);
   else
-    decode_16<__nv_bfloat16>(out, out16, qkv, kcache, vcache, B, C, NH, maxT, pos, s);
+    decode_16<__nv_bfloat16>(out, out16, qkv, kcache, vcache, B, C, NH, pos, pos_arr, rows, s);
 }
 
 void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, float* vcache, int B, int C, int NH,
-                                 int maxT, int pos, cudaStream_t s) {
+                                 int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s) {
   switch (C / NH) {
-    case 16: decode_typed<float, float, 16>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
-    case 32: decode_typed<float, float, 32>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
-    default: decode_typed<float, float, 64>(out, qkv, kcache, vcache, B, C, NH, maxT, pos, s); break;
+    case 16: decode_typed<float, float, 16>(out, qkv, kcache, vcache, B, C, NH, pos, pos_arr, rows, s); break;
+    case 32: decode_typed<float, float, 32>(out, qkv, kcache, vcache, B, C, NH, pos, pos_arr, rows, s); break;
+    default: decode_typed<float, float, 64>(out, qkv, kcache, vcache, B, C, NH, pos, pos_arr, rows, s); break;
   }
 }
 

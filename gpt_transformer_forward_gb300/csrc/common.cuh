@@ -18,7 +18,8 @@
 // bits of the device error word
 #define GPT2_DEVERR_TOKEN 1u      // a token id outside [0, V)
 #define GPT2_DEVERR_TIMEOUT 2u    // a pipeline wait gave up (bounded spin)
-#define GPT2_DEVERR_POSITION 4u   // a position outside [0, maxT)
+#define GPT2_DEVERR_POSITION 4u   // a position outside [0, maxT) or past a sequence's cache
+#define GPT2_DEVERR_BLOCK 8u      // a block-table entry outside [0, num_blocks)
 
 namespace gpt2 {
 
@@ -520,6 +521,13 @@ __device__ __forceinline__ float exp2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ float gelu_exact(float x) {

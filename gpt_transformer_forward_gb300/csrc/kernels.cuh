@@ -45,11 +45,28 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Where the cached keys and values of (sequence b, head h, position p) live
+// inside one layer's K (or V) half of a KV cache.  Dense (table == nullptr):
+// [B][NH][maxT][hs], row (b * NH + h) * maxT + p.  Paged: a pool of blocks
+// [num_blocks][NH][2^lbs][hs]; position p of sequence b is in block
+// table[b * max_blocks + p / 2^lbs], row (block * NH + h) * 2^lbs + p % 2^lbs.
+constexpr int kMaxBlocksPerSeq = 1024;  // block-table entries per sequence (paged layout)
+struct KVRows {
+  const int* table;
+  int lbs;
+  int max_blocks;
+  int num_blocks;
+  int maxT;
+  int capacity;  // positions one sequence can hold
+};
+
 // rowwise.cu
 void launch_encoder(float* out, const int* tok, const float* wte, const float* wpe, int N, int T, int C, int V,
                     cudaStream_t s);
-void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos, int C, int V,
-                        cudaStream_t s);
+// Decode-step encoder: row b is token tok[b] at position pos (pos_arr[b]
+// when pos_arr is given; one outside [0, maxT) is flagged and read as 0).
+void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos,
+                        const int* pos_arr, int maxT, int C, int V, cudaStream_t s);
 void launch_layernorm_f32(float* out, float* mean, float* rstd, const float* inp, const float* w, const float* b,
                           int N, int C, cudaStream_t s);
 // LayerNorm writing the 16-bit operand type T (bf16 or fp16)
@@ -66,11 +83,13 @@ void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cud
 void launch_argmax(int* next, const float* logits, int B, int V, int Vp, cudaStream_t s);
 template <typename T>
 void launch_f32_to_16(T* out, const float* in, long long n, cudaStream_t s);
-void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, int NH, int maxT, int pos0,
+// Copies the keys and values of rows [0, T) of each sequence from the QKV
+// buffer [B*T, 3C] into one layer's cache halves kc, vc (positions 0..T-1).
+void launch_kv_store_f32(float* kc, float* vc, const float* qkv, int B, int T, int C, int NH, const KVRows& rows,
                          cudaStream_t s);
 // 16-bit cache (bf16 or fp16: a plain copy of 2-byte elements)
-void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
-                        cudaStream_t s);
+void launch_kv_store_16(uint16_t* kc, uint16_t* vc, const uint16_t* qkv, int B, int T, int C, int NH,
+                        const KVRows& rows, cudaStream_t s);
 
 // Encodes a tiled TMA map with the given shared-memory swizzle: dims[0]
 // innermost (in elements), strides_bytes[i] the byte stride of dimension
@@ -132,11 +151,12 @@ int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B,
 // fp32 CUDA-core causal attention (head size 16, 32 or 64).
 int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s);
 // Decode attention: one query per sequence (row b of qkv [B,3C]) against the
-// cache positions [0, pos], the key and value of position pos taken from
-// qkv and appended to the cache; output [B,C].
+// cache positions [0, pos] (pos_arr[b] when pos_arr is given), the key and
+// value of position pos taken from qkv and appended to the cache; output
+// [B,C].  kcache, vcache: the layer's K and V halves, laid out as `rows`.
 void launch_decode_attention_16(void* out, bool out16, const void* qkv, void* kcache, void* vcache, int op, int B,
-                                int C, int NH, int maxT, int pos, cudaStream_t s);
+                                int C, int NH, int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s);
 void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, float* vcache, int B, int C, int NH,
-                                 int maxT, int pos, cudaStream_t s);
+                                 int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s);
 
 }  // namespace gpt2

@@ -34,10 +34,10 @@ __global__ void encoder_kernel(float4* __restrict__ out, const int* __restrict__
   out[idx] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
 }
 
-// Decode-step encoder: row b is token tok[b] at position pos.
+// Decode-step encoder: row b is token tok[b] at position pos (or pos_arr[b]).
 __global__ void encoder_pos_kernel(float4* __restrict__ out, const int* __restrict__ tok,
-                                   const float4* __restrict__ wte, const float4* __restrict__ wpe, int B, int pos,
-                                   int C4, int V) {
+                                   const float4* __restrict__ wte, const float4* __restrict__ wpe, int B, int pos_all,
+                                   const int* __restrict__ pos_arr, int maxT, int C4, int V) {
   pdl_wait();  // tok comes from the argmax before it
   pdl_trigger();
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -47,6 +47,11 @@ __global__ void encoder_pos_kernel(float4* __restrict__ out, const int* __restri
   if (ix < 0 || ix >= V) {
     if (c == 0) set_error(GPT2_DEVERR_TOKEN);
     ix = 0;
+  }
+  int pos = pos_arr != nullptr ? __ldg(pos_arr + b) : pos_all;
+  if (pos < 0 || pos >= maxT) {
+    if (c == 0) set_error(GPT2_DEVERR_POSITION);
+    pos = 0;
   }
   const float4 a = __ldg(wte + static_cast<size_t>(ix) * C4 + c);
   const float4 p = __ldg(wpe + static_cast<size_t>(pos) * C4 + c);
@@ -63,13 +68,13 @@ void launch_encoder(float* out, const int* tok, const float* wte, const float* w
              reinterpret_cast<const float4*>(wte), reinterpret_cast<const float4*>(wpe), N, T, C4, V);
 }
 
-void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos, int C, int V,
-                        cudaStream_t s) {
+void launch_encoder_pos(float* out, const int* tok, const float* wte, const float* wpe, int B, int pos,
+                        const int* pos_arr, int maxT, int C, int V, cudaStream_t s) {
   const int C4 = C / 4;
   const int threads = 256;
   launch_pdl(encoder_pos_kernel, dim3((B * C4 + threads - 1) / threads), dim3(threads), 0, s,
              reinterpret_cast<float4*>(out), tok, reinterpret_cast<const float4*>(wte),
-             reinterpret_cast<const float4*>(wpe), B, pos, C4, V);
+             reinterpret_cast<const float4*>(wpe), B, pos, pos_arr, maxT, C4, V);
 }
 
 // -------------------------------------------------------------- LayerNorm
@@ -562,12 +567,12 @@ template void launch_f32_to_16<__half>(__half*, const float*, long long, cudaStr
 
 // ----------------------------------------------------------- KV cache
 // Copies keys and values of rows [0, T) of each sequence from the QKV buffer
-// ([B*T, 3C], element type T_) into a layer's cache slab
-// [2][B][NH][maxT][hs] at positions [pos0, pos0 + T).  One thread per 16
-// bytes of a head row.
+// ([B*T, 3C], element type E) into a layer's cache halves at positions
+// [0, T), through the cache's row layout (dense or paged).  One thread per
+// 16 bytes of a head row.
 template <typename E>
-__global__ void kv_store_kernel(E* __restrict__ cache, const E* __restrict__ qkv, int B, int T, int C, int NH,
-                                int maxT, int pos0) {
+__global__ void kv_store_kernel(E* __restrict__ kc, E* __restrict__ vc, const E* __restrict__ qkv, int B, int T,
+                                int C, int NH, KVRows rows) {
   pdl_wait();  // the QKV projection ahead has finished
   pdl_trigger();
   constexpr int kPer = 16 / sizeof(E);
@@ -582,24 +587,34 @@ __global__ void kv_store_kernel(E* __restrict__ cache, const E* __restrict__ qkv
     const int t = static_cast<int>(r % T); r /= T;
     const int b = static_cast<int>(r % B); r /= B;
     const int kv = static_cast<int>(r);  // 0 = keys, 1 = values
+    size_t row;
+    if (rows.table == nullptr) {
+      row = (static_cast<size_t>(b) * NH + h) * rows.maxT + t;
+    } else {
+      int blk = __ldg(rows.table + static_cast<size_t>(b) * rows.max_blocks + (t >> rows.lbs));
+      if (blk < 0 || blk >= rows.num_blocks) {
+        if (ch == 0 && h == 0) set_error(GPT2_DEVERR_BLOCK);
+        continue;
+      }
+      row = ((static_cast<size_t>(blk) * NH + h) << rows.lbs) + (t & ((1 << rows.lbs) - 1));
+    }
     const E* src = qkv + (static_cast<size_t>(b) * T + t) * 3 * C + (kv + 1) * C + h * hs + ch * kPer;
-    E* dst = cache + ((((static_cast<size_t>(kv) * B + b) * NH + h) * maxT) + pos0 + t) * hs + ch * kPer;
+    E* dst = (kv == 0 ? kc : vc) + row * hs + ch * kPer;
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
 }
 
-void launch_kv_store_f32(float* cache, const float* qkv, int B, int T, int C, int NH, int maxT, int pos0,
+void launch_kv_store_f32(float* kc, float* vc, const float* qkv, int B, int T, int C, int NH, const KVRows& rows,
                          cudaStream_t s) {
   const long long total = 2LL * B * T * C / 4;
-  launch_pdl(kv_store_kernel<float>, dim3(stream_grid(total, 256)), dim3(256), 0, s, cache, qkv, B, T, C, NH, maxT,
-             pos0);
+  launch_pdl(kv_store_kernel<float>, dim3(stream_grid(total, 256)), dim3(256), 0, s, kc, vc, qkv, B, T, C, NH, rows);
 }
 
-void launch_kv_store_16(uint16_t* cache, const uint16_t* qkv, int B, int T, int C, int NH, int maxT, int pos0,
-                        cudaStream_t s) {
+void launch_kv_store_16(uint16_t* kc, uint16_t* vc, const uint16_t* qkv, int B, int T, int C, int NH,
+                        const KVRows& rows, cudaStream_t s) {
   const long long total = 2LL * B * T * C / 8;
-  launch_pdl(kv_store_kernel<uint16_t>, dim3(stream_grid(total, 256)), dim3(256), 0, s, cache, qkv, B, T, C, NH,
-             maxT, pos0);
+  launch_pdl(kv_store_kernel<uint16_t>, dim3(stream_grid(total, 256)), dim3(256), 0, s, kc, vc, qkv, B, T, C, NH,
+             rows);
 }
 
 }  // namespace gpt2

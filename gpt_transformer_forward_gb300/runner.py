@@ -46,6 +46,11 @@ class GPT2Model:
         nbytes = ab.gpt2_kvcache_size(self.cfg, B, self.precision)
         return torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
 
+    def new_paged_kvcache(self, num_blocks: int, block_size: int):
+        """A zeroed pool of num_blocks blocks of block_size positions."""
+        nbytes = ab.gpt2_paged_kvcache_size(self.cfg, num_blocks, block_size, self.precision)
+        return torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+
     # ----------------------------------------------------------------- calls
     def forward(self, tok, logits, probs=None, kvcache=None, stream=None):
         B, T = tok.shape
@@ -61,3 +66,17 @@ class GPT2Model:
         B = tok.shape[0]
         ab.gpt2_decode_step(self.cfg, self.params, self.packed, kvcache, tok, B, pos, logits, probs,
                             self.workspace, self.ws_bytes, self.precision, stream)
+
+    def prefill_paged(self, tok, logits, kv, probs=None, stream=None):
+        """gpt2_forward writing positions [0, T) through the paged cache kv
+        (a binding.GPT2PagedKVCache)."""
+        B, T = tok.shape
+        ab.gpt2_prefill_paged(self.cfg, self.params, self.packed, tok, B, T, logits, probs, kv, self.workspace,
+                              self.ws_bytes, self.precision, stream)
+
+    def decode_step_paged(self, kv, tok, pos, logits, probs=None, stream=None):
+        """One decode step, sequence b at position pos[b] (a device int32
+        tensor)."""
+        B = tok.shape[0]
+        ab.gpt2_decode_step_paged(self.cfg, self.params, self.packed, kv, tok, pos, B, logits, probs, self.workspace,
+                                  self.ws_bytes, self.precision, stream)

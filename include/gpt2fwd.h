@@ -92,7 +92,8 @@ enum {
  * combined into a positive bit set, see below). */
 #define GPT2_DEVERR_TOKEN_BIT 1    /* token id outside [0, V); the read was clamped */
 #define GPT2_DEVERR_TIMEOUT_BIT 2  /* a pipeline wait gave up after ~1 s */
-#define GPT2_DEVERR_POSITION_BIT 4 /* a decode position outside [0, maxT) */
+#define GPT2_DEVERR_POSITION_BIT 4 /* a decode position outside [0, maxT) or past its sequence's blocks */
+#define GPT2_DEVERR_BLOCK_BIT 8    /* a block-table entry outside [0, num_blocks); read as block 0 */
 
 /* ----------------------------------------------------------- single steps */
 
@@ -251,6 +252,63 @@ GPT2_API int gpt2_forward(const GPT2Config* cfg, const float* params, const void
 GPT2_API int gpt2_decode_step(const GPT2Config* cfg, const float* params, const void* packed, void* kvcache, const int* tok,
                      int B, int pos, float* logits, float* probs, void* workspace, size_t ws_bytes, int precision,
                      void* stream);
+
+/* --------------------------------------------------- paged KV cache */
+
+/* A paged KV cache [NTU "KV Caching": the keys and values of earlier
+ * positions are kept and reused, not recomputed].  Instead of one dense
+ * [maxT] slab per sequence, positions live in fixed-size blocks of a shared
+ * pool, found through a per-sequence block table, so that sequences of
+ * different lengths share one allocation and a sequence holds only the
+ * blocks it uses.
+ *   pool:        DEVICE, gpt2_paged_kvcache_size(cfg, num_blocks,
+ *                block_size, precision) bytes, 16-byte aligned; layout
+ *                [L][2][num_blocks][NH][block_size][hs] (per layer the key
+ *                blocks, then the value blocks), element type as the dense
+ *                cache's (fp32, or the 16-bit type in GPT2_BF16/GPT2_FP16);
+ *   block_table: DEVICE int32 [B][max_blocks_per_seq]: position p of
+ *                sequence b is in block block_table[b][p / block_size],
+ *                slot p % block_size.  Entries a call never reaches may hold
+ *                anything; an entry it reaches outside [0, num_blocks) sets
+ *                GPT2_DEVERR_BLOCK_BIT (block 0 is used instead).
+ *   block_size:  positions per block, a power of two;
+ *   max_blocks_per_seq: row length of block_table, 1 .. 1024.
+ * A sequence can hold min(maxT, max_blocks_per_seq * block_size)
+ * positions.  The library never writes block_table; the caller owns the
+ * pool, the table and the assignment of blocks to sequences. */
+typedef struct {
+  void* pool;
+  const int* block_table;
+  int num_blocks;
+  int block_size;
+  int max_blocks_per_seq;
+} GPT2PagedKVCache;
+
+/* Bytes of a paged pool of num_blocks blocks (0 for invalid arguments). */
+GPT2_API size_t gpt2_paged_kvcache_size(const GPT2Config* cfg, int num_blocks, int block_size, int precision);
+
+/* gpt2_forward that writes the keys and values of positions [0, T) of each
+ * sequence into the paged cache `kv` (the prefill of paged decoding); the
+ * outputs are gpt2_forward's.  Prompts of different lengths can share one
+ * call padded to T: each sequence's later decode steps start at its own
+ * length and overwrite the padded positions.  Requires T <= the capacity
+ * of a sequence.  Other arguments as gpt2_forward. */
+GPT2_API int gpt2_prefill_paged(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B,
+                                int T, float* logits, float* probs, const GPT2PagedKVCache* kv, void* workspace,
+                                size_t ws_bytes, int precision, void* stream);
+
+/* One KV-cached decode step over a paged cache [NTU "KV Caching"], each
+ * sequence at its own position: sequence b has pos[b] positions cached and
+ * gets token tok[b] at position pos[b] (pos: DEVICE int32 [B]).  Writes
+ * that position's keys and values through the block table and computes
+ * logits [B,Vp] (probs [B,Vp] when non-null) exactly as row pos[b] of
+ * gpt2_forward over that sequence would.  A pos[b] outside [0, capacity)
+ * sets GPT2_DEVERR_POSITION_BIT and leaves the cache unwritten (that row's
+ * results are not meaningful).  Workspace: gpt2_workspace_size(cfg, B, 1,
+ * precision).  Launch behaviour as gpt2_decode_step. */
+GPT2_API int gpt2_decode_step_paged(const GPT2Config* cfg, const float* params, const void* packed,
+                                    const GPT2PagedKVCache* kv, const int* tok, const int* pos, int B, float* logits,
+                                    float* probs, void* workspace, size_t ws_bytes, int precision, void* stream);
 
 /* ------------------------------------------------------------ diagnostics */
 

@@ -17,7 +17,7 @@ def lib():
 
 def test_every_declared_function_is_exported(lib):
     names = ab.header_functions()
-    assert len(names) == 23
+    assert len(names) == 26
     for n in names:
         assert hasattr(lib, n), n
         assert n in ab._SIGNATURES, n
@@ -84,3 +84,26 @@ def test_wait_timeout_diagnostic_checks_its_arguments_on_the_host(lib):
     assert e.value.code == -1
     assert lib.gpt2_diag_wait_timeout(999, None, None) == -1
     assert lib.gpt2_diag_wait_timeout(2_000_000_000, None, None) == -1
+
+
+def test_paged_calls_check_their_arguments_on_the_host(lib):
+    cfg = inputs.TINY
+    assert ab.gpt2_paged_kvcache_size(cfg, 10, 16, ab.GPT2_FP16) == cfg.num_layers * 2 * 10 * cfg.channels * 16 * 2
+    assert ab.gpt2_paged_kvcache_size(cfg, 10, 24, ab.GPT2_FP16) == 0  # not a power of two
+    assert ab.gpt2_paged_kvcache_size(cfg, 0, 16, ab.GPT2_FP16) == 0
+    fake = 1 << 20  # an aligned address that is never dereferenced: every call below fails its checks first
+    for bs, nb, mb, code in [(24, 8, 4, -1), (16, 0, 4, -1), (16, 8, 0, -1), (16, 8, 2000, -2)]:
+        kv = ab.paged_kv(fake, fake, nb, bs, mb)
+        with pytest.raises(ab.GPT2Error) as e:
+            ab.gpt2_decode_step_paged(cfg, fake, fake, kv, fake, fake, 2, fake, None, fake, 1 << 20, ab.GPT2_FP16,
+                                      stream=0)
+        assert e.value.code == code, (bs, nb, mb)
+    # a prompt longer than one sequence's blocks (2 blocks of 16 positions)
+    kv = ab.paged_kv(fake, fake, 8, 16, 2)
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_prefill_paged(cfg, fake, fake, fake, 2, 40, fake, None, kv, fake, 1 << 20, ab.GPT2_FP16, stream=0)
+    assert e.value.code == -2
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_decode_step_paged(cfg, fake, fake, None, fake, fake, 2, fake, None, fake, 1 << 20, ab.GPT2_FP16,
+                                  stream=0)
+    assert e.value.code == -1

@@ -11,15 +11,14 @@ padding, causality, batch permutation) are checked on every row.
 Tolerances: logits 2e-2 absolute and probabilities 1e-3 absolute with
 tensor-core operands (fp16, bf16, tf32); 1e-4 / 1e-6 in fp32 mode.
 
-bf16 operands meet the 2e-2 logit bar up to 6 layers of 124M width (the
-tests below), not at 12 (124M) or 24 (medium) layers: there the largest
-logit error is 2.1e-2 (124M) and 2.7e-2 (medium) over tens of millions of
-compared logits, from bf16's 8-bit rounding of every operand, and keeping
-the projections' outputs in fp32 did not change that (measured).  So bf16
-at full depth is checked for the properties that hold at any precision,
-and the full-depth parity claims are fp16's and tf32's."""
-import dataclasses
-
+bf16 operands meet the 2e-2 logit bar at the tiny width (C = 64) but not
+at GPT-2's width (C = 768): there the largest logit error is 2.1e-2 at 6
+and at 12 layers and 2.7e-2 at medium's 24 layers (C = 1024), over millions
+of compared logits, from bf16's 8-bit rounding of the operands; keeping the
+projections' outputs in fp32 did not change that (measured).  So bf16 is
+held to the bar at the tiny width, and at full width it is checked for the
+properties that hold at any precision; the full-width parity claims are
+fp16's and tf32's."""
 import numpy as np
 import pytest
 import torch
@@ -136,22 +135,9 @@ def test_gpt2_medium_sampled():
     check_sampled(w, ab.GPT2_FP16, logits, probs, params, tok, 32, w.B - 1)
 
 
-def test_bf16_at_124m_width_six_layers():
-    # the bf16 parity case: 124M width and vocabulary, half its depth
-    cfg = dataclasses.replace(inputs.GPT2_124M, num_layers=6)
-    w = inputs.Workload("gpt2-124m-width-L6-b2", cfg, B=2, T=1024, index=5)
-    params, tok = inputs.workload_inputs(w)
-    m = GPT2Model(cfg, params, w.B, w.T, ab.GPT2_BF16)
-    logits, probs = m.new_outputs(w.B, w.T)
-    m.forward(dev(tok), logits, probs)
-    no_device_error()
-    check_properties(cfg, logits, probs)
-    check_sampled(w, ab.GPT2_BF16, logits, probs, params, tok, 64, w.B - 1)
-
-
 @pytest.mark.parametrize("name", ["gpt2-124m-b16", "gpt2-medium-b8"])
-def test_bf16_full_depth_properties(name):
-    # full depth in bf16: the properties that hold at any precision (rows
+def test_bf16_full_width_properties(name):
+    # GPT-2 width in bf16: the properties that hold at any precision (rows
     # sum to 1, padding exactly 0, non-negative, finite)
     w = inputs.WORKLOADS[name]
     params, tok = inputs.workload_inputs(w)
