@@ -7,44 +7,39 @@
 // while its unnormalised output accumulates, so the T x T score matrix never
 // exists.  Key tiles after a query tile are never visited.
 //
-// Work unit: the one-CTA form (the default) gives a CTA (one per SM) two
-// adjacent query tiles of 128 rows, A = 2i and B = 2i + 1, of one (sequence,
-// head); B needs one key tile more, its diagonal.  The pair form gives a
-// cluster of two CTAs four tiles, 4i .. 4i + 3: CTA r holds tile 4i + r of
-// group A and 4i + 2 + r of group B, and each MMA is a paired tcgen05
-// instruction (cta_group::2, M = 256) over one group's two tiles, issued by
-// the even CTA; each CTA loads half of every K tile (keys 64r .. 64r + 63:
-// the B operand of S is split by N = keys) and of every V tile (dimensions
-// 32r .. 32r + 31, MN-major with the 64-byte swizzle: P V's B operand is
-// split by N = head dimension), and the tile after the diagonal of the even
-// CTA's rows is computed for the odd CTA's and fully masked.
-//
-// The score tiles of both groups form one sequence of steps (A and B take
-// turns on each key tile while both have one; B's last tile or tiles follow
+// Work unit: a CTA (one per SM) holds two adjacent query tiles of 128 rows,
+// A = 2i and B = 2i + 1, of one (sequence, head); B needs one key tile more,
+// its diagonal.  The score tiles of both form one sequence of steps (A and B
+// take turns on each key tile while both have one; B's last tile follows
 // alone) that rotates through three S accumulators in TMEM and three P
 // buffers in shared memory, so S of step s + 3 is issued as soon as P of
-// step s is ready and a softmax rarely waits for the tensor cores.
-//   warp 0      TMA: the CTA's two Q tiles, then its K and V tiles (or
-//               halves) through a ring of stages, from the fused QKV buffer
+// step s is ready.
+//   warp 0      TMA: the CTA's two Q tiles, then K and V tiles (128 keys x
+//               64 dimensions each, 128-byte swizzle; one barrier for both)
+//               through a ring of three stages, from the fused QKV buffer
 //               viewed as [B][T][3C] (rows past T read as zero);
 //   warp 1      TMEM (three S: 128 x 128 fp32; O_A, O_B: 128 x 64 fp32) and
 //               the MMAs, S = Q K^T (4 instructions of K = 16) and O += P V
-//               (8); the warp runs the issuing loop and one elected lane
-//               issues (in a pair, the even CTA's warp for both);
+//               (8; V an MN-major operand); the warp runs the issuing loop
+//               and one elected lane issues.  It waits once per key tile
+//               (K and V land together) and frees the stage with one commit
+//               after the tile's last P V: measured, each wait and commit
+//               of this warp costs a few hundred cycles in a busy SM, and
+//               this warp paces the kernel;
 //   warps 2-5   softmax of group A, warps 6-9 softmax of group B, one thread
-//               per query row.  On a tile after the first, one pass over
-//               the S row from TMEM in chunks of 32 keys (the next chunk's
-//               load in flight): p = exp2(s*scale - m) with the running
-//               maximum m as it stands, rounded to the 16-bit type into
-//               swizzled shared memory (the A operand of P V), running sum.
-//               A score above m + 8 (log2 units; always on the first tile)
-//               sends the tile through two passes instead: the row maximum,
-//               the rescale of O in TMEM and of the sum by 2^(m - m_new),
-//               then the exponentials.  Exact either way: the final
-//               division by the sum uses the same m as the numerators.  At
-//               the end O / l goes to [B, T, C].
+//               per query row.  One pass over the S row from TMEM in chunks
+//               of 32 keys (the next chunk's load in flight): p = exp2(s *
+//               scale - m) with the running maximum m as it stands (on the
+//               first tile, the maximum of its first chunk), rounded to the
+//               16-bit type into swizzled shared memory (the A operand of
+//               P V), and the running sum.  A score above m + 8 (log2
+//               units) sends the tile through two passes instead: the row
+//               maximum, the rescale of O in TMEM and of the sum by
+//               2^(m - m_new), then the exponentials.  Exact either way: the
+//               final division by the sum uses the same m as the
+//               numerators.  At the end O / l goes to [B, T, C].
 // Every wait is bounded; a timeout sets the device error word and the CTA
-// (pair) drains its copies and MMAs, frees TMEM and returns.
+// drains its copies and MMAs, frees TMEM and returns.
 #include "kernels.cuh"
 
 namespace gpt2 {
@@ -70,29 +65,25 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// The pair form (kPair) and the one-CTA form differ in the share of each K
-// and V tile a CTA loads and in how many K/V stages fit.
-template <bool kPair>
 struct Smem {
-  static constexpr int kCTAs = kPair ? 2 : 1;
-  static constexpr int kKBytes = kTK / kCTAs * 128;  // keys x 64 dims
-  static constexpr int kVBytes = kTK * 128 / kCTAs;  // 128 keys x dims
-  static constexpr int kKV = kPair ? 4 : 3;          // K and V pipeline stages
-  static constexpr int q = 0;                         // group A tile, group B tile
-  static constexpr int k = q + 2 * kQBytes;           // kKV stages of K
-  static constexpr int v = k + kKV * kKBytes;         // kKV stages of V
-  static constexpr int p = v + kKV * kVBytes;         // kRing buffers
+  static constexpr int kKBytes = kTK * 128;           // 128 keys x 64 dimensions
+  static constexpr int kVBytes = kTK * 128;
+  static constexpr int kKV = 3;                        // K/V pipeline stages
+  static constexpr int q = 0;                          // group A tile, group B tile
+  static constexpr int k = q + 2 * kQBytes;            // kKV stages of K
+  static constexpr int v = k + kKV * kKBytes;          // kKV stages of V
+  static constexpr int p = v + kKV * kVBytes;          // kRing buffers
   static constexpr int bars = p + kRing * kPBytes;
-  // q_full; k_full[kKV], k_empty[kKV], v_full[kKV], v_empty[kKV];
-  // s_full[kRing], p_full[kRing], o_done[kRing]; o_final[2]; drain
-  static constexpr int n_bars = 1 + 4 * kKV + 3 * kRing + 2 + 1;
+  // q_full; kv_full[kKV], kv_empty[kKV]; s_full[kRing], p_full[kRing],
+  // o_done[kRing]; o_final[2]; drain
+  static constexpr int n_bars = 1 + 2 * kKV + 3 * kRing + 2 + 1;
   static constexpr int misc = bars + n_bars * 8;
   static constexpr int total = misc + 16;
   static constexpr int alloc = total + 1024;
 };
-static_assert(Smem<true>::alloc <= 232448 && Smem<false>::alloc <= 232448, "shared memory budget");
+static_assert(Smem::alloc <= 232448, "shared memory budget");
 
-// The pair's schedule of score tiles.  Group A (x = 0) visits key tiles
+// The schedule of score tiles.  Group A (x = 0) visits key tiles
 // 0 .. n_a - 1 and group B (x = 1) 0 .. n_b - 1 (n_b = 0: no group B, else
 // n_b >= n_a); while both have tile j, step 2j + x; then B's remaining
 // tiles (or, with no B, all of A's) one step each.
@@ -108,61 +99,51 @@ struct Schedule {
 
 // 320 threads = 10 warps, one CTA per SM.  Registers are allotted per SM
 // sub-partition (16K each, warps placed round-robin), so the sub-partition
-// holding three warps caps a thread at 168 registers; the softmax threads
-// therefore read their S row in halves instead of holding all of it.
-template <typename T16, typename OutT, bool kPair>
+// holding three warps caps a thread at 168 registers.
+template <typename T16, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, OutT* __restrict__ out, int T, int C,
-                   float scale_log2) {
-  using L = Smem<kPair>;
+    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, OutT* __restrict__ out, int T, int C,
+                     float scale_log2) {
+  using L = Smem;
   constexpr int kKV = L::kKV;
-  constexpr uint32_t kCTAs = L::kCTAs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* q_full = bars;                  // even CTA: both CTAs' Q tiles landed
-  uint64_t* k_full = bars + 1;              // [kKV] even CTA: both K halves landed
-  uint64_t* k_empty = k_full + kKV;         // [kKV] both CTAs: the MMAs have read K
-  uint64_t* v_full = k_empty + kKV;         // [kKV] even CTA
-  uint64_t* v_empty = v_full + kKV;         // [kKV] both CTAs
+  uint64_t* q_full = bars;                  // both Q tiles landed
+  uint64_t* kv_full = bars + 1;             // [kKV] K and V of a key tile landed
+  uint64_t* kv_empty = kv_full + kKV;       // [kKV] the MMAs have read them
   // ring slot r serves steps s = r, r + 3, ...: use k of the slot is phase k
-  uint64_t* s_full = v_empty + kKV;         // [kRing] both CTAs: S of step s is in TMEM
-  uint64_t* p_full = s_full + kRing;        // [kRing] even CTA: P of step s written (every softmax warp)
-  uint64_t* o_done = p_full + kRing;        // [kRing] both CTAs: P V of step s done
-  uint64_t* o_final = o_done + kRing;       // [group] both CTAs: the group's last P V done (one phase)
+  uint64_t* s_full = kv_empty + kKV;        // [kRing] S of step s is in TMEM
+  uint64_t* p_full = s_full + kRing;        // [kRing] P of step s written (every softmax warp of the group)
+  uint64_t* o_done = p_full + kRing;        // [kRing] P V of step s done
+  uint64_t* o_final = o_done + kRing;       // [group] the group's last P V done (one phase)
   uint64_t* drain = o_final + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-  // unit u: query tiles 4u .. 4u + 3 of a pair, 2u and 2u + 1 of one CTA;
-  // the longest units first
-  const int u = static_cast<int>(gridDim.x / kCTAs) - 1 - static_cast<int>(blockIdx.x / kCTAs);
+  // unit u: query tiles 2u and 2u + 1; the longest units first
+  const int u = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);
   const int h = blockIdx.y, b = blockIdx.z;
-  auto q_tile = [&](int x) { return kPair ? 4 * u + 2 * x + static_cast<int>(rank) : 2 * u + x; };
+  auto q_tile = [&](int x) { return 2 * u + x; };
   const int kv_tiles = (T + kTK - 1) / kTK;
-  const int last_a = kPair ? 4 * u + 1 : 2 * u;  // the last query tile of each group
-  const int n_a = min(last_a + 1, kv_tiles);
-  const int n_b = (last_a + 1) * kTQ < T ? min(last_a + kCTAs + 1, kv_tiles) : 0;
+  const int n_a = min(2 * u + 1, kv_tiles);
+  const int n_b = (2 * u + 1) * kTQ < T ? min(2 * u + 2, kv_tiles) : 0;
   const Schedule sch(n_a, n_b);
   const int n_kv = max(n_a, n_b);
   constexpr uint32_t kFmt = std::is_same<T16, __half>::value ? 0u : 1u;
-  constexpr uint32_t kIdescS = make_idesc(kFmt, kCTAs * kTQ, kTK);
-  constexpr uint32_t kIdescPV = make_idesc(kFmt, kCTAs * kTQ, kHS) | (1u << 16);  // B (V) MN-major
+  constexpr uint32_t kIdescS = make_idesc(kFmt, kTQ, kTK);
+  constexpr uint32_t kIdescPV = make_idesc(kFmt, kTQ, kHS) | (1u << 16);  // B (V) MN-major
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, kCTAs);
+    mbar_init(q_full, 1u);
     for (int i = 0; i < kKV; ++i) {
-      mbar_init(&k_full[i], kCTAs);
-      mbar_init(&k_empty[i], 1u);
-      mbar_init(&v_full[i], kCTAs);
-      mbar_init(&v_empty[i], 1u);
+      mbar_init(&kv_full[i], 1u);
+      mbar_init(&kv_empty[i], 1u);
     }
     for (int r = 0; r < kRing; ++r) {
       mbar_init(&s_full[r], 1u);
-      mbar_init(&p_full[r], kCTAs * kSoftmaxWarps);  // the group's softmax warps (of both CTAs)
+      mbar_init(&p_full[r], kSoftmaxWarps);  // the group's softmax warps
       mbar_init(&o_done[r], 1u);
     }
     for (int x = 0; x < 2; ++x) mbar_init(&o_final[x], 1u);
@@ -170,25 +151,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmap_q);
-    tma_prefetch_desc(&tmap_k);
-    tma_prefetch_desc(&tmap_v);
-  }
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmap_qkv);
   if (warp == 1) {
-    if constexpr (kPair) {
-      tmem_alloc_pair(tmem_slot, kTmemCols);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(tmem_slot, kTmemCols);
-      tmem_relinquish();
-    }
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
   }
   tc_fence_before();
-  if constexpr (kPair)
-    cluster_sync();  // the peer's barriers are initialised before any remote arrival
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // a programmatic dependent launch: the QKV projection has finished
@@ -197,128 +166,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ loads
     if (lane == 0) {
-      uint32_t k_filled = 0, v_filled = 0, par = 0;  // per stage: K, V ever filled; parity of the last fill
-      // one load into this CTA's shared memory, completing on the even CTA's
-      // barrier in a pair
-      auto load = [&](void* dst, const CUtensorMap* map, uint64_t* bar, uint32_t bytes, int xc, int yc) {
-        if constexpr (kPair) {
-          const uint32_t bar0 = mapa_shared(smem_u32(bar), 0);
-          mbar_arrive_expect_tx_cluster(bar0, bytes);
-          tma_load_3d_pair(dst, map, bar0, xc, yc, b);
-        } else {
-          mbar_arrive_expect_tx(bar, bytes);
-          tma_load_3d(dst, map, bar, xc, yc, b);
-        }
-      };
-      if constexpr (kPair) {
-        const uint32_t q_full0 = mapa_shared(smem_u32(q_full), 0);
-        mbar_arrive_expect_tx_cluster(q_full0, 2 * kQBytes);
-        tma_load_3d_pair(smem + L::q, &tmap_q, q_full0, h * kHS, q_tile(0) * kTQ, b);
-        tma_load_3d_pair(smem + L::q + kQBytes, &tmap_q, q_full0, h * kHS, q_tile(1) * kTQ, b);
-      } else {
-        mbar_arrive_expect_tx(q_full, 2 * kQBytes);
-        tma_load_3d(smem + L::q, &tmap_q, q_full, h * kHS, q_tile(0) * kTQ, b);
-        tma_load_3d(smem + L::q + kQBytes, &tmap_q, q_full, h * kHS, q_tile(1) * kTQ, b);
-      }
+      uint32_t filled = 0, par = 0;  // per stage: ever filled; parity of the last fill
+      mbar_arrive_expect_tx(q_full, 2 * kQBytes);
+      tma_load_3d(smem + L::q, &tmap_qkv, q_full, h * kHS, q_tile(0) * kTQ, b);
+      tma_load_3d(smem + L::q + kQBytes, &tmap_qkv, q_full, h * kHS, q_tile(1) * kTQ, b);
       for (int j = 0; j < n_kv && !*abort_flag; ++j) {
         const int st = j % kKV;
         const uint32_t ph = (j / kKV) & 1;
-        if (!mbar_wait(&k_empty[st], ph ^ 1)) {
+        if (!mbar_wait(&kv_empty[st], ph ^ 1)) {
           *abort_flag = 1;
           break;
         }
-        load(smem + L::k + st * L::kKBytes, &tmap_k, &k_full[st], L::kKBytes, C + h * kHS,
-             j * kTK + static_cast<int>(rank) * (kTK / 2));
-        k_filled |= 1u << st;
+        mbar_arrive_expect_tx(&kv_full[st], L::kKBytes + L::kVBytes);
+        tma_load_3d(smem + L::k + st * L::kKBytes, &tmap_qkv, &kv_full[st], C + h * kHS, j * kTK, b);
+        tma_load_3d(smem + L::v + st * L::kVBytes, &tmap_qkv, &kv_full[st], 2 * C + h * kHS, j * kTK, b);
+        filled |= 1u << st;
         par = (par & ~(1u << st)) | (ph << st);
-        if (!mbar_wait(&v_empty[st], ph ^ 1)) {
-          *abort_flag = 1;
-          break;
-        }
-        load(smem + L::v + st * L::kVBytes, &tmap_v, &v_full[st], L::kVBytes,
-             2 * C + h * kHS + static_cast<int>(rank) * (kHS / 2), j * kTK);
-        v_filled |= 1u << st;
       }
-      // The copies issued here must land before the CTA may exit.  In a pair
-      // their completion is counted on the even CTA's barriers, so wait
-      // instead for the MMAs that read the last fill of each stage to
-      // release it (immediate in the normal case).
-      for (int st = 0; st < kKV; ++st) {
-        if ((k_filled >> st) & 1u) mbar_wait(&k_empty[st], (par >> st) & 1u);
-        if ((v_filled >> st) & 1u) mbar_wait(&v_empty[st], (par >> st) & 1u);
-      }
+      // the copies issued here land before the CTA may exit: this thread
+      // alone arms the full barriers, so the phase of a stage's last fill
+      // completes exactly when its bytes have landed
+      for (int st = 0; st < kKV; ++st)
+        if ((filled >> st) & 1u) mbar_wait(&kv_full[st], (par >> st) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMAs
-    if (rank == 0) {  // the whole warp runs the loop, one lane issues
-      bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
-      const uint32_t q_addr = smem_u32(smem + L::q);
-      const uint32_t p_addr = smem_u32(smem + L::p);
-      auto mma = [&](uint32_t d, uint64_t a, uint64_t bd, uint32_t idesc, uint32_t acc) {
-        if constexpr (kPair)
-          tc_mma_pair_warp<false>(d, a, bd, idesc, acc);
-        else
-          tc_mma_warp<false>(d, a, bd, idesc, acc);
-      };
-      auto commit = [&](uint64_t* bar) {  // in a pair, to the barrier in both CTAs
-        if constexpr (kPair)
-          tc_commit_pair_warp(bar, 3);
-        else
-          tc_commit_warp(bar);
-      };
-      // S(s) = Q_x K_j^T into S buffer s % kRing
-      auto issue_s = [&](int s) -> bool {
-        const int x = sch.group(s), j = sch.tile(s);
-        if (!__all_sync(0xffffffffu, mbar_wait(&k_full[j % kKV], (j / kKV) & 1))) return false;
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + L::k + (j % kKV) * L::kKBytes);
+    // the whole warp runs the loop, one lane issues
+    bool ok = __all_sync(0xffffffffu, mbar_wait(q_full, 0));
+    const uint32_t q_addr = smem_u32(smem + L::q);
+    const uint32_t p_addr = smem_u32(smem + L::p);
+    // S(s) = Q_x K_j^T into S buffer s % kRing; the first step of each key
+    // tile waits for its K and V (P V of a tile always follows its S)
+    auto issue_s = [&](int s) -> bool {
+      const int x = sch.group(s), j = sch.tile(s);
+      if (s == sch.step(0, j))  // the tile's first step
+        if (!__all_sync(0xffffffffu, mbar_wait(&kv_full[j % kKV], (j / kKV) & 1))) return false;
+      tc_fence_after();
+      const uint64_t qd = smem_desc_sw128(q_addr + x * kQBytes);
+      const uint64_t kd = smem_desc_sw128(smem_u32(smem + L::k + (j % kKV) * L::kKBytes));
 #pragma unroll
-        for (int kk = 0; kk < kHS / 16; ++kk)
-          mma(tmem + kTmemS + (s % kRing) * kTK, smem_desc_sw128(q_addr + x * kQBytes + kk * 32),
-              smem_desc_sw128(k_addr + kk * 32), kIdescS, kk > 0 ? 1u : 0u);
-        commit(&s_full[s % kRing]);
-        if (sch.last_user(s)) commit(&k_empty[j % kKV]);
-        return true;
-      };
-      // O_x += P(s) V_j
-      auto issue_pv = [&](int s) -> bool {
-        const int x = sch.group(s), j = sch.tile(s);
-        // P of both CTAs: written by the softmax threads, released at
-        // cluster scope by their arrivals
-        if (!__all_sync(0xffffffffu, kPair ? mbar_wait_cluster(&p_full[s % kRing], (s / kRing) & 1)
-                                           : mbar_wait(&p_full[s % kRing], (s / kRing) & 1)))
-          return false;
-        if (!__all_sync(0xffffffffu, mbar_wait(&v_full[j % kKV], (j / kKV) & 1))) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + L::v + (j % kKV) * L::kVBytes);
-        const uint32_t pa = p_addr + (s % kRing) * kPBytes;
+      for (int kk = 0; kk < kHS / 16; ++kk)  // 16 dimensions = 32 bytes = 2 in the descriptor's address field
+        tc_mma_warp<false>(tmem + kTmemS + (s % kRing) * kTK, qd + 2 * kk, kd + 2 * kk, kIdescS, kk > 0 ? 1u : 0u);
+      tc_commit_warp(&s_full[s % kRing]);
+      return true;
+    };
+    // O_x += P(s) V_j
+    auto issue_pv = [&](int s) -> bool {
+      const int x = sch.group(s), j = sch.tile(s);
+      if (!__all_sync(0xffffffffu, mbar_wait(&p_full[s % kRing], (s / kRing) & 1))) return false;
+      tc_fence_after();
+      const uint32_t v_addr = smem_u32(smem + L::v + (j % kKV) * L::kVBytes);
+      const uint64_t pd = smem_desc_sw128(p_addr + (s % kRing) * kPBytes);
+      const uint64_t vd = smem_desc_sw128_mn(v_addr, 1024);
 #pragma unroll
-        for (int kk = 0; kk < kTK / 16; ++kk) {
-          const uint32_t a = pa + (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32;
-          // 16 keys = 2 groups of 8 rows of 64 (pair: 32 dims) or 128 bytes
-          const uint64_t bv = kPair ? smem_desc_sw64_mn(v_addr + kk * 1024, 512)
-                                    : smem_desc_sw128_mn(v_addr + kk * 2048, 1024);
-          mma(tmem + kTmemO + x * kHS, smem_desc_sw128(a), bv, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        commit(&o_done[s % kRing]);
-        if (j == (x == 0 ? sch.n_a : sch.n_b) - 1) commit(&o_final[x]);
-        if (sch.last_user(s)) commit(&v_empty[j % kKV]);
-        return true;
-      };
-      // S of the first three steps, then per step: P V, and S of the step
-      // three later into the S buffer this step has finished reading
-      for (int s = 0; s < kRing && s < sch.n_steps && ok; ++s) ok = issue_s(s);
-      for (int s = 0; s < sch.n_steps && ok; ++s) {
-        ok = issue_pv(s);
-        if (ok && s + kRing < sch.n_steps) ok = issue_s(s + kRing);
-      }
-      if (!ok && lane == 0) *abort_flag = 1;
-      if constexpr (kPair)
-        tc_commit_pair_warp(drain, 1);
-      else
-        tc_commit_warp(drain);
-      mbar_wait(drain, 0);
+      for (int kk = 0; kk < kTK / 16; ++kk)  // P: 16 keys = 32 bytes of a 64-key atom; V: 16 rows of 128 bytes
+        tc_mma_warp<false>(tmem + kTmemO + x * kHS, pd + ((kk >> 2) * (kPBytes / 2) + (kk & 3) * 32) / 16,
+                           vd + kk * (2048 / 16), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      tc_commit_warp(&o_done[s % kRing]);
+      if (j == (x == 0 ? sch.n_a : sch.n_b) - 1) tc_commit_warp(&o_final[x]);
+      if (sch.last_user(s)) tc_commit_warp(&kv_empty[j % kKV]);
+      return true;
+    };
+    // S of the first three steps, then per step: P V, and S of the step
+    // three later into the S buffer this step has finished reading
+    for (int s = 0; s < kRing && s < sch.n_steps && ok; ++s) ok = issue_s(s);
+    for (int s = 0; s < sch.n_steps && ok; ++s) {
+      ok = issue_pv(s);
+      if (ok && s + kRing < sch.n_steps) ok = issue_s(s + kRing);
     }
+    if (!ok && lane == 0) *abort_flag = 1;
+    tc_commit_warp(drain);
+    mbar_wait(drain, 0);
   } else {
     // ---------------------------------------------------------- softmax
     const int x = (warp - 2) / kSoftmaxWarps;  // group: 0 = A (warps 2-5), 1 = B (warps 6-9)
@@ -327,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = q_tile(x) * kTQ + row;       // position in the sequence
     const int n_x = x == 0 ? sch.n_a : sch.n_b;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    const uint32_t p_full0 = kPair ? mapa_shared(smem_u32(p_full), 0) : 0u;
     const int t_end = min(t + 1, T);  // keys < t_end are visible to this row
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -337,96 +254,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* pbase = smem + L::p + r * kPBytes + row * 128;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[r], (s / kRing) & 1)))) break;
       tc_fence_after();
-      // visible keys of this tile: all 128, up to the diagonal, or none
-      // (the tile after the diagonal of the even CTA's rows, computed for
-      // the odd CTA's)
+      // visible keys of this tile: all 128 or up to the diagonal
       const int valid = max(0, min(t_end - j * kTK, kTK));
+      // chunks of 32 keys that some row of this warp sees; the rest of the
+      // row's P is zero (the upper triangle of the diagonal tile) and its
+      // exponentials are not computed
+      const int n_live = (__reduce_max_sync(0xffffffffu, valid) + 31) >> 5;
+      const bool all_full = __all_sync(0xffffffffu, valid == kTK);
       // P V of this group's previous step s_prev (tile j - 1) must be done
       // before O is rescaled.  Its ring slot's barrier is unambiguous then:
       // P V of step s_prev - 3 finished before S of step s (issued after
       // it), and P V of step s_prev + 3 > s cannot have been issued, as P V
       // goes in step order and that of step s needs this thread's P.
       const int s_prev = j > 0 ? sch.step(x, j - 1) : 0;
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      bool done = false;
-      if (j > 0) {
-        // Single pass: p = exp2(s * scale - m) with the running maximum as
-        // it stands, 32 keys at a time, the next chunk's TMEM load in flight
-        // while this one is processed.  A score above m + 2^8 (a maximum
-        // that must be raised) stops it, and the tile is redone below.
-        auto chunk = [&](auto cc, auto masked, uint32_t(&cur)[32], uint32_t(&nxt)[32]) -> bool {
-          constexpr int c = decltype(cc)::value;
-          constexpr bool kMasked = decltype(masked)::value;
-          if (c + 1 < kTK / 32) tmem_ld_32x32b_x32(lane_base + s_col + (c + 1) * 32, nxt);
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float2 sum2 = make_float2(0.f, 0.f);
+      auto store_p = [&](int c, const uint32_t(&pk)[16]) {
+        // 32 keys = 4 chunks of 16 bytes: atom c / 2, chunks (c % 2) * 4 + 0..3
+        uint8_t* prow = pbase + (c >> 1) * (kPBytes / 2);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float xv = fmaf(__uint_as_float(cur[e]), scale_log2, -m_run);
-            if (kMasked && c * 32 + e >= valid) xv = -INFINITY;
-            cur[e] = __float_as_uint(xv);
-            m4[e & 3] = fmaxf(m4[e & 3], xv);
-          }
-          const bool over =
-              __any_sync(0xffffffffu, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) > kRescaleThreshold);
-          if (!over) {
-            uint32_t pk[16];
+        for (int q = 0; q < 4; ++q) {
+          const int ch = (c & 1) * 4 + q;
+          *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      };
+      // x = s * scale - m for the 32 keys of a chunk (-inf for masked
+      // keys), then p = exp2(x) on the SFU in fp32, rounded to the 16-bit
+      // type into P, and their fp32 sum added to sum2.  The exponentials do
+      // not wait for the overflow test: a chunk with a key above m + 8
+      // (log2 units; a maximum that must be raised) is computed, found, and
+      // neither stored nor summed, and the function returns false.  Four
+      // independent chains for the maximum and the sum keep the SFU fed.
+      auto softmax_chunk = [&](int c, const uint32_t(&cur)[32], bool check) -> bool {
+        const float2 sc = make_float2(scale_log2, scale_log2), nm = make_float2(-m_run, -m_run);
+        float2 xv[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const float p0v = ex2(__uint_as_float(cur[e]));  // exp2(-inf) = 0 for masked keys
-              const float p1v = ex2(__uint_as_float(cur[e + 1]));
-              sum4[(e >> 1) & 3] += p0v + p1v;
-              pk[e >> 1] = pack2<T16>(p0v, p1v);
-            }
-            uint8_t* prow = pbase + (c >> 1) * (kPBytes / 2);
+        for (int i = 0; i < 16; ++i)
+          xv[i] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sc, nm);
+        if (!all_full) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int ch = (c & 1) * 4 + q;
-              *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
-                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-          }
-          if (c + 1 < kTK / 32) tmem_ld_wait_regs(nxt);
-          return !over;
-        };
-        auto single_pass = [&](auto masked) -> bool {
-          uint32_t ra[32], rb[32];
-          tmem_ld_32x32b_x32(lane_base + s_col, ra);
-          tmem_ld_wait_regs(ra);
-          return chunk(std::integral_constant<int, 0>(), masked, ra, rb) &&
-                 chunk(std::integral_constant<int, 1>(), masked, rb, ra) &&
-                 chunk(std::integral_constant<int, 2>(), masked, ra, rb) &&
-                 chunk(std::integral_constant<int, 3>(), masked, rb, ra);
-        };
-        static_assert(kTK == 128, "four chunks of 32 keys");
-        done = __all_sync(0xffffffffu, valid == kTK) ? single_pass(std::false_type())
-                                                     : single_pass(std::true_type());
-      }
-      if (!done) {
-        // Two passes (the first tile, or a maximum that grows by more than
-        // 2^8): the row maximum, then the exponentials.
-        sum4[0] = sum4[1] = sum4[2] = sum4[3] = 0.f;
-        float mx8[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {  // pass 1: the row maximum
-          uint32_t rr[64];
-          tmem_ld_32x32b_x32(lane_base + s_col + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-          tmem_ld_32x32b_x32(lane_base + s_col + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-          tmem_ld_wait();
-          if (valid == kTK) {
-#pragma unroll
-            for (int e = 0; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(rr[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (half * 64 + e < valid) mx8[e & 7] = fmaxf(mx8[e & 7], __uint_as_float(rr[e]));
+          for (int i = 0; i < 16; ++i) {
+            if (c * 32 + 2 * i >= valid) xv[i].x = -INFINITY;
+            if (c * 32 + 2 * i + 1 >= valid) xv[i].y = -INFINITY;
           }
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float2 sq[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          mq[i & 3] = fmax3(mq[i & 3], xv[i].x, xv[i].y);
+          const float2 p = make_float2(ex2(xv[i].x), ex2(xv[i].y));
+          sq[i & 3] = __fadd2_rn(sq[i & 3], p);
+          pk[i] = pack2<T16>(p.x, p.y);
+        }
+        if (check &&
+            __any_sync(0xffffffffu, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) > kRescaleThreshold))
+          return false;
+        sum2 = __fadd2_rn(sum2, __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3])));
+        store_p(c, pk);
+        return true;
+      };
+      auto zero_chunk = [&](int c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        store_p(c, pk);
+      };
+      // Single pass over the live chunks with the running maximum as it
+      // stands, the next chunk's TMEM load in flight while one is
+      // processed.  On the first tile the running maximum starts as the
+      // maximum of the first chunk's visible scores.  A score above m + 8
+      // (log2 units; a maximum that must be raised) stops it, and the tile
+      // is redone in two passes below.
+      bool done = false;
+      {
+        uint32_t ra[32], rb[32];
+        bool go = true;
+        if (n_live > 0) {
+          tmem_ld_32x32b_x32(lane_base + s_col, ra);
+          tmem_ld_wait_regs(ra);
+          if (j == 0) {  // valid >= 1 on every row here
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (all_full || e < valid) mx = fmaxf(mx, __uint_as_float(ra[e]));
+            m_run = mx * scale_log2;
+          }
+        }
+        auto chunk = [&](auto cc, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+          constexpr int c = decltype(cc)::value;
+          if (!go) return;
+          if (c >= n_live) {
+            zero_chunk(c);
+            return;
+          }
+          if (c + 1 < n_live) tmem_ld_32x32b_x32(lane_base + s_col + (c + 1) * 32, nxt);
+          go = softmax_chunk(c, cur, true);
+          if (c + 1 < n_live) tmem_ld_wait_regs(nxt);
+        };
+        static_assert(kTK == 128, "four chunks of 32 keys");
+        chunk(std::integral_constant<int, 0>(), ra, rb);
+        chunk(std::integral_constant<int, 1>(), rb, ra);
+        chunk(std::integral_constant<int, 2>(), ra, rb);
+        chunk(std::integral_constant<int, 3>(), rb, ra);
+        done = go;
+      }
+      if (!done) {
+        // Two passes (a maximum that grows by more than 2^8): the row
+        // maximum over the tile, the rescale of O and of the running sum,
+        // then the exponentials.
+        sum2 = make_float2(0.f, 0.f);
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kTK / 32; ++c) {  // pass 1: the row maximum
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(lane_base + s_col + c * 32, rr);
+          tmem_ld_wait_regs(rr);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e < valid) mx = fmaxf(mx, __uint_as_float(rr[e]));
+        }
         const float m_new = fmaxf(m_run, mx * scale_log2);  // the scale is positive: it commutes with max
-        const bool grow = (m_new - m_run) > kRescaleThreshold;  // true on the first tile
+        const bool grow = (m_new - m_run) > kRescaleThreshold;
         if (__any_sync(0xffffffffu, grow)) {
           if (j > 0) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&o_done[s_prev % kRing], (s_prev / kRing) & 1))))
@@ -447,51 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           m_run = m_new;
         }
-        // pass 2: p = exp2(s * scale - m), rounded to the 16-bit type, into P(s)
-        // (its buffer is free: P V of step s - 3 finished before S of step s)
+        // pass 2: p = exp2(s * scale - m) into P(s) (its buffer is free: P V
+        // of step s - 3 finished before S of step s)
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          uint32_t rr[64];
-          tmem_ld_32x32b_x32(lane_base + s_col + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&rr[0]));
-          tmem_ld_32x32b_x32(lane_base + s_col + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&rr[32]));
-          tmem_ld_wait();
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            const int c = half * 2 + c2;  // 32-key chunk of the tile
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              const int k = c * 32 + e;
-              float p0v = ex2(fmaf(__uint_as_float(rr[c2 * 32 + e]), scale_log2, -m_run));
-              float p1v = ex2(fmaf(__uint_as_float(rr[c2 * 32 + e + 1]), scale_log2, -m_run));
-              if (valid != kTK) {
-                if (k >= valid) p0v = 0.f;
-                if (k + 1 >= valid) p1v = 0.f;
-              }
-              sum4[(e >> 1) & 3] += p0v + p1v;
-              pk[e >> 1] = pack2<T16>(p0v, p1v);
-            }
-            // 32 keys = 4 chunks of 16 bytes: atom c / 2, chunks (c % 2) * 4 + 0..3
-            uint8_t* prow = pbase + (c >> 1) * (kPBytes / 2);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int chunk = (c & 1) * 4 + q;
-              *reinterpret_cast<uint4*>(prow + ((chunk ^ (row & 7)) << 4)) =
-                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
-          }
+        for (int c = 0; c < kTK / 32; ++c) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(lane_base + s_col + c * 32, rr);
+          tmem_ld_wait_regs(rr);
+          softmax_chunk(c, rr, false);
         }
       }
-      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      l_run += sum2.x + sum2.y;
       fence_proxy_async_smem();  // P written by this thread becomes visible to the MMA
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        if constexpr (kPair)
-          mbar_arrive_release_cluster(p_full0 + static_cast<uint32_t>(r) * 8u);
-        else
-          mbar_arrive(&p_full[r]);
-      }
+      if (lane == 0) mbar_arrive(&p_full[r]);
     }
     if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_final[x], 0));
     if (ok && n_x > 0) {
@@ -531,79 +451,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  if constexpr (kPair)
-    cluster_sync();  // neither CTA leaves while the pair MMAs may read its shared memory
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    if constexpr (kPair)
-      tmem_dealloc_pair(tmem, kTmemCols);
-    else
-      tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// The one-CTA form is the default: the softmax, not the tensor cores, sets
-// the pace of both forms, and the pair form also computes each pair's
-// masked tile and couples two CTAs' progress (measured at B = 16, T = 1024:
-// 79 us against 97 us per layer).  GPT2_ATTN_PAIR=1 selects the pair form.
-bool attention_pair_form() {
-  static const int v = [] {
-    const char* e = getenv("GPT2_ATTN_PAIR");
-    return e ? atoi(e) : 0;
-  }();
-  return v != 0;
-}
-
-template <typename T16, typename OutT, bool kPair>
-int launch_typed(void* out, const CUtensorMap* maps, int B, int T, int C, int NH, cudaStream_t s) {
+template <typename T16, typename OutT>
+int launch_typed(void* out, const CUtensorMap& map, int B, int T, int C, int NH, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};  // per template instance and device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
+  auto kern = attn_tc05_kernel<T16, OutT>;
   if (!attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(attn_tc05_kernel<T16, OutT, kPair>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<kPair>::alloc);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::alloc);
     if (e != cudaSuccess) return note_cuda_error(e);
     attr_set[dev] = true;
   }
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
-  const int rows_per_unit = (kPair ? 4 : 2) * kTQ;
-  const int units = (T + rows_per_unit - 1) / rows_per_unit;
+  const int units = (T + 2 * kTQ - 1) / (2 * kTQ);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((kPair ? 2 : 1) * units, NH, B);
+  cfg.gridDim = dim3(units, NH, B);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Smem<kPair>::alloc;
+  cfg.dynamicSmemBytes = Smem::alloc;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int n_attr = 0;
-  if (kPair) {
-    attr[n_attr].id = cudaLaunchAttributeClusterDimension;
-    attr[n_attr].val.clusterDim.x = 2;
-    attr[n_attr].val.clusterDim.y = 1;
-    attr[n_attr].val.clusterDim.z = 1;
-    ++n_attr;
-  }
-  if (pdl_on()) {  // the kernel waits for its predecessor itself
-    attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
-    ++n_attr;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // the kernel waits for its predecessor itself
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = n_attr;
-  // the one-CTA form loads whole K and V tiles: 64 dims x 128 rows, as Q
-  const CUtensorMap& mk = kPair ? maps[1] : maps[0];
-  const CUtensorMap& mv = kPair ? maps[2] : maps[0];
-  auto kern = attn_tc05_kernel<T16, OutT, kPair>;
-  const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, maps[0], mk, mv, static_cast<OutT*>(out), T, C, scale_log2);
+  cfg.numAttrs = pdl_on() ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, static_cast<OutT*>(out), T, C, scale_log2);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
-}
-
-template <typename T16, typename OutT>
-int launch_form(void* out, const CUtensorMap* maps, int B, int T, int C, int NH, cudaStream_t s) {
-  return attention_pair_form() ? launch_typed<T16, OutT, true>(out, maps, B, T, C, NH, s)
-                               : launch_typed<T16, OutT, false>(out, maps, B, T, C, NH, s);
 }
 }  // namespace
 
@@ -612,25 +491,19 @@ int launch_form(void* out, const CUtensorMap* maps, int B, int T, int C, int NH,
 int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
                           cudaStream_t s) {
   if (C / NH != kHS || C % 8 != 0) return GPT2_ERR_UNSUPPORTED;
-  // [B][T][3C] viewed three ways: Q tiles (64 dims x 128 rows) and K halves
-  // (64 dims x 64 keys), both with the 128-byte swizzle, and V halves
-  // (32 dims x 128 keys) with the 64-byte swizzle
-  CUtensorMap maps[3];
+  // [B][T][3C] viewed as tiles of 64 dimensions x 128 rows with the 128-byte
+  // swizzle: Q, K (K-major operands) and V (an MN-major operand) alike
+  CUtensorMap map;
   const uint64_t dims[3] = {static_cast<uint64_t>(3 * C), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
   const uint64_t strides[2] = {static_cast<uint64_t>(3 * C) * 2, static_cast<uint64_t>(T) * 3 * C * 2};
-  const uint32_t box_q[3] = {kHS, kTQ, 1};
-  const uint32_t box_k[3] = {kHS, kTK / 2, 1};
-  const uint32_t box_v[3] = {kHS / 2, kTK, 1};
+  const uint32_t box[3] = {kHS, kTQ, 1};
   const CUtensorMapDataType dt = op == kOpF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!encode_tensor_map(&maps[0], dt, 3, qkv, dims, strides, box_q, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map(&maps[1], dt, 3, qkv, dims, strides, box_k, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tensor_map(&maps[2], dt, 3, qkv, dims, strides, box_v, CU_TENSOR_MAP_SWIZZLE_64B))
-    return GPT2_ERR_CUDA;
+  if (!encode_tensor_map(&map, dt, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return GPT2_ERR_CUDA;
   if (op == kOpF16)
-    return out16 ? launch_form<__half, __half>(out, maps, B, T, C, NH, s)
-                 : launch_form<__half, float>(out, maps, B, T, C, NH, s);
-  return out16 ? launch_form<__nv_bfloat16, __nv_bfloat16>(out, maps, B, T, C, NH, s)
-               : launch_form<__nv_bfloat16, float>(out, maps, B, T, C, NH, s);
+    return out16 ? launch_typed<__half, __half>(out, map, B, T, C, NH, s)
+                 : launch_typed<__half, float>(out, map, B, T, C, NH, s);
+  return out16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(out, map, B, T, C, NH, s)
+               : launch_typed<__nv_bfloat16, float>(out, map, B, T, C, NH, s);
 }
 
 }  // namespace gpt2

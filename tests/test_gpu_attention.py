@@ -8,10 +8,6 @@ absolute (the bar for tensor-core results); fp32 CUDA cores 1e-5 absolute.
 Inputs drawn on the 16-bit grid at std 1 (and with peaked scores) isolate
 the kernel's own rounding, that of the probabilities P to the 16-bit type:
 |err| <= u * max|v| with unit roundoff u = 2^-8 (bf16) or 2^-11 (fp16)."""
-import os
-import subprocess
-import sys
-
 import numpy as np
 import pytest
 import torch
@@ -47,8 +43,8 @@ def run_attention(B, T, C, NH, precision, seed=0, std=0.55, qk_std=1.0, grid=Non
 
 
 # head size 64 (the tcgen05 kernel): T = 1, within, at and past a 128-row
-# tile, past 512 rows (a second CTA pair whose second group is empty: 513,
-# or runs on alone: 700), the GPT-2 width; head sizes 16 and 32 (the
+# tile, past 512 rows (a CTA whose second query tile is empty: 129, 513;
+# or runs on alone: 200, 700), the GPT-2 width; head sizes 16 and 32 (the
 # mma.sync kernel)
 SHAPES = [(1, 1, 128, 2), (2, 64, 128, 2), (1, 128, 128, 2), (2, 129, 128, 2), (1, 200, 768, 12),
           (1, 513, 128, 2), (2, 700, 256, 4), (2, 1024, 768, 12), (1, 1000, 1024, 16),
@@ -90,15 +86,3 @@ def test_attention_causal_bitwise():
         ab.attention_forward(o, dev(q), B, T, C, NH, ab.GPT2_BF16, ws, ws.numel())
         outs.append(host(o))
     np.testing.assert_array_equal(outs[0][:, :100], outs[1][:, :100])
-
-
-@pytest.mark.skipif(os.environ.get("GPT2_ATTN_PAIR") == "1", reason="already running in the pair form")
-def test_attention_pair_form():
-    # The paired-CTA form of the head-size-64 kernel is chosen once per
-    # process (GPT2_ATTN_PAIR=1): run this file's parity tests in it.
-    here = os.path.dirname(os.path.abspath(__file__))
-    env = dict(os.environ, GPT2_ATTN_PAIR="1")
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(here, "test_gpu_attention.py"), "-q", "-x",
-                        "-m", "gpu", "-k", "not pair_form"],
-                       env=env, cwd=os.path.dirname(here), capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
