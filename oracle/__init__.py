@@ -133,6 +133,28 @@ def attention_online(qkv, NH: int, Br: int, Bc: int) -> np.ndarray:
     return out
 
 
+def attention_backward(qkv, dout, NH: int) -> np.ndarray:
+    """Backward of Algorithm 0 causal attention: dqkv [B, T, 3C] (dQ, dK,
+    dV in the Q, K, V column blocks) for dL/dO = dout [B, T, C]."""
+    qkv, dout = _f64(qkv), _f64(dout)
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    dqkv = np.empty_like(qkv)
+    lib().oracle_attention_backward(_p(dqkv), _p(dout), _p(qkv), B, T, C, NH)
+    return dqkv
+
+
+def attention_backward_online(qkv, dout, out, NH: int, Br: int, Bc: int) -> np.ndarray:
+    """The tiled (Algorithm 1) backward, recomputing the attention matrix
+    block by block from row statistics; out = the forward's output."""
+    qkv, dout, out = _f64(qkv), _f64(dout), _f64(out)
+    B, T, C3 = qkv.shape
+    C = C3 // 3
+    dqkv = np.empty_like(qkv)
+    lib().oracle_attention_backward_online(_p(dqkv), _p(dout), _p(qkv), _p(out), B, T, C, NH, Br, Bc)
+    return dqkv
+
+
 def gelu(x) -> np.ndarray:
     x = _f64(x)
     out = np.empty_like(x)

@@ -19,6 +19,9 @@
  *     Splitting and Tensor Shapes"); scale 1/sqrt(head size);
  *   - an independent Algorithm 1 recompute (tiled, online softmax), used
  *     only to cross-check Algorithm 0 (FlashAttention (I), Task 2);
+ *   - the backward algorithms of Algorithms 0 and 1 for causal attention
+ *     (FlashAttention (II): the chain rule through the softmax, and its
+ *     tiled form recomputing the attention matrix from row statistics);
  *   - tanh-form GELU, the residual add, the vocabulary softmax;
  *   - the KV-cached decode step (NanoGPT project, "KV Caching").
  * All arithmetic is in double; parameters arrive as the caller's fp32 buffer
@@ -224,6 +227,192 @@ void oracle_attention_online(double* out, const double* qkv, int B, int T, int C
             out[((size_t)b * T + i0 + r) * C + h * hs + d] = O[(size_t)r * hs + d];
       }
   free(S); free(m); free(l); free(O);
+}
+
+/* ------------------------------------------------------ attention backward */
+/* The backward pass of causal attention (FlashAttention (II): the backward
+ * algorithm of Algorithm 0).  Given dout = dL/dO [B,T,C], per (b, h), with
+ * S = Q K^T * scale (masked), P = softmax_rows(S), O = P V:
+ *   dV = P^T dO,  dP = dO V^T,
+ *   dS[t][j] = P[t][j] (dP[t][j] - sum_k P[t][k] dP[t][k])   (the softmax
+ *              Jacobian applied to row t),
+ *   dQ = dS K * scale,  dK = dS^T Q * scale.
+ * dqkv [B,T,3C] holds dQ, dK, dV in the column blocks of Q, K, V. */
+void oracle_attention_backward(double* dqkv, const double* dout, const double* qkv, int B, int T, int C, int NH) {
+  const int hs = C / NH;
+  const double scale = 1.0 / sqrt((double)hs);
+  memset(dqkv, 0, sizeof(double) * (size_t)B * T * 3 * C);
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int b = 0; b < B; b++)
+    for (int h = 0; h < NH; h++) {
+      double* P = (double*)malloc(sizeof(double) * (size_t)T * T);
+      double* dP = (double*)malloc(sizeof(double) * (size_t)T * T);
+      const double* base = qkv + (size_t)b * T * 3 * C;
+      double* dbase = dqkv + (size_t)b * T * 3 * C;
+      /* P: the forward's probabilities, as in oracle_attention */
+      for (int t = 0; t < T; t++) {
+        const double* q = base + (size_t)t * 3 * C + h * hs;
+        double mx = -INFINITY;
+        for (int j = 0; j <= t; j++) {
+          const double* k = base + (size_t)j * 3 * C + C + h * hs;
+          double dot = 0.0;
+          for (int d = 0; d < hs; d++) dot += q[d] * k[d];
+          P[(size_t)t * T + j] = dot * scale;
+          if (P[(size_t)t * T + j] > mx) mx = P[(size_t)t * T + j];
+        }
+        double sum = 0.0;
+        for (int j = 0; j <= t; j++) {
+          P[(size_t)t * T + j] = exp(P[(size_t)t * T + j] - mx);
+          sum += P[(size_t)t * T + j];
+        }
+        for (int j = 0; j <= t; j++) P[(size_t)t * T + j] /= sum;
+        for (int j = t + 1; j < T; j++) P[(size_t)t * T + j] = 0.0;
+      }
+      /* dP = dO V^T (only j <= t matters) and dV = P^T dO */
+      for (int t = 0; t < T; t++) {
+        const double* go = dout + ((size_t)b * T + t) * C + h * hs;
+        for (int j = 0; j <= t; j++) {
+          const double* v = base + (size_t)j * 3 * C + 2 * C + h * hs;
+          double dot = 0.0;
+          for (int d = 0; d < hs; d++) dot += go[d] * v[d];
+          dP[(size_t)t * T + j] = dot;
+        }
+      }
+      for (int j = 0; j < T; j++) {
+        double* dv = dbase + (size_t)j * 3 * C + 2 * C + h * hs;
+        for (int d = 0; d < hs; d++) {
+          double acc = 0.0;
+          for (int t = j; t < T; t++) acc += P[(size_t)t * T + j] * dout[((size_t)b * T + t) * C + h * hs + d];
+          dv[d] = acc;
+        }
+      }
+      /* dS, written over dP */
+      for (int t = 0; t < T; t++) {
+        double rowdot = 0.0;
+        for (int k = 0; k <= t; k++) rowdot += P[(size_t)t * T + k] * dP[(size_t)t * T + k];
+        for (int j = 0; j <= t; j++) dP[(size_t)t * T + j] = P[(size_t)t * T + j] * (dP[(size_t)t * T + j] - rowdot);
+      }
+      /* dQ = dS K * scale, dK = dS^T Q * scale */
+      for (int t = 0; t < T; t++) {
+        double* dq = dbase + (size_t)t * 3 * C + h * hs;
+        for (int d = 0; d < hs; d++) {
+          double acc = 0.0;
+          for (int j = 0; j <= t; j++) acc += dP[(size_t)t * T + j] * base[(size_t)j * 3 * C + C + h * hs + d];
+          dq[d] = acc * scale;
+        }
+      }
+      for (int j = 0; j < T; j++) {
+        double* dk = dbase + (size_t)j * 3 * C + C + h * hs;
+        for (int d = 0; d < hs; d++) {
+          double acc = 0.0;
+          for (int t = j; t < T; t++) acc += dP[(size_t)t * T + j] * base[(size_t)t * 3 * C + h * hs + d];
+          dk[d] = acc * scale;
+        }
+      }
+      free(P);
+      free(dP);
+    }
+}
+
+/* The backward algorithm of Algorithm 1 (FlashAttention (II)): tiled, with
+ * the attention matrix recomputed block by block instead of stored.  The
+ * forward leaves per row the statistic L = m + log(l) (its running maximum
+ * and sum; P = exp(S - L)), computed here by a first tiled sweep, and
+ * D[t] = sum_d dO[t][d] O[t][d] (which equals sum_k P[t][k] dP[t][k]).  Then
+ * for each key block j and each query block i that sees it:
+ *   P = exp(S_ij - L_i), dV_j += P^T dO_i, dP = dO_i V_j^T,
+ *   dS = P (dP - D_i), dQ_i += dS K_j * scale, dK_j += dS^T Q_i * scale.
+ * `out` is the forward output O [B,T,C]. */
+void oracle_attention_backward_online(double* dqkv, const double* dout, const double* qkv, const double* out,
+                                      int B, int T, int C, int NH, int Br, int Bc) {
+  const int hs = C / NH;
+  const double scale = 1.0 / sqrt((double)hs);
+  memset(dqkv, 0, sizeof(double) * (size_t)B * T * 3 * C);
+  double* L = (double*)malloc(sizeof(double) * T);
+  double* D = (double*)malloc(sizeof(double) * T);
+  double* Pt = (double*)malloc(sizeof(double) * (size_t)Br * Bc);
+  for (int b = 0; b < B; b++)
+    for (int h = 0; h < NH; h++) {
+      const double* base = qkv + (size_t)b * T * 3 * C;
+      double* dbase = dqkv + (size_t)b * T * 3 * C;
+      /* the forward's row statistics, block by block (online max and sum) */
+      for (int t = 0; t < T; t++) {
+        const double* q = base + (size_t)t * 3 * C + h * hs;
+        double m = -INFINITY, l = 0.0;
+        for (int j0 = 0; j0 <= t; j0 += Bc) {
+          double mt = -INFINITY;
+          const int je = (j0 + Bc - 1 < t) ? j0 + Bc - 1 : t;
+          for (int j = j0; j <= je; j++) {
+            const double* k = base + (size_t)j * 3 * C + C + h * hs;
+            double dot = 0.0;
+            for (int d = 0; d < hs; d++) dot += q[d] * k[d];
+            if (dot * scale > mt) mt = dot * scale;
+          }
+          const double m_new = m > mt ? m : mt;
+          double lt = 0.0;
+          for (int j = j0; j <= je; j++) {
+            const double* k = base + (size_t)j * 3 * C + C + h * hs;
+            double dot = 0.0;
+            for (int d = 0; d < hs; d++) dot += q[d] * k[d];
+            lt += exp(dot * scale - m_new);
+          }
+          l = l * exp(m - m_new) + lt;
+          m = m_new;
+        }
+        L[t] = m + log(l);
+        double dd = 0.0;
+        for (int d = 0; d < hs; d++)
+          dd += dout[((size_t)b * T + t) * C + h * hs + d] * out[((size_t)b * T + t) * C + h * hs + d];
+        D[t] = dd;
+      }
+      for (int j0 = 0; j0 < T; j0 += Bc) {
+        const int bc = (T - j0 < Bc) ? T - j0 : Bc;
+        for (int i0 = (j0 / Br) * Br; i0 < T; i0 += Br) {  /* query blocks that can see key block j0 */
+          const int br = (T - i0 < Br) ? T - i0 : Br;
+          for (int r = 0; r < br; r++) {
+            const int t = i0 + r;
+            const double* q = base + (size_t)t * 3 * C + h * hs;
+            for (int c = 0; c < bc; c++) {
+              const int j = j0 + c;
+              double p = 0.0;
+              if (j <= t) {
+                const double* k = base + (size_t)j * 3 * C + C + h * hs;
+                double dot = 0.0;
+                for (int d = 0; d < hs; d++) dot += q[d] * k[d];
+                p = exp(dot * scale - L[t]);
+              }
+              Pt[(size_t)r * Bc + c] = p;
+            }
+          }
+          for (int r = 0; r < br; r++) {
+            const int t = i0 + r;
+            const double* go = dout + ((size_t)b * T + t) * C + h * hs;
+            for (int c = 0; c < bc; c++) {
+              const int j = j0 + c;
+              const double p = Pt[(size_t)r * Bc + c];
+              if (p == 0.0) continue;
+              const double* v = base + (size_t)j * 3 * C + 2 * C + h * hs;
+              double dp = 0.0;
+              for (int d = 0; d < hs; d++) dp += go[d] * v[d];
+              const double ds = p * (dp - D[t]);
+              double* dq = dbase + (size_t)t * 3 * C + h * hs;
+              double* dk = dbase + (size_t)j * 3 * C + C + h * hs;
+              double* dv = dbase + (size_t)j * 3 * C + 2 * C + h * hs;
+              const double* k = base + (size_t)j * 3 * C + C + h * hs;
+              const double* q = base + (size_t)t * 3 * C + h * hs;
+              for (int d = 0; d < hs; d++) {
+                dv[d] += p * go[d];
+                dq[d] += ds * k[d] * scale;
+                dk[d] += ds * q[d] * scale;
+              }
+            }
+          }
+        }
+      }
+    }
+  free(L);
+  free(D);
+  free(Pt);
 }
 
 /* ------------------------------------------------------------ elementwise */
