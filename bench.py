@@ -23,6 +23,7 @@ per step; rank 0 alone runs it.
 prefill of 32 prompts of 512 tokens (reported apart), then 128 greedy steps
 (argmax + gpt2_decode_step), K runs timed; value = decoded tokens/s.
 --gemm-diag adds each GEMM site's time beside cuBLAS at the same shape.
+--attention-backward times one layer's attention backward (fp32) instead.
 """
 from __future__ import annotations
 
@@ -390,6 +391,58 @@ def run_decode(args, w, precision):
         pg.destroy_process_group()
 
 
+ATTN_BWD_METRIC = "GPT-2 124M causal attention backward, one layer (B=16,T=1024,12 heads of 64), fp32, ms"
+
+
+def attention_backward_flops(B, T, C, NH):
+    """Algorithmic FLOPs of one attention backward: the four gradient
+    products dV = P^T dO, dP = dO V^T, dQ = dS K, dK = dS^T Q over the causal
+    (t, j) pairs, 2 hs FLOPs each (the recomputation of S is not counted)."""
+    hs = C // NH
+    return B * NH * (T * (T + 1) // 2) * 4 * 2 * hs
+
+
+def run_attention_backward(args, w):
+    """One layer's attention backward (fp32 CUDA cores) at the workload's
+    shape: K timed calls after W warm-up calls, CUDA events on the stream."""
+    import torch
+    from gpt_transformer_forward_gb300 import binding as ab
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    cfg, B, T = w.cfg, w.B, w.T
+    C, NH = cfg.channels, cfg.num_heads
+    qkv = torch.from_numpy(inputs.make_normal(801 + rank, (B, T, 3 * C), 0.55).astype("float32")).cuda()
+    dout = torch.from_numpy(inputs.make_normal(802 + rank, (B, T, C), 1.0).astype("float32")).cuda()
+    out = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
+    ab.attention_forward(out, qkv, B, T, C, NH, ab.GPT2_FP32, None, 0)
+    dqkv = torch.empty((B, T, 3 * C), dtype=torch.float32, device="cuda")
+    wsz = ab.attention_backward_workspace_size(B, T, C, NH)
+    ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, ws, wsz)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, ws, wsz)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+    flops = attention_backward_flops(B, T, C, NH)
+    line = {"metric": ATTN_BWD_METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name + "-attention-backward", "B": B, "T": T, "C": C, "heads": NH},
+            "tflops": flops / (ms * 1e-3) / 1e12, "algorithmic_flops": flops,
+            "gpu_launches": 3 * args.steps, "device_error_word": ab.gpt2_get_error()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     from gpt_transformer_forward_gb300 import binding as ab
@@ -397,6 +450,8 @@ def run_ours(args):
 
     w = inputs.WORKLOADS[args.workload]
     precision = ab.PRECISIONS[args.precision]
+    if args.attention_backward:
+        return run_attention_backward(args, w)
     if w.decode_steps:
         return run_decode(args, w, precision)
     rank, world, local, pg = dist_setup(args.gpus)
@@ -545,6 +600,8 @@ def main():
     ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--precision", default="fp16", choices=["fp16", "bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attention-backward", action="store_true",
+                    help="time one layer's attention backward (fp32) at the workload's shape instead")
     ap.add_argument("--gemm-diag", action="store_true",
                     help="add each GEMM site's time beside cuBLAS at the same shape (diagnostic)")
     args = ap.parse_args()

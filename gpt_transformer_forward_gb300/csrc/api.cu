@@ -364,6 +364,28 @@ int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH,
   return check_launch();
 }
 
+size_t attention_backward_workspace_size(int B, int T, int C, int NH) {
+  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0) return 0;
+  return 2 * round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256);
+}
+
+int attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, int B, int T, int C, int NH,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  RETURN_IF(!dqkv || !dout || !qkv || !out, GPT2_ERR_ARG);
+  RETURN_IF(B < 0 || T < 0 || C <= 0 || NH <= 0, GPT2_ERR_ARG);
+  RETURN_IF(C % NH != 0, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(C, NH));
+  if (B == 0 || T == 0) return GPT2_OK;
+  RETURN_IF(workspace == nullptr || ws_bytes < attention_backward_workspace_size(B, T, C, NH), GPT2_ERR_WORKSPACE);
+  RETURN_IF(!aligned16(dqkv) || !aligned16(dout) || !aligned16(qkv) || !aligned16(out) || !aligned16(workspace),
+            GPT2_ERR_ALIGN);
+  float* Lrow = static_cast<float*>(workspace);
+  float* Drow = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                         round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256));
+  TRY(launch_attention_backward(dqkv, dout, qkv, out, Lrow, Drow, B, T, C, NH, as_stream(stream)));
+  return check_launch();
+}
+
 int gelu_forward(float* out, const float* inp, int n, void* stream) {
   RETURN_IF(!out || !inp || n < 0, GPT2_ERR_ARG);
   RETURN_IF(!aligned16(out) || !aligned16(inp), GPT2_ERR_ALIGN);

@@ -159,4 +159,9 @@ void launch_decode_attention_16(void* out, bool out16, const void* qkv, void* kc
 void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, float* vcache, int B, int C, int NH,
                                  int pos, const int* pos_arr, const KVRows& rows, cudaStream_t s);
 
+// attention_bwd.cu: the backward of causal attention in fp32; Lrow, Drow:
+// [B][NH][T] floats of scratch (the forward's row statistic, rowsum dO*O).
+int launch_attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, float* Lrow,
+                              float* Drow, int B, int T, int C, int NH, cudaStream_t s);
+
 }  // namespace gpt2

@@ -170,6 +170,26 @@ GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
 GPT2_API int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH, int precision, void* workspace,
                       size_t ws_bytes, void* stream);
 
+/* Scratch bytes attention_backward needs: two [B][NH][T] fp32 arrays (the
+ * forward's per-row softmax statistic and rowsum(dout * out)). */
+GPT2_API size_t attention_backward_workspace_size(int B, int T, int C, int NH);
+
+/* The backward pass of causal multi-head attention ["Understand
+ * FlashAttention (II)": the backward algorithms of Algorithms 0 and 1; the
+ * llm.c table's attention backward kernels], in fp32 on CUDA cores:
+ *   with S = q k^T / sqrt(hs) (causal), P = softmax_rows(S), out = P v and
+ *   dout = dL/dout:  dv = P^T dout,  dP = dout v^T,
+ *   dS = P (dP - rowsum(dout * out)),  dq = dS k / sqrt(hs),
+ *   dk = dS^T q / sqrt(hs),
+ * per (sequence, head), written into dqkv [B,T,3C] in the column blocks of
+ * q, k and v (every element written).  qkv [B,T,3C] and out [B,T,C] are
+ * the forward's input and output (out as attention_forward computes it in
+ * GPT2_FP32), dout [B,T,C].  P is recomputed tile by tile from a per-row
+ * statistic, never stored; the results do not depend on timing.  Requires
+ * hs in {16, 32, 64}; workspace of attention_backward_workspace_size bytes. */
+GPT2_API int attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, int B, int T,
+                                int C, int NH, void* workspace, size_t ws_bytes, void* stream);
+
 /* tanh-GELU [ECE408 "GELU"; llm.c gelu_forward]:
  *   out = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), n elements. */
 GPT2_API int gelu_forward(float* out, const float* inp, int n, void* stream);

@@ -17,7 +17,7 @@ def lib():
 
 def test_every_declared_function_is_exported(lib):
     names = ab.header_functions()
-    assert len(names) == 26
+    assert len(names) == 28
     for n in names:
         assert hasattr(lib, n), n
         assert n in ab._SIGNATURES, n
