@@ -250,3 +250,55 @@ def decode_step(cfg, params, cache, tok, pos: int, want_probs: bool = False):
     lib().oracle_gpt2_decode_step(ctypes.byref(c), _p(params), _p(kc), _p(vc), _p(tok), B, pos,
                                   _p(logits), _p(probs) if probs is not None else None)
     return (logits, probs) if want_probs else logits
+
+
+# ----------------------------------------------------------- training step
+def matmul_backward(dout, inp, W):
+    """y = x W^T + b: (dx, dW, db)."""
+    dout, inp, W = _f64(dout), _f64(inp), _f32(W)
+    OC, C = W.shape
+    N = inp.size // C
+    dinp = np.empty(inp.shape, dtype=np.float64)
+    dW = np.zeros((OC, C), dtype=np.float64)
+    db = np.zeros(OC, dtype=np.float64)
+    lib().oracle_matmul_backward(_p(dinp), _p(dW), _p(db), _p(dout), _p(inp), _p(W), N, C, OC)
+    return dinp, dW, db
+
+
+def layernorm_backward(dout, x, w, mean, rstd):
+    """(dx, dw, db) of LayerNorm, with the forward's mean and rstd."""
+    dout, x, w, mean, rstd = _f64(dout), _f64(x), _f32(w), _f64(mean), _f64(rstd)
+    C = x.shape[-1]
+    N = x.size // C
+    dx = np.empty_like(x)
+    dw = np.zeros(C, dtype=np.float64)
+    db = np.zeros(C, dtype=np.float64)
+    lib().oracle_layernorm_backward(_p(dx), _p(dw), _p(db), _p(dout), _p(x), _p(w), _p(mean), _p(rstd), N, C)
+    return dx, dw, db
+
+
+def gelu_backward(x, dout) -> np.ndarray:
+    x, dout = _f64(x), _f64(dout)
+    out = np.empty_like(x)
+    lib().oracle_gelu_backward(_p(out), _p(x), _p(dout), x.size)
+    return out
+
+
+def forward_backward(cfg, params, tok, targets):
+    """(mean cross-entropy loss, gradient [num_params] float64)."""
+    params, tok, targets = _f32(params), _i32(tok), _i32(targets)
+    B, T = tok.shape
+    c = config(cfg)
+    grads = np.empty(num_params(cfg), dtype=np.float64)
+    loss = ctypes.c_double()
+    lib().oracle_gpt2_forward_backward(ctypes.byref(c), _p(params), _p(tok), _p(targets), B, T, _p(grads),
+                                       ctypes.byref(loss))
+    return loss.value, grads
+
+
+def adamw(p, g, m, v, lr, b1, b2, eps, wd, t):
+    """One AdamW step on float64 copies; returns (p, m, v)."""
+    p, g, m, v = _f64(p).copy(), _f64(g), _f64(m).copy(), _f64(v).copy()
+    lib().oracle_adamw(_p(p), _p(g), _p(m), _p(v), ctypes.c_size_t(p.size), ctypes.c_double(lr),
+                       ctypes.c_double(b1), ctypes.c_double(b2), ctypes.c_double(eps), ctypes.c_double(wd), t)
+    return p, m, v

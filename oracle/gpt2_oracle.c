@@ -23,7 +23,10 @@
  *     (FlashAttention (II): the chain rule through the softmax, and its
  *     tiled form recomputing the attention matrix from row statistics);
  *   - tanh-form GELU, the residual add, the vocabulary softmax;
- *   - the KV-cached decode step (NanoGPT project, "KV Caching").
+ *   - the KV-cached decode step (NanoGPT project, "KV Caching");
+ *   - a training step's loss and gradient (softmax cross-entropy and the
+ *     backward of every forward step) and AdamW (llm.c "State of the
+ *     Union": forward blocks, classifier, backward blocks, optimizer).
  * All arithmetic is in double; parameters arrive as the caller's fp32 buffer
  * and are widened exactly.  OpenMP pragmas only split independent output
  * elements across threads: each element is still summed by one thread in
@@ -32,6 +35,7 @@
  * Parity pins for every function live in the test suite (closed forms,
  * invariants, brute force and library cross-checks); none is unpinned.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
@@ -626,4 +630,209 @@ void oracle_gpt2_decode_step(const OracleGPT2Config* cfg, const float* params,
   oracle_matmul(logits, h, w.wte, NULL, B, C, cfg->padded_vocab_size);
   if (probs) oracle_softmax(probs, logits, B, cfg->vocab_size, cfg->padded_vocab_size);
   free(x); free(h); free(qkv); free(att); free(proj); free(fc); free(fcg); free(p);
+}
+
+/* ====================================================== the training step */
+/* The backward pass of the whole model and the optimizer step (llm.c "State
+ * of the Union": a GPT-2 training step = forward blocks, the classifier
+ * (softmax cross-entropy), backward blocks, AdamW; the per-kernel table
+ * names their backward kernels: matmul backward with its bias, layernorm
+ * backward, gelu backward, the attention softmax backward, encoder
+ * backward).  Each backward below is the chain rule of its forward, written
+ * from the forward's definition. */
+
+/* y = x W^T + b:  dx = dy W (set),  dW += dy^T x,  db += sum over rows of dy */
+void oracle_matmul_backward(double* dinp, double* dW, double* db, const double* dout, const double* inp,
+                            const float* W, int N, int C, int OC) {
+#pragma omp parallel for schedule(static)
+  for (int n = 0; n < N; n++)
+    for (int c = 0; c < C; c++) {
+      double acc = 0.0;
+      for (int o = 0; o < OC; o++) acc += dout[(size_t)n * OC + o] * (double)W[(size_t)o * C + c];
+      dinp[(size_t)n * C + c] = acc;
+    }
+#pragma omp parallel for schedule(static)
+  for (int o = 0; o < OC; o++) {
+    for (int c = 0; c < C; c++) {
+      double acc = 0.0;
+      for (int n = 0; n < N; n++) acc += dout[(size_t)n * OC + o] * inp[(size_t)n * C + c];
+      dW[(size_t)o * C + c] += acc;
+    }
+    if (db) {
+      double acc = 0.0;
+      for (int n = 0; n < N; n++) acc += dout[(size_t)n * OC + o];
+      db[o] += acc;
+    }
+  }
+}
+
+/* y = xhat w + b with xhat = (x - mean) rstd:  dw += sum dy xhat,
+ * db += sum dy, and with g = dy w:
+ * dx = rstd (g - mean_c(g) - xhat mean_c(g xhat))  (set) */
+void oracle_layernorm_backward(double* dinp, double* dw, double* db, const double* dout, const double* inp,
+                               const float* w, const double* mean, const double* rstd, int N, int C) {
+  for (int n = 0; n < N; n++) {
+    const double* x = inp + (size_t)n * C;
+    const double* dy = dout + (size_t)n * C;
+    double mg = 0.0, mgx = 0.0;
+    for (int c = 0; c < C; c++) {
+      const double xhat = (x[c] - mean[n]) * rstd[n];
+      const double g = dy[c] * (double)w[c];
+      mg += g;
+      mgx += g * xhat;
+      dw[c] += dy[c] * xhat;
+      db[c] += dy[c];
+    }
+    mg /= C;
+    mgx /= C;
+    for (int c = 0; c < C; c++) {
+      const double xhat = (x[c] - mean[n]) * rstd[n];
+      dinp[(size_t)n * C + c] = rstd[n] * (dy[c] * (double)w[c] - mg - xhat * mgx);
+    }
+  }
+}
+
+/* d/dx of 0.5 x (1 + tanh(u)), u = sqrt(2/pi) (x + 0.044715 x^3):
+ * 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) sqrt(2/pi) (1 + 3 * 0.044715 x^2) */
+void oracle_gelu_backward(double* dinp, const double* inp, const double* dout, int n) {
+  const double k = sqrt(2.0 / M_PI);
+  for (int i = 0; i < n; i++) {
+    const double x = inp[i];
+    const double th = tanh(k * (x + 0.044715 * x * x * x));
+    const double d = 0.5 * (1.0 + th) + 0.5 * x * (1.0 - th * th) * k * (1.0 + 3.0 * 0.044715 * x * x);
+    dinp[i] = dout[i] * d;
+  }
+}
+
+/* One training step's loss and gradient: mean over the B*T positions of the
+ * cross-entropy -log probs[n][targets[n]] of the vocabulary softmax, and its
+ * gradient with respect to every parameter, in the parameter buffer's
+ * layout (grads: double[num_params], overwritten).  The forward keeps every
+ * activation the backward needs. */
+void oracle_gpt2_forward_backward(const OracleGPT2Config* cfg, const float* params, const int* tok,
+                                  const int* targets, int B, int T, double* grads, double* loss_out) {
+  const int C = cfg->channels, L = cfg->num_layers, NH = cfg->num_heads;
+  const int V = cfg->vocab_size, Vp = cfg->padded_vocab_size;
+  const size_t N = (size_t)B * T, NC = N * C;
+  OracleParams w = oracle_params(cfg, params);
+  /* the gradient buffer, viewed like the parameters */
+  const size_t np = oracle_num_params(cfg);
+  memset(grads, 0, sizeof(double) * np);
+  const size_t o_wte = w.wte - params, o_wpe = w.wpe - params, o_ln1w = w.ln1w - params, o_ln1b = w.ln1b - params,
+               o_qkvw = w.qkvw - params, o_qkvb = w.qkvb - params, o_apw = w.attprojw - params,
+               o_apb = w.attprojb - params, o_ln2w = w.ln2w - params, o_ln2b = w.ln2b - params,
+               o_fcw = w.fcw - params, o_fcb = w.fcb - params, o_fpw = w.fcprojw - params,
+               o_fpb = w.fcprojb - params, o_lnfw = w.lnfw - params, o_lnfb = w.lnfb - params;
+  /* ---- forward, keeping activations (per layer) */
+  double* xin = (double*)malloc(sizeof(double) * (L + 1) * NC);   /* residual stream entering layer l; [L] = final */
+  double* xmid = (double*)malloc(sizeof(double) * L * NC);        /* after the attention sub-block */
+  double* ln1 = (double*)malloc(sizeof(double) * L * NC);
+  double* ln1m = (double*)malloc(sizeof(double) * L * N);
+  double* ln1r = (double*)malloc(sizeof(double) * L * N);
+  double* qkv = (double*)malloc(sizeof(double) * L * 3 * NC);
+  double* att = (double*)malloc(sizeof(double) * L * NC);
+  double* ln2 = (double*)malloc(sizeof(double) * L * NC);
+  double* ln2m = (double*)malloc(sizeof(double) * L * N);
+  double* ln2r = (double*)malloc(sizeof(double) * L * N);
+  double* fc = (double*)malloc(sizeof(double) * L * 4 * NC);
+  double* fcg = (double*)malloc(sizeof(double) * L * 4 * NC);
+  double* lnf = (double*)malloc(sizeof(double) * NC);
+  double* lnfm = (double*)malloc(sizeof(double) * N);
+  double* lnfr = (double*)malloc(sizeof(double) * N);
+  double* logits = (double*)malloc(sizeof(double) * N * Vp);
+  double* proj = (double*)malloc(sizeof(double) * NC);
+  oracle_encoder(xin, tok, w.wte, w.wpe, B, T, C);
+  for (int l = 0; l < L; l++) {
+    double* x = xin + (size_t)l * NC;
+    double* xm = xmid + (size_t)l * NC;
+    oracle_layernorm(ln1 + l * NC, ln1m + l * N, ln1r + l * N, x, w.ln1w + (size_t)l * C, w.ln1b + (size_t)l * C,
+                     (int)N, C);
+    oracle_matmul(qkv + l * 3 * NC, ln1 + l * NC, w.qkvw + (size_t)l * 3 * C * C, w.qkvb + (size_t)l * 3 * C, (int)N,
+                  C, 3 * C);
+    oracle_attention(att + l * NC, qkv + l * 3 * NC, B, T, C, NH);
+    oracle_matmul(proj, att + l * NC, w.attprojw + (size_t)l * C * C, w.attprojb + (size_t)l * C, (int)N, C, C);
+    oracle_residual(xm, x, proj, (int)NC);
+    oracle_layernorm(ln2 + l * NC, ln2m + l * N, ln2r + l * N, xm, w.ln2w + (size_t)l * C, w.ln2b + (size_t)l * C,
+                     (int)N, C);
+    oracle_matmul(fc + l * 4 * NC, ln2 + l * NC, w.fcw + (size_t)l * 4 * C * C, w.fcb + (size_t)l * 4 * C, (int)N, C,
+                  4 * C);
+    oracle_gelu(fcg + l * 4 * NC, fc + l * 4 * NC, (int)(4 * NC));
+    oracle_matmul(proj, fcg + l * 4 * NC, w.fcprojw + (size_t)l * 4 * C * C, w.fcprojb + (size_t)l * C, (int)N,
+                  4 * C, C);
+    oracle_residual(xin + (size_t)(l + 1) * NC, xm, proj, (int)NC);
+  }
+  oracle_layernorm(lnf, lnfm, lnfr, xin + (size_t)L * NC, w.lnfw, w.lnfb, (int)N, C);
+  oracle_matmul(logits, lnf, w.wte, NULL, (int)N, C, Vp);
+  /* ---- the loss and dL/dlogits (softmax cross-entropy, mean over rows) */
+  double loss = 0.0;
+  for (size_t n = 0; n < N; n++) {
+    double* lg = logits + n * Vp;
+    double mx = -INFINITY;
+    for (int v = 0; v < V; v++) if (lg[v] > mx) mx = lg[v];
+    double sum = 0.0;
+    for (int v = 0; v < V; v++) sum += exp(lg[v] - mx);
+    loss += -(lg[targets[n]] - mx - log(sum));
+    for (int v = 0; v < Vp; v++) {  /* logits become dlogits */
+      const double p = v < V ? exp(lg[v] - mx) / sum : 0.0;
+      lg[v] = (p - (v == targets[n] ? 1.0 : 0.0)) / (double)N;
+    }
+  }
+  *loss_out = loss / (double)N;
+  /* ---- backward */
+  double* dx = (double*)malloc(sizeof(double) * NC);
+  double* dh = (double*)malloc(sizeof(double) * NC);
+  double* dt = (double*)malloc(sizeof(double) * 4 * NC);
+  double* dt2 = (double*)malloc(sizeof(double) * 4 * NC);
+  double* dqkv = (double*)malloc(sizeof(double) * 3 * NC);
+  /* the tied LM head: logits = lnf wte^T */
+  oracle_matmul_backward(dh, grads + o_wte, NULL, logits, lnf, w.wte, (int)N, C, Vp);
+  oracle_layernorm_backward(dx, grads + o_lnfw, grads + o_lnfb, dh, xin + (size_t)L * NC, w.lnfw, lnfm, lnfr, (int)N,
+                            C);
+  for (int l = L - 1; l >= 0; l--) {
+    /* x_out = x_mid + fcproj(GELU(fc(LN2(x_mid)))): dx is dL/dx_out */
+    oracle_matmul_backward(dt, grads + o_fpw + (size_t)l * 4 * C * C, grads + o_fpb + (size_t)l * C, dx,
+                           fcg + l * 4 * NC, w.fcprojw + (size_t)l * 4 * C * C, (int)N, 4 * C, C);
+    oracle_gelu_backward(dt2, fc + l * 4 * NC, dt, (int)(4 * NC));
+    oracle_matmul_backward(dh, grads + o_fcw + (size_t)l * 4 * C * C, grads + o_fcb + (size_t)l * 4 * C, dt2,
+                           ln2 + l * NC, w.fcw + (size_t)l * 4 * C * C, (int)N, C, 4 * C);
+    oracle_layernorm_backward(dt, grads + o_ln2w + (size_t)l * C, grads + o_ln2b + (size_t)l * C, dh,
+                              xmid + (size_t)l * NC, w.ln2w + (size_t)l * C, ln2m + l * N, ln2r + l * N, (int)N, C);
+    for (size_t i = 0; i < NC; i++) dx[i] += dt[i];  /* dL/dx_mid: the residual path plus the MLP's */
+    /* x_mid = x_in + attproj(attention(qkv(LN1(x_in)))) */
+    oracle_matmul_backward(dh, grads + o_apw + (size_t)l * C * C, grads + o_apb + (size_t)l * C, dx, att + l * NC,
+                           w.attprojw + (size_t)l * C * C, (int)N, C, C);
+    oracle_attention_backward(dqkv, dh, qkv + l * 3 * NC, B, T, C, NH);
+    oracle_matmul_backward(dh, grads + o_qkvw + (size_t)l * 3 * C * C, grads + o_qkvb + (size_t)l * 3 * C, dqkv,
+                           ln1 + l * NC, w.qkvw + (size_t)l * 3 * C * C, (int)N, C, 3 * C);
+    oracle_layernorm_backward(dt, grads + o_ln1w + (size_t)l * C, grads + o_ln1b + (size_t)l * C, dh,
+                              xin + (size_t)l * NC, w.ln1w + (size_t)l * C, ln1m + l * N, ln1r + l * N, (int)N, C);
+    for (size_t i = 0; i < NC; i++) dx[i] += dt[i];  /* dL/dx_in */
+  }
+  /* the encoder: x = wte[tok] + wpe[t] */
+  for (int b = 0; b < B; b++)
+    for (int t = 0; t < T; t++) {
+      const size_t n = (size_t)b * T + t;
+      for (int c = 0; c < C; c++) {
+        grads[o_wte + (size_t)tok[n] * C + c] += dx[n * C + c];
+        grads[o_wpe + (size_t)t * C + c] += dx[n * C + c];
+      }
+    }
+  free(xin); free(xmid); free(ln1); free(ln1m); free(ln1r); free(qkv); free(att); free(ln2); free(ln2m);
+  free(ln2r); free(fc); free(fcg); free(lnf); free(lnfm); free(lnfr); free(logits); free(proj);
+  free(dx); free(dh); free(dt); free(dt2); free(dqkv);
+}
+
+/* AdamW (Loshchilov and Hutter, "Decoupled Weight Decay Regularization",
+ * Algorithm 2), step t >= 1, the same decay for every parameter:
+ *   m = b1 m + (1 - b1) g,  v = b2 v + (1 - b2) g^2,
+ *   mhat = m / (1 - b1^t),  vhat = v / (1 - b2^t),
+ *   p -= lr (mhat / (sqrt(vhat) + eps) + wd p). */
+void oracle_adamw(double* p, const double* g, double* m, double* v, size_t n, double lr, double b1, double b2,
+                  double eps, double wd, int t) {
+  const double c1 = 1.0 - pow(b1, t), c2 = 1.0 - pow(b2, t);
+  for (size_t i = 0; i < n; i++) {
+    m[i] = b1 * m[i] + (1.0 - b1) * g[i];
+    v[i] = b2 * v[i] + (1.0 - b2) * g[i] * g[i];
+    p[i] -= lr * ((m[i] / c1) / (sqrt(v[i] / c2) + eps) + wd * p[i]);
+  }
 }
