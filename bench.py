@@ -24,6 +24,8 @@ prefill of 32 prompts of 512 tokens (reported apart), then 128 greedy steps
 (argmax + gpt2_decode_step), K runs timed; value = decoded tokens/s.
 --gemm-diag adds each GEMM site's time beside cuBLAS at the same shape.
 --attention-backward times one layer's attention backward (fp32) instead.
+--train times whole training steps (forward, softmax cross-entropy,
+backward, AdamW; tf32 GEMMs, or fp32 with --precision fp32) instead.
 """
 from __future__ import annotations
 
@@ -443,6 +445,58 @@ def run_attention_backward(args, w):
         pg.destroy_process_group()
 
 
+TRAIN_METRIC = "GPT-2 training step tokens/s (forward, softmax cross-entropy, backward, AdamW) on 1 GB300"
+
+
+def run_train(args, w):
+    """Training steps at the workload's shape: gpt2_forward_backward then
+    gpt2_adamw, K timed steps after W warm-up steps (fp32 activations; tf32
+    tensor-core operands unless --precision fp32)."""
+    import torch
+    from gpt_transformer_forward_gb300 import binding as ab
+
+    precision = ab.GPT2_FP32 if args.precision == "fp32" else ab.GPT2_TF32
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    params, tok = inputs.workload_inputs(w)
+    tok = rank_tokens(w, tok, rank)
+    cfg, B, T = w.cfg, w.B, w.T
+    tgt = np.roll(tok, -1, axis=1)  # next-token targets (the last wraps to the first)
+    P = torch.from_numpy(params).cuda()
+    G, M, V = torch.empty_like(P), torch.zeros_like(P), torch.zeros_like(P)
+    tk, tg = torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda()
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    wsz = ab.gpt2_train_workspace_size(cfg, B, T, precision)
+    ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+
+    def step(t):
+        ab.gpt2_forward_backward(cfg, P, G, tk, tg, B, T, loss, ws, wsz, precision)
+        ab.gpt2_adamw(P, G, M, V, P.numel(), 3e-4, 0.9, 0.95, 1e-8, 0.0, t)
+
+    for t in range(1, args.warmup + 1):
+        step(t)
+    torch.cuda.synchronize()
+    first = float(loss.item())
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(args.warmup + 1, args.warmup + args.steps + 1):
+        step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+    line = {"metric": TRAIN_METRIC, "value": job_tokens_per_s(world, B * T, ms), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32" if precision == ab.GPT2_FP32 else "f32 (tf32 GEMMs)",
+            "data": "synthetic", "config": {"workload": w.name + "-train", "B": B, "T": T, "layers": cfg.num_layers},
+            "loss_after_warmup": first, "loss_last": float(loss.item()),
+            "workspace_gb": wsz / 1e9, "device_error_word": ab.gpt2_get_error()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def run_ours(args):
     import torch
     from gpt_transformer_forward_gb300 import binding as ab
@@ -452,6 +506,8 @@ def run_ours(args):
     precision = ab.PRECISIONS[args.precision]
     if args.attention_backward:
         return run_attention_backward(args, w)
+    if args.train:
+        return run_train(args, w)
     if w.decode_steps:
         return run_decode(args, w, precision)
     rank, world, local, pg = dist_setup(args.gpus)
@@ -600,6 +656,8 @@ def main():
     ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--precision", default="fp16", choices=["fp16", "bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--train", action="store_true",
+                    help="time training steps (forward, loss, backward, AdamW) at the workload's shape instead")
     ap.add_argument("--attention-backward", action="store_true",
                     help="time one layer's attention backward (fp32) at the workload's shape instead")
     ap.add_argument("--gemm-diag", action="store_true",

@@ -79,6 +79,10 @@ _SIGNATURES = {
     "gpt2_kvcache_size": (_Z, [_CFG, _I, _I]),
     "gpt2_forward": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _P, _P, _Z, _I, _P]),
     "gpt2_decode_step": (_I, [_CFG, _P, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _I, _P]),
+    "gpt2_train_workspace_size": (_Z, [_CFG, _I, _I, _I]),
+    "gpt2_forward_backward": (_I, [_CFG, _P, _P, _P, _P, _I, _I, _P, _P, _Z, _I, _P]),
+    "gpt2_adamw": (_I, [_P, _P, _P, _P, _Z, ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                        ctypes.c_float, _I, _P]),
     "gpt2_paged_kvcache_size": (_Z, [_CFG, _I, _I, _I]),
     "gpt2_prefill_paged": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _PKV, _P, _Z, _I, _P]),
     "gpt2_decode_step_paged": (_I, [_CFG, _P, _P, _PKV, _P, _P, _I, _P, _P, _P, _Z, _I, _P]),
@@ -254,6 +258,22 @@ def gpt2_decode_step(cfg, params, packed, kvcache, tok, B, pos, logits, probs, w
 
 
 STAGES = ["encoder", "ln1", "qkv", "attention", "attproj", "ln2", "fc", "fcproj", "lnf", "lm_head", "softmax"]
+
+
+def gpt2_train_workspace_size(cfg, B, T, precision) -> int:
+    return _lib().gpt2_train_workspace_size(_cfg(cfg), B, T, precision)
+
+
+def gpt2_forward_backward(cfg, params, grads, tok, targets, B, T, loss, workspace, ws_bytes, precision,
+                          stream=None):
+    _check("gpt2_forward_backward", _lib().gpt2_forward_backward(
+        _cfg(cfg), _ptr(params), _ptr(grads), _ptr(tok), _ptr(targets), B, T, _ptr(loss), _ptr(workspace), ws_bytes,
+        precision, _stream(stream)))
+
+
+def gpt2_adamw(params, grads, m, v, n, lr, beta1, beta2, eps, weight_decay, t, stream=None):
+    _check("gpt2_adamw", _lib().gpt2_adamw(_ptr(params), _ptr(grads), _ptr(m), _ptr(v), n, lr, beta1, beta2, eps,
+                                           weight_decay, t, _stream(stream)))
 
 
 def paged_kv(pool, block_table, num_blocks, block_size, max_blocks_per_seq) -> GPT2PagedKVCache:

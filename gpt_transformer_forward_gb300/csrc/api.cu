@@ -281,6 +281,57 @@ struct StageProfiler {
   }
 };
 
+// ----------------------------------------------------- training workspace
+// fp32 activations of every layer kept for the backward, and the backward's
+// scratch; offsets in bytes, each 256-byte aligned.
+struct TrainLayout {
+  size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj, dx,
+      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, total;
+};
+
+TrainLayout train_layout(const GPT2Config* c, int B, int T) {
+  const size_t N = static_cast<size_t>(B) * T, C = c->channels, L = c->num_layers, Vp = c->padded_vocab_size;
+  const size_t NC = N * C, F = sizeof(float);
+  const size_t wide = Vp > 4 * C ? Vp : 4 * C;
+  TrainLayout t;
+  size_t p = 0;
+  auto take = [&](size_t floats) {
+    const size_t at = p;
+    p = round_up(p + floats * F, 256);
+    return at;
+  };
+  t.xin = take((L + 1) * NC);
+  t.xmid = take(L * NC);
+  t.ln1 = take(L * NC);
+  t.ln2 = take(L * NC);
+  t.ln1m = take(L * N);
+  t.ln1r = take(L * N);
+  t.ln2m = take(L * N);
+  t.ln2r = take(L * N);
+  t.qkv = take(L * 3 * NC);
+  t.att = take(L * NC);
+  t.fc = take(L * 4 * NC);
+  t.fcg = take(L * 4 * NC);
+  t.lnf = take(NC);
+  t.lnfm = take(N);
+  t.lnfr = take(N);
+  t.logits = take(N * Vp);
+  t.losses = take(N);
+  t.proj = take(NC);
+  t.dx = take(NC);
+  t.dh = take(NC);
+  t.dt = take(4 * NC);
+  t.dt2 = take(4 * NC);
+  t.dqkv = take(3 * NC);
+  t.tA = take(N * wide);
+  t.tB = take(4 * NC);
+  t.Wt = take(wide * C);
+  t.part = take(2 * static_cast<size_t>(column_parts(static_cast<int>(N))) * wide);
+  t.attn = take(2 * static_cast<size_t>(B) * c->num_heads * T);
+  t.total = p;
+  return t;
+}
+
 }  // namespace
 }  // namespace gpt2
 
@@ -742,5 +793,123 @@ const char* gpt2_strerror(int code) {
 }
 
 const char* gpt2_last_cuda_error(void) { return g_last_cuda_error.c_str(); }
+
+size_t gpt2_train_workspace_size(const GPT2Config* cfg, int B, int T, int precision) {
+  if (check_config(cfg) != GPT2_OK || B <= 0 || T <= 0 || (precision != GPT2_FP32 && precision != GPT2_TF32))
+    return 0;
+  return train_layout(cfg, B, T).total;
+}
+
+int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* grads, const int* tok,
+                          const int* targets, int B, int T, float* loss, void* workspace, size_t ws_bytes,
+                          int precision, void* stream) {
+  TRY(check_config(cfg));
+  RETURN_IF(!params || !grads || !tok || !targets || !loss || !workspace, GPT2_ERR_ARG);
+  RETURN_IF(B <= 0 || T <= 0, GPT2_ERR_ARG);
+  RETURN_IF(precision != GPT2_FP32 && precision != GPT2_TF32, GPT2_ERR_UNSUPPORTED);
+  RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
+  TRY(check_attention_shape(cfg->channels, cfg->num_heads));
+  // tf32 operands: every K-major row of a GEMM operand is a whole number of
+  // 16-byte units (the reductions run over C, 4C, Vp and the B*T tokens)
+  RETURN_IF(precision == GPT2_TF32 && (cfg->channels % 8 != 0 || (B * T) % 4 != 0), GPT2_ERR_SHAPE);
+  RETURN_IF(!aligned16(params) || !aligned16(grads) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0,
+            GPT2_ERR_ALIGN);
+  const TrainLayout tl = train_layout(cfg, B, T);
+  RETURN_IF(ws_bytes < tl.total, GPT2_ERR_WORKSPACE);
+  cudaStream_t s = as_stream(stream);
+  const int C = cfg->channels, L = cfg->num_layers, NH = cfg->num_heads, V = cfg->vocab_size;
+  const int Vp = cfg->padded_vocab_size, maxT = cfg->max_seq_len;
+  const int N = B * T;
+  const size_t NC = static_cast<size_t>(N) * C, CC = static_cast<size_t>(C) * C;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  auto buf = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+  float *xin = buf(tl.xin), *xmid = buf(tl.xmid), *ln1 = buf(tl.ln1), *ln2 = buf(tl.ln2);
+  float *ln1m = buf(tl.ln1m), *ln1r = buf(tl.ln1r), *ln2m = buf(tl.ln2m), *ln2r = buf(tl.ln2r);
+  float *qkv = buf(tl.qkv), *att = buf(tl.att), *fc = buf(tl.fc), *fcg = buf(tl.fcg);
+  float *lnf = buf(tl.lnf), *lnfm = buf(tl.lnfm), *lnfr = buf(tl.lnfr), *logits = buf(tl.logits);
+  float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
+  float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
+  float *part = buf(tl.part), *attn = buf(tl.attn);
+  const ParamOffsets po = param_offsets(cfg);
+  auto P = [&](size_t off) { return params + off; };
+  auto G = [&](size_t off) { return grads + off; };
+  // ---------------------------------------------------------------- forward
+  launch_encoder(xin, tok, P(po.wte), P(po.wpe), N, T, C, V, s);
+  for (int l = 0; l < L; ++l) {
+    float* x = xin + l * NC;
+    launch_layernorm_f32(ln1 + l * NC, ln1m + static_cast<size_t>(l) * N, ln1r + static_cast<size_t>(l) * N, x,
+                         P(po.ln1w) + l * C, P(po.ln1b) + l * C, N, C, s);
+    TRY(gemm(precision, qkv + l * 3 * NC, ln1 + l * NC, P(po.qkvw) + l * 3 * CC, P(po.qkvb) + l * 3 * C, N, 3 * C, C,
+             kEpiF32, s));
+    TRY(launch_attention_f32(att + l * NC, qkv + l * 3 * NC, B, T, C, NH, s));
+    TRY(gemm(precision, proj, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, N, C, C, kEpiF32, s));
+    launch_residual(xmid + l * NC, x, proj, static_cast<int>(NC), s);
+    launch_layernorm_f32(ln2 + l * NC, ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N,
+                         xmid + l * NC, P(po.ln2w) + l * C, P(po.ln2b) + l * C, N, C, s);
+    TRY(gemm(precision, fc + l * 4 * NC, ln2 + l * NC, P(po.fcw) + l * 4 * CC, P(po.fcb) + l * 4 * C, N, 4 * C, C,
+             kEpiF32, s));
+    launch_gelu(fcg + l * 4 * NC, fc + l * 4 * NC, static_cast<int>(4 * NC), s);
+    TRY(gemm(precision, proj, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC, P(po.fcprojb) + l * C, N, C, 4 * C,
+             kEpiF32, s));
+    launch_residual(xin + (l + 1) * NC, xmid + l * NC, proj, static_cast<int>(NC), s);
+  }
+  launch_layernorm_f32(lnf, lnfm, lnfr, xin + L * NC, P(po.lnfw), P(po.lnfb), N, C, s);
+  TRY(gemm(precision, logits, lnf, P(po.wte), nullptr, N, Vp, C, kEpiF32, s));
+  launch_crossentropy(logits, losses, loss, targets, N, V, Vp, s);  // logits become dL/dlogits
+  TRY(check_launch());
+  // --------------------------------------------------------------- backward
+  // y = x W^T + b with x [N,K], W [OC,K]: dx = dy W (set), dW = dy^T x (set),
+  // db = column sums of dy; the GEMM kernels take K-major operands, so W,
+  // dy and x are transposed first
+  auto mm_bwd = [&](float* dinp, float* dW, float* db, const float* dy, const float* x, const float* W, int OC,
+                    int K) -> int {
+    launch_transpose(Wt, W, OC, K, s);  // [K][OC]
+    TRY(gemm(precision, dinp, dy, Wt, nullptr, N, K, OC, kEpiF32, s));
+    launch_transpose(tA, dy, N, OC, s);  // [OC][N]
+    launch_transpose(tB, x, N, K, s);    // [K][N]
+    TRY(gemm(precision, dW, tA, tB, nullptr, OC, K, N, kEpiF32, s));
+    if (db != nullptr) launch_column_sum(db, part, dy, N, OC, false, s);
+    return check_launch();
+  };
+  TRY(mm_bwd(dh, G(po.wte), nullptr, logits, lnf, P(po.wte), Vp, C));  // the tied LM head
+  launch_layernorm_backward(dx, G(po.lnfw), G(po.lnfb), part, dh, xin + L * NC, P(po.lnfw), lnfm, lnfr, N, C, false,
+                            s);
+  for (int l = L - 1; l >= 0; --l) {
+    // x_out = x_mid + fcproj(GELU(fc(LN2(x_mid)))); dx = dL/dx_out
+    TRY(mm_bwd(dt, G(po.fcprojw) + l * 4 * CC, G(po.fcprojb) + l * C, dx, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC,
+               C, 4 * C));
+    launch_gelu_backward(dt2, fc + l * 4 * NC, dt, static_cast<long long>(4 * NC), s);
+    TRY(mm_bwd(dh, G(po.fcw) + l * 4 * CC, G(po.fcb) + l * 4 * C, dt2, ln2 + l * NC, P(po.fcw) + l * 4 * CC, 4 * C,
+               C));
+    launch_layernorm_backward(dx, G(po.ln2w) + l * C, G(po.ln2b) + l * C, part, dh, xmid + l * NC, P(po.ln2w) + l * C,
+                              ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N, N, C, true, s);
+    // x_mid = x_in + attproj(attention(qkv(LN1(x_in)))); dx = dL/dx_mid
+    TRY(mm_bwd(dh, G(po.attprojw) + l * CC, G(po.attprojb) + l * C, dx, att + l * NC, P(po.attprojw) + l * CC, C, C));
+    TRY(launch_attention_backward(dqkv, dh, qkv + l * 3 * NC, att + l * NC, attn,
+                                  attn + static_cast<size_t>(B) * NH * T, B, T, C, NH, s));
+    TRY(mm_bwd(dh, G(po.qkvw) + l * 3 * CC, G(po.qkvb) + l * 3 * C, dqkv, ln1 + l * NC, P(po.qkvw) + l * 3 * CC,
+               3 * C, C));
+    launch_layernorm_backward(dx, G(po.ln1w) + l * C, G(po.ln1b) + l * C, part, dh, xin + l * NC, P(po.ln1w) + l * C,
+                              ln1m + static_cast<size_t>(l) * N, ln1r + static_cast<size_t>(l) * N, N, C, true, s);
+  }
+  // the encoder: x = wte[tok] + wpe[t]; the position rows past T get none
+  if (T < maxT) {
+    const cudaError_t e = cudaMemsetAsync(G(po.wpe) + static_cast<size_t>(T) * C, 0,
+                                          static_cast<size_t>(maxT - T) * C * sizeof(float), s);
+    if (e != cudaSuccess) return note_cuda_error(e);
+  }
+  launch_encoder_backward(G(po.wte), G(po.wpe), dx, tok, B, T, C, V, s);
+  return check_launch();
+}
+
+int gpt2_adamw(float* params, const float* grads, float* m, float* v, size_t n, float lr, float beta1, float beta2,
+               float eps, float weight_decay, int t, void* stream) {
+  RETURN_IF(!params || !grads || !m || !v || t < 1, GPT2_ERR_ARG);
+  RETURN_IF(!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(eps > 0.f), GPT2_ERR_ARG);
+  if (n == 0) return GPT2_OK;
+  launch_adamw(params, grads, m, v, static_cast<long long>(n), lr, beta1, beta2, eps, weight_decay, t,
+               as_stream(stream));
+  return check_launch();
+}
 
 }  // extern "C"

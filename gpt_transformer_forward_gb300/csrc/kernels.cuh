@@ -164,4 +164,25 @@ void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, fl
 int launch_attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, float* Lrow,
                               float* Drow, int B, int T, int C, int NH, cudaStream_t s);
 
+// train.cu: the training step's kernels (fp32).  column_parts(rows): the
+// partial sums a column reduction over `rows` rows keeps in scratch.
+int column_parts(int rows);
+void launch_transpose(float* out, const float* in, int rows, int cols, cudaStream_t s);
+// softmax cross-entropy over the first V of Vp columns: losses[n], the mean
+// into loss[0], dlogits (p - onehot) / N written over the logits
+void launch_crossentropy(float* logits, float* losses, float* loss, const int* targets, int N, int V, int Vp,
+                         cudaStream_t s);
+// out[c] (+)= sum over rows of in[r][c]; part: column_parts(rows) x cols floats
+void launch_column_sum(float* out, float* part, const float* in, int rows, int cols, bool accumulate, cudaStream_t s);
+// dx (+)= LayerNorm backward; dw, db set; part: 2 x column_parts(N) x C floats
+void launch_layernorm_backward(float* dx, float* dw, float* db, float* part, const float* dy, const float* x,
+                               const float* w, const float* mean, const float* rstd, int N, int C, bool accumulate,
+                               cudaStream_t s);
+void launch_gelu_backward(float* dinp, const float* inp, const float* dout, long long n, cudaStream_t s);
+// dwpe rows [0, T) set; dwte[tok] += dx
+void launch_encoder_backward(float* dwte, float* dwpe, const float* dx, const int* tok, int B, int T, int C, int V,
+                             cudaStream_t s);
+void launch_adamw(float* p, const float* g, float* m, float* v, long long n, float lr, float b1, float b2, float eps,
+                  float wd, int t, cudaStream_t s);
+
 }  // namespace gpt2

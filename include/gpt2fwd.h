@@ -273,6 +273,47 @@ GPT2_API int gpt2_decode_step(const GPT2Config* cfg, const float* params, const 
                      int B, int pos, float* logits, float* probs, void* workspace, size_t ws_bytes, int precision,
                      void* stream);
 
+/* ------------------------------------------------------- training step */
+
+/* Workspace bytes of gpt2_forward_backward for B sequences of T tokens
+ * (every layer's fp32 activations and the backward's scratch); 0 unless
+ * precision is GPT2_FP32 or GPT2_TF32. */
+GPT2_API size_t gpt2_train_workspace_size(const GPT2Config* cfg, int B, int T, int precision);
+
+/* The loss and gradient of one training step [llm.c "State of the Union":
+ * a GPT-2 training step is the forward blocks, the classifier (softmax with
+ * cross-entropy), the backward blocks and the optimizer; its per-kernel
+ * table names the backward kernels built here: matmul backward with its
+ * bias, layernorm backward, gelu backward, attention backward, encoder
+ * backward]:
+ *   loss = mean over the B*T positions of -log softmax(logits)[target],
+ *          the softmax over the first V columns (loss: DEVICE, one float);
+ *   grads = dloss/dparams, in the layout of the flat parameter buffer
+ *          (gpt2_num_parameters floats, DEVICE, every element written).
+ * params as gpt2_forward's (fp32, never written); tok, targets [B,T] int32
+ * (DEVICE).  Activations and gradients are fp32; the matmuls (and their
+ * backward products) run on fp32 CUDA cores in GPT2_FP32 and on tcgen05
+ * tensor cores with tf32 operands in GPT2_TF32 (then B*T % 4 == 0); the
+ * attention's forward and backward run in fp32 on CUDA cores in both.
+ * Other precisions return GPT2_ERR_UNSUPPORTED.  The token-embedding
+ * gradient sums repeated tokens with atomics: its last bits can vary from
+ * run to run; every other element is deterministic.  A target outside
+ * [0, V) sets GPT2_DEVERR_TOKEN_BIT. */
+GPT2_API int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* grads, const int* tok,
+                                   const int* targets, int B, int T, float* loss, void* workspace, size_t ws_bytes,
+                                   int precision, void* stream);
+
+/* One AdamW step over n fp32 values [llm.c "State of the Union": the
+ * optimizer of the training step; the update is AdamW's, decoupled weight
+ * decay (Loshchilov and Hutter), the same decay for every parameter]:
+ *   m = beta1 m + (1 - beta1) g,  v = beta2 v + (1 - beta2) g^2,
+ *   params -= lr (m / (1 - beta1^t) / (sqrt(v / (1 - beta2^t)) + eps)
+ *                 + weight_decay params),
+ * t >= 1 the step number; m and v (DEVICE, n floats each, zero before the
+ * first step) are updated in place. */
+GPT2_API int gpt2_adamw(float* params, const float* grads, float* m, float* v, size_t n, float lr, float beta1,
+                        float beta2, float eps, float weight_decay, int t, void* stream);
+
 /* --------------------------------------------------- paged KV cache */
 
 /* A paged KV cache [NTU "KV Caching": the keys and values of earlier

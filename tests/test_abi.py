@@ -17,7 +17,7 @@ def lib():
 
 def test_every_declared_function_is_exported(lib):
     names = ab.header_functions()
-    assert len(names) == 28
+    assert len(names) == 31
     for n in names:
         assert hasattr(lib, n), n
         assert n in ab._SIGNATURES, n
@@ -106,4 +106,23 @@ def test_paged_calls_check_their_arguments_on_the_host(lib):
     with pytest.raises(ab.GPT2Error) as e:
         ab.gpt2_decode_step_paged(cfg, fake, fake, None, fake, fake, 2, fake, None, fake, 1 << 20, ab.GPT2_FP16,
                                   stream=0)
+    assert e.value.code == -1
+
+
+def test_training_calls_check_their_arguments_on_the_host(lib):
+    cfg = inputs.TINY
+    assert ab.gpt2_train_workspace_size(cfg, 2, 32, ab.GPT2_BF16) == 0  # fp32 activations only
+    assert ab.gpt2_train_workspace_size(cfg, 2, 32, ab.GPT2_FP32) > 0
+    fake = 1 << 20
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_forward_backward(cfg, fake, fake, fake, fake, 2, 32, fake, fake, 1 << 30, ab.GPT2_FP16, stream=0)
+    assert e.value.code == -7
+    with pytest.raises(ab.GPT2Error) as e:  # tf32 needs B*T % 4 == 0
+        ab.gpt2_forward_backward(cfg, fake, fake, fake, fake, 1, 3, fake, fake, 1 << 30, ab.GPT2_TF32, stream=0)
+    assert e.value.code == -2
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_forward_backward(cfg, fake, fake, fake, fake, 2, 32, fake, fake, 16, ab.GPT2_FP32, stream=0)
+    assert e.value.code == -4
+    with pytest.raises(ab.GPT2Error) as e:
+        ab.gpt2_adamw(fake, fake, fake, fake, 10, 1e-3, 0.9, 0.95, 1e-8, 0.0, 0, stream=0)  # t starts at 1
     assert e.value.code == -1
