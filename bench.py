@@ -23,7 +23,8 @@ per step; rank 0 alone runs it.
 prefill of 32 prompts of 512 tokens (reported apart), then 128 greedy steps
 (argmax + gpt2_decode_step), K runs timed; value = decoded tokens/s.
 --gemm-diag adds each GEMM site's time beside cuBLAS at the same shape.
---attention-backward times one layer's attention backward (fp32) instead.
+--attention-forward / --attention-backward time one layer's attention
+forward (16-bit operands) / backward (fp32) instead.
 --train times whole training steps (forward, softmax cross-entropy,
 backward, AdamW; tf32 GEMMs, or fp32 with --precision fp32) instead.
 """
@@ -404,6 +405,50 @@ def attention_backward_flops(B, T, C, NH):
     return B * NH * (T * (T + 1) // 2) * 4 * 2 * hs
 
 
+ATTN_FWD_METRIC = "GPT-2 124M causal attention forward, one layer (B=16,T=1024,12 heads of 64), ms"
+
+
+def run_attention_forward(args, w):
+    """One layer's attention forward at the workload's shape through
+    attention_forward (16-bit operands per --precision; the call converts
+    the fp32 qkv to the operand type, then runs the attention kernel):
+    K timed calls after W warm-up calls; the attention kernel alone is
+    timed by the forward pass's stage profile."""
+    import torch
+    from gpt_transformer_forward_gb300 import binding as ab
+
+    rank, world, local, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    precision = ab.PRECISIONS[args.precision]
+    cfg, B, T = w.cfg, w.B, w.T
+    C, NH = cfg.channels, cfg.num_heads
+    qkv = torch.from_numpy(inputs.make_normal(803 + rank, (B, T, 3 * C), 0.55).astype("float32")).cuda()
+    out = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
+    wsz = ab.attention_workspace_size(B, T, C, precision)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        ab.attention_forward(out, qkv, B, T, C, NH, precision, ws, wsz)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ab.attention_forward(out, qkv, B, T, C, NH, precision, ws, wsz)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
+    line = {"metric": ATTN_FWD_METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": args.precision, "data": "synthetic",
+            "config": {"workload": w.name + "-attention-forward", "B": B, "T": T, "C": C, "heads": NH,
+                       "includes": "fp32 -> 16-bit conversion of qkv"},
+            "gpu_launches": 2 * args.steps, "device_error_word": ab.gpt2_get_error()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def run_attention_backward(args, w):
     """One layer's attention backward (fp32 CUDA cores) at the workload's
     shape: K timed calls after W warm-up calls, CUDA events on the stream."""
@@ -506,6 +551,8 @@ def run_ours(args):
     precision = ab.PRECISIONS[args.precision]
     if args.attention_backward:
         return run_attention_backward(args, w)
+    if args.attention_forward:
+        return run_attention_forward(args, w)
     if args.train:
         return run_train(args, w)
     if w.decode_steps:
@@ -658,6 +705,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--train", action="store_true",
                     help="time training steps (forward, loss, backward, AdamW) at the workload's shape instead")
+    ap.add_argument("--attention-forward", action="store_true",
+                    help="time one layer's attention_forward at the workload's shape instead")
     ap.add_argument("--attention-backward", action="store_true",
                     help="time one layer's attention backward (fp32) at the workload's shape instead")
     ap.add_argument("--gemm-diag", action="store_true",

@@ -830,6 +830,7 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
   float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
   float *part = buf(tl.part), *attn = buf(tl.attn);
+  void* qkv16 = dt;  // the tf32 mode's bf16 copy of one layer's qkv (the backward's scratch is free during the forward)
   const ParamOffsets po = param_offsets(cfg);
   auto P = [&](size_t off) { return params + off; };
   auto G = [&](size_t off) { return grads + off; };
@@ -841,7 +842,12 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
                          P(po.ln1w) + l * C, P(po.ln1b) + l * C, N, C, s);
     TRY(gemm(precision, qkv + l * 3 * NC, ln1 + l * NC, P(po.qkvw) + l * 3 * CC, P(po.qkvb) + l * 3 * C, N, 3 * C, C,
              kEpiF32, s));
-    TRY(launch_attention_f32(att + l * NC, qkv + l * 3 * NC, B, T, C, NH, s));
+    if (precision == GPT2_FP32) {
+      TRY(launch_attention_f32(att + l * NC, qkv + l * 3 * NC, B, T, C, NH, s));
+    } else {  // as in the forward pass's tf32 mode: the bf16 tensor-core kernel on a bf16 copy of qkv
+      to16(GPT2_BF16, qkv16, qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
+      TRY(launch_attention_16(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s));
+    }
     TRY(gemm(precision, proj, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, N, C, C, kEpiF32, s));
     launch_residual(xmid + l * NC, x, proj, static_cast<int>(NC), s);
     launch_layernorm_f32(ln2 + l * NC, ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N,

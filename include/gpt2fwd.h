@@ -294,7 +294,9 @@ GPT2_API size_t gpt2_train_workspace_size(const GPT2Config* cfg, int B, int T, i
  * (DEVICE).  Activations and gradients are fp32; the matmuls (and their
  * backward products) run on fp32 CUDA cores in GPT2_FP32 and on tcgen05
  * tensor cores with tf32 operands in GPT2_TF32 (then B*T % 4 == 0); the
- * attention's forward and backward run in fp32 on CUDA cores in both.
+ * attention's forward runs in fp32 on CUDA cores in GPT2_FP32 and on the
+ * bf16 tensor-core kernel in GPT2_TF32 (as gpt2_forward's tf32 mode), its
+ * backward in fp32 on CUDA cores in both.
  * Other precisions return GPT2_ERR_UNSUPPORTED.  The token-embedding
  * gradient sums repeated tokens with atomics: its last bits can vary from
  * run to run; every other element is deterministic.  A target outside

@@ -4,11 +4,12 @@ own position.
 
 - With a shuffled block table, paged decoding gives bitwise the logits of
   the dense cache (the arithmetic is the same; only where rows live
-  differs), at 80 sequences: more than 64 rows, so the decode GEMMs run on
-  the tensor-core tile kernel, not the small-M one.
-- Ragged batches: 128 sequences with prompts of 1..40 tokens prefilled
-  together (padded to 40), then decoded each at its own position, against
-  the oracle's full forward pass of each sequence (teacher-forced).
+  differs), at 80 and 256 sequences: more than 64 rows, so the decode GEMMs
+  run on the tensor-core tile kernel (one CTA, and CTA pairs past 128
+  rows), not the small-M one.
+- Ragged batches: 128 and 256 sequences with prompts of 1..40 tokens
+  prefilled together (padded to 40), then decoded each at its own position,
+  against the oracle's full forward pass of each sequence (teacher-forced).
 - GPT-2 124M width, 128 sequences (fp16): sampled sequences against the
   oracle.
 - Block-table entries and positions outside the cache are flagged on the
@@ -48,10 +49,11 @@ def paged(m, B, block_size, extra_blocks, seed):
     return ab.paged_kv(pool, table, num_blocks, block_size, max_blocks), (pool, table)
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_FP32])
-def test_paged_decode_equals_dense_bitwise(precision):
+@pytest.mark.parametrize("precision,B", [(ab.GPT2_FP16, 80), (ab.GPT2_FP32, 80), (ab.GPT2_FP16, 256)])
+def test_paged_decode_equals_dense_bitwise(precision, B):
+    # 80 rows: the tile GEMM's one-CTA form; 256 rows: its paired-CTA form
     cfg = inputs.TINY
-    B, P, steps = 80, 24, 8
+    P, steps = 24, 8
     params = inputs.make_params(cfg, 120, "perturbed")
     tok = inputs.make_tokens(121, B, P + steps, cfg.vocab_size)
     m = GPT2Model(cfg, params, B, P, precision)
@@ -73,11 +75,12 @@ def test_paged_decode_equals_dense_bitwise(precision):
     no_device_error()
 
 
-@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_BF16, ab.GPT2_FP32])
-@pytest.mark.parametrize("block_size", [16, 32])
-def test_paged_ragged_decode_matches_oracle(precision, block_size):
+@pytest.mark.parametrize("precision,block_size,B", [(ab.GPT2_FP16, 16, 128), (ab.GPT2_BF16, 16, 128),
+                                                    (ab.GPT2_FP32, 16, 128), (ab.GPT2_FP16, 32, 128),
+                                                    (ab.GPT2_FP32, 32, 128), (ab.GPT2_FP16, 16, 256)])
+def test_paged_ragged_decode_matches_oracle(precision, block_size, B):
     cfg = inputs.TINY
-    B, P, steps = 128, 40, 16
+    P, steps = 40, 16
     rng = np.random.default_rng(123)
     params = inputs.make_params(cfg, 124, "perturbed")
     tok = inputs.make_tokens(125, B, P + steps, cfg.vocab_size)
