@@ -394,7 +394,7 @@ def run_decode(args, w, precision):
         pg.destroy_process_group()
 
 
-ATTN_BWD_METRIC = "GPT-2 124M causal attention backward, one layer (B=16,T=1024,12 heads of 64), fp32, ms"
+ATTN_BWD_METRIC = "GPT-2 124M causal attention backward, one layer (B=16,T=1024,12 heads of 64), {}, ms"
 
 
 def attention_backward_flops(B, T, C, NH):
@@ -450,13 +450,17 @@ def run_attention_forward(args, w):
 
 
 def run_attention_backward(args, w):
-    """One layer's attention backward (fp32 CUDA cores) at the workload's
-    shape: K timed calls after W warm-up calls, CUDA events on the stream."""
+    """One layer's attention backward at the workload's shape through
+    attention_backward: fp32 CUDA cores with --precision fp32, else the bf16
+    tensor-core path (the call converts qkv and dout to bf16, reruns the
+    forward for the row statistic, then runs the two backward kernels).  K
+    timed calls after W warm-up calls, CUDA events on the stream."""
     import torch
     from gpt_transformer_forward_gb300 import binding as ab
 
     rank, world, local, pg = dist_setup(args.gpus)
     torch.cuda.set_device(local)
+    precision = ab.GPT2_FP32 if args.precision == "fp32" else ab.GPT2_BF16
     cfg, B, T = w.cfg, w.B, w.T
     C, NH = cfg.channels, cfg.num_heads
     qkv = torch.from_numpy(inputs.make_normal(801 + rank, (B, T, 3 * C), 0.55).astype("float32")).cuda()
@@ -464,26 +468,30 @@ def run_attention_backward(args, w):
     out = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
     ab.attention_forward(out, qkv, B, T, C, NH, ab.GPT2_FP32, None, 0)
     dqkv = torch.empty((B, T, 3 * C), dtype=torch.float32, device="cuda")
-    wsz = ab.attention_backward_workspace_size(B, T, C, NH)
+    wsz = ab.attention_backward_workspace_size(B, T, C, NH, precision)
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
     for _ in range(args.warmup):
-        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, ws, wsz)
+        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, precision, ws, wsz)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, ws, wsz)
+        ab.attention_backward(dqkv, dout, qkv, out, B, T, C, NH, precision, ws, wsz)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, pg, "cuda")
     flops = attention_backward_flops(B, T, C, NH)
-    line = {"metric": ATTN_BWD_METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": w.name + "-attention-backward", "B": B, "T": T, "C": C, "heads": NH},
+    f32 = precision == ab.GPT2_FP32
+    line = {"metric": ATTN_BWD_METRIC.format("fp32" if f32 else "bf16 tensor cores"), "value": ms, "unit": "ms",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32" if f32 else "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name + "-attention-backward", "B": B, "T": T, "C": C, "heads": NH,
+                       "includes": "the fp32 kernels" if f32 else
+                       "qkv and dout to bf16, the forward rerun for the row statistic, dO prep, dK/dV and dQ"},
             "tflops": flops / (ms * 1e-3) / 1e12, "algorithmic_flops": flops,
-            "gpu_launches": 3 * args.steps, "device_error_word": ab.gpt2_get_error()}
+            "gpu_launches": (3 if f32 else 5) * args.steps, "device_error_word": ab.gpt2_get_error()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg is not None:
@@ -708,7 +716,8 @@ def main():
     ap.add_argument("--attention-forward", action="store_true",
                     help="time one layer's attention_forward at the workload's shape instead")
     ap.add_argument("--attention-backward", action="store_true",
-                    help="time one layer's attention backward (fp32) at the workload's shape instead")
+                    help="time one layer's attention backward at the workload's shape instead (fp32 with --precision fp32, "
+                         "else bf16 tensor cores)")
     ap.add_argument("--gemm-diag", action="store_true",
                     help="add each GEMM site's time beside cuBLAS at the same shape (diagnostic)")
     args = ap.parse_args()

@@ -66,8 +66,8 @@ _SIGNATURES = {
     "matmul_forward_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P]),
     "attention_workspace_size": (_Z, [_I, _I, _I, _I]),
     "attention_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
-    "attention_backward_workspace_size": (_Z, [_I, _I, _I, _I]),
-    "attention_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _Z, _P]),
+    "attention_backward_workspace_size": (_Z, [_I, _I, _I, _I, _I]),
+    "attention_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _Z, _P]),
     "gelu_forward": (_I, [_P, _P, _I, _P]),
     "residual_forward": (_I, [_P, _P, _P, _I, _P]),
     "softmax_forward": (_I, [_P, _P, _I, _I, _I, _P]),
@@ -197,13 +197,13 @@ def attention_forward(out, qkv, B, T, C, NH, precision, workspace=None, ws_bytes
                                                          _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def attention_backward_workspace_size(B, T, C, NH) -> int:
-    return _lib().attention_backward_workspace_size(B, T, C, NH)
+def attention_backward_workspace_size(B, T, C, NH, precision) -> int:
+    return _lib().attention_backward_workspace_size(B, T, C, NH, precision)
 
 
-def attention_backward(dqkv, dout, qkv, out, B, T, C, NH, workspace=None, ws_bytes=0, stream=None):
+def attention_backward(dqkv, dout, qkv, out, B, T, C, NH, precision, workspace=None, ws_bytes=0, stream=None):
     _check("attention_backward", _lib().attention_backward(_ptr(dqkv), _ptr(dout), _ptr(qkv), _ptr(out), B, T, C, NH,
-                                                           _ptr(workspace), ws_bytes, _stream(stream)))
+                                                           precision, _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def gelu_forward(out, inp, n, stream=None):

@@ -286,7 +286,7 @@ struct StageProfiler {
 // scratch; offsets in bytes, each 256-byte aligned.
 struct TrainLayout {
   size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj, dx,
-      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, total;
+      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, total;
 };
 
 TrainLayout train_layout(const GPT2Config* c, int B, int T) {
@@ -327,7 +327,8 @@ TrainLayout train_layout(const GPT2Config* c, int B, int T) {
   t.tB = take(4 * NC);
   t.Wt = take(wide * C);
   t.part = take(2 * static_cast<size_t>(column_parts(static_cast<int>(N))) * wide);
-  t.attn = take(2 * static_cast<size_t>(B) * c->num_heads * T);
+  t.attn = take(2 * static_cast<size_t>(B) * c->num_heads * attn_bwd_padded_len(T));
+  t.lse = take(L * static_cast<size_t>(B) * c->num_heads * attn_bwd_padded_len(T));
   t.total = p;
   return t;
 }
@@ -415,25 +416,61 @@ int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH,
   return check_launch();
 }
 
-size_t attention_backward_workspace_size(int B, int T, int C, int NH) {
-  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0) return 0;
-  return 2 * round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256);
+// the 16-bit backward's workspace: bf16 copies of qkv and dout, the bf16
+// output of the forward recompute that yields the row statistic, then the
+// statistic L and rowsum(dout * out), [B][NH][Tp] each
+struct AttnBwd16Layout {
+  size_t qkv16, do16, o16, lse, dvec, total;
+};
+AttnBwd16Layout attn_bwd16_layout(int B, int T, int C, int NH) {
+  const size_t N = static_cast<size_t>(B) * T, S = static_cast<size_t>(B) * NH * attn_bwd_padded_len(T);
+  AttnBwd16Layout l;
+  l.qkv16 = 0;
+  l.do16 = l.qkv16 + round_up(N * 3 * C * 2, 256);
+  l.o16 = l.do16 + round_up(N * C * 2, 256);
+  l.lse = l.o16 + round_up(N * C * 2, 256);
+  l.dvec = l.lse + round_up(S * sizeof(float), 256);
+  l.total = l.dvec + round_up(S * sizeof(float), 256);
+  return l;
+}
+
+size_t attention_backward_workspace_size(int B, int T, int C, int NH, int precision) {
+  if (B <= 0 || T <= 0 || C <= 0 || NH <= 0 || C % NH != 0) return 0;
+  if (precision == GPT2_FP32) return 2 * round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256);
+  if ((precision == GPT2_TF32 || precision == GPT2_BF16) && C / NH == 64) return attn_bwd16_layout(B, T, C, NH).total;
+  return 0;
 }
 
 int attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, int B, int T, int C, int NH,
-                       void* workspace, size_t ws_bytes, void* stream) {
+                       int precision, void* workspace, size_t ws_bytes, void* stream) {
   RETURN_IF(!dqkv || !dout || !qkv || !out, GPT2_ERR_ARG);
-  RETURN_IF(B < 0 || T < 0 || C <= 0 || NH <= 0, GPT2_ERR_ARG);
+  RETURN_IF(B < 0 || T < 0 || C <= 0 || NH <= 0 || !valid_precision(precision), GPT2_ERR_ARG);
   RETURN_IF(C % NH != 0, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(C, NH));
+  // the 16-bit path: bf16 operands (the gradients need bf16's exponent
+  // range), head size 64
+  RETURN_IF(precision == GPT2_FP16 || (precision != GPT2_FP32 && C / NH != 64), GPT2_ERR_UNSUPPORTED);
   if (B == 0 || T == 0) return GPT2_OK;
-  RETURN_IF(workspace == nullptr || ws_bytes < attention_backward_workspace_size(B, T, C, NH), GPT2_ERR_WORKSPACE);
+  RETURN_IF(workspace == nullptr || ws_bytes < attention_backward_workspace_size(B, T, C, NH, precision),
+            GPT2_ERR_WORKSPACE);
   RETURN_IF(!aligned16(dqkv) || !aligned16(dout) || !aligned16(qkv) || !aligned16(out) || !aligned16(workspace),
             GPT2_ERR_ALIGN);
-  float* Lrow = static_cast<float*>(workspace);
-  float* Drow = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                         round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256));
-  TRY(launch_attention_backward(dqkv, dout, qkv, out, Lrow, Drow, B, T, C, NH, as_stream(stream)));
+  cudaStream_t s = as_stream(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (precision == GPT2_FP32) {
+    float* Lrow = reinterpret_cast<float*>(ws);
+    float* Drow = reinterpret_cast<float*>(ws + round_up(static_cast<size_t>(B) * NH * T * sizeof(float), 256));
+    TRY(launch_attention_backward(dqkv, dout, qkv, out, Lrow, Drow, B, T, C, NH, s));
+    return check_launch();
+  }
+  const AttnBwd16Layout l = attn_bwd16_layout(B, T, C, NH);
+  float* lse = reinterpret_cast<float*>(ws + l.lse);
+  float* dvec = reinterpret_cast<float*>(ws + l.dvec);
+  to16(GPT2_BF16, ws + l.qkv16, qkv, static_cast<long long>(B) * T * 3 * C, s);
+  // the forward again, for each row's log-sum-exp (its output is not used)
+  TRY(launch_attention_tc05(ws + l.o16, true, ws + l.qkv16, kOpBF16, B, T, C, NH, s, lse));
+  launch_attn_bwd_prep(ws + l.do16, dvec, lse, dout, out, B, T, C, NH, s);
+  TRY(launch_attention_backward_tc05(dqkv, ws + l.qkv16, ws + l.do16, lse, dvec, B, T, C, NH, s));
   return check_launch();
 }
 
@@ -829,8 +866,15 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   float *lnf = buf(tl.lnf), *lnfm = buf(tl.lnfm), *lnfr = buf(tl.lnfr), *logits = buf(tl.logits);
   float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
   float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
-  float *part = buf(tl.part), *attn = buf(tl.attn);
-  void* qkv16 = dt;  // the tf32 mode's bf16 copy of one layer's qkv (the backward's scratch is free during the forward)
+  float *part = buf(tl.part), *attn = buf(tl.attn), *lse = buf(tl.lse);
+  // the tf32 mode's bf16 copy of one layer's qkv, and of the attention
+  // output's gradient, in the backward's scratch (free while they are used)
+  void* qkv16 = dt;
+  void* do16 = ws + tl.dt + round_up(3 * NC * 2, 256);
+  // tf32 with head size 64: attention forward and backward on tcgen05, the
+  // forward keeping each row's log-sum-exp (per layer) for the backward
+  const bool attn_tc = precision == GPT2_TF32 && C / NH == 64;
+  const size_t SL = static_cast<size_t>(B) * NH * attn_bwd_padded_len(T);
   const ParamOffsets po = param_offsets(cfg);
   auto P = [&](size_t off) { return params + off; };
   auto G = [&](size_t off) { return grads + off; };
@@ -846,7 +890,10 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
       TRY(launch_attention_f32(att + l * NC, qkv + l * 3 * NC, B, T, C, NH, s));
     } else {  // as in the forward pass's tf32 mode: the bf16 tensor-core kernel on a bf16 copy of qkv
       to16(GPT2_BF16, qkv16, qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
-      TRY(launch_attention_16(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s));
+      if (attn_tc)
+        TRY(launch_attention_tc05(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s, lse + l * SL));
+      else
+        TRY(launch_attention_16(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s));
     }
     TRY(gemm(precision, proj, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, N, C, C, kEpiF32, s));
     launch_residual(xmid + l * NC, x, proj, static_cast<int>(NC), s);
@@ -891,8 +938,14 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
                               ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N, N, C, true, s);
     // x_mid = x_in + attproj(attention(qkv(LN1(x_in)))); dx = dL/dx_mid
     TRY(mm_bwd(dh, G(po.attprojw) + l * CC, G(po.attprojb) + l * C, dx, att + l * NC, P(po.attprojw) + l * CC, C, C));
-    TRY(launch_attention_backward(dqkv, dh, qkv + l * 3 * NC, att + l * NC, attn,
-                                  attn + static_cast<size_t>(B) * NH * T, B, T, C, NH, s));
+    if (attn_tc) {
+      to16(GPT2_BF16, qkv16, qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
+      launch_attn_bwd_prep(do16, attn, lse + l * SL, dh, att + l * NC, B, T, C, NH, s);
+      TRY(launch_attention_backward_tc05(dqkv, qkv16, do16, lse + l * SL, attn, B, T, C, NH, s));
+    } else {
+      TRY(launch_attention_backward(dqkv, dh, qkv + l * 3 * NC, att + l * NC, attn,
+                                    attn + static_cast<size_t>(B) * NH * T, B, T, C, NH, s));
+    }
     TRY(mm_bwd(dh, G(po.qkvw) + l * 3 * CC, G(po.qkvb) + l * 3 * C, dqkv, ln1 + l * NC, P(po.qkvw) + l * 3 * CC,
                3 * C, C));
     launch_layernorm_backward(dx, G(po.ln1w) + l * C, G(po.ln1b) + l * C, part, dh, xin + l * NC, P(po.ln1w) + l * C,

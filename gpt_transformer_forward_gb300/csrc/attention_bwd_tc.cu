@@ -1,0 +1,512 @@
+// attention_bwd_tc.cu -- the backward pass of causal attention on the
+// sm_103a tensor cores (tcgen05, TMEM, TMA), head size 64, bf16 operands
+// and fp32 accumulation ("Understand FlashAttention (II)": the backward of
+// Algorithm 1, P recomputed tile by tile from the forward's row statistic).
+//
+// With S = Q K^T / sqrt(64) (causal), P = softmax_rows(S), O = P V and the
+// incoming gradient dO:
+//   dV = P^T dO,  dP = dO V^T,  dS = P (dP - D),  D[t] = sum_d dO[t][d] O[t][d],
+//   dQ = dS K / sqrt(64),  dK = dS^T Q / sqrt(64),
+// and P = exp2(S log2(e) - L) from L = m + log2(l), the log-sum-exp of the
+// forward's softmax in log2 units (written by the forward kernel).  The
+// factor 1/sqrt(64) = 2^-3 is applied to dS before it is rounded to bf16
+// (exact: a power of two).
+//
+// Two kernels, each a CTA (one per SM) over one 128-row tile of one
+// (sequence, head), so that every gradient element is accumulated in one
+// place and written once (no atomics; results do not depend on timing):
+//   dK/dV  per key tile j: streams the query tiles i >= j (Q_i, dO_i and
+//          their L and D), computes S^T = K Q_i^T and dP^T = V dO_i^T in
+//          TMEM, P^T and dS^T (rows = keys) into shared memory, and
+//          accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM;
+//   dQ     per query tile i: streams the key tiles j <= i (K_j, V_j),
+//          computes S = Q K_j^T and dP = dO V_j^T, dS into shared memory,
+//          and accumulates dQ += dS K_j.
+// In both, the "fixed" pair of tiles (K, V or Q, dO) stays in shared memory
+// and the "streamed" pair (Q_i, dO_i or K_j, V_j) passes through a ring of
+// three stages; the products are then uniform:
+//   S  = fixed0 stream0^T,  dP = fixed1 stream1^T          (K-major operands)
+//   dV += P^T stream1,  dK += dS^T stream0,  dQ += dS stream0   (stream tiles
+//                                                    as MN-major B operands)
+// Roles: warp 0 loads (TMA), warp 1 owns TMEM and issues the MMAs (one
+// elected lane), warps 2-9 compute P and dS, one row per thread and half of
+// the 128 columns per warp (two warps per TMEM lane quadrant).  TMEM: two S
+// buffers (S of tile u + 2 is issued while tile u + 1 is processed), one dP
+// buffer, the accumulators.  The softmax warps first turn S into P (kept
+// in fp32 registers; stored as bf16 for dV), then wait for dP and form dS,
+// so the dP product overlaps the exponentials.
+// Every wait is bounded; a timeout sets the device error word and the CTA
+// drains its copies and MMAs, frees TMEM and returns.
+#include "kernels.cuh"
+
+namespace gpt2 {
+namespace {
+
+constexpr int kR = 128;               // rows of a tile (keys or queries) = TMEM lanes
+constexpr int kHS = 64;               // head size
+constexpr int kTile = kR * kHS * 2;   // 16 KB: 128 rows of 128 bytes
+constexpr int kSq = kR * kR * 2;      // 32 KB: a 128 x 128 bf16 operand, two 64-column swizzle atoms
+constexpr int kStages = 3;
+constexpr int kSmWarps = 8;
+constexpr int kThreads = 64 + 32 * kSmWarps;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;         // S buffers 0 and 1 (128 columns each)
+constexpr uint32_t kTmemDP = 2 * kR;   // dP
+constexpr uint32_t kTmemAcc = 3 * kR;  // dV (64 columns) then dK (64), or dQ (64)
+constexpr uint32_t kIdescS = make_idesc(1u, kR, kR);                  // bf16, 128 x 128, both K-major
+constexpr uint32_t kIdescAcc = make_idesc(1u, kR, kHS) | (1u << 16);  // 128 x 64, B MN-major
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool kDQ>
+struct BwdSmem {
+  static constexpr int fixed = 0;                                 // two tiles
+  static constexpr int stage = fixed + 2 * kTile;                 // kStages x two tiles
+  static constexpr int p = stage + kStages * 2 * kTile;           // P^T (dK/dV kernel)
+  static constexpr int ds = p + (kDQ ? 0 : kSq);                  // dS^T or dS
+  static constexpr int stats = ds + kSq;                          // dK/dV: kStages x (L[128], D[128])
+  static constexpr int bars = stats + (kDQ ? 0 : kStages * 2 * kR * 4);
+  // fixed_full; st_full[kStages], st_empty[kStages]; s_full[2]; dp_full,
+  // p_full, ds_full, p_empty, ds_empty, acc_done, drain
+  static constexpr int n_bars = 1 + 2 * kStages + 2 + 7;
+  static constexpr int misc = bars + n_bars * 8;
+  static constexpr int total = misc + 16;
+  static constexpr int alloc = total + 1024;
+};
+static_assert(BwdSmem<false>::alloc <= 232448 && BwdSmem<true>::alloc <= 232448, "shared memory budget");
+
+// D = A B^T over the 64 head dimensions: A, B K-major 128-row tiles
+__device__ __forceinline__ void mma_dim(uint32_t d, uint32_t a_addr, uint32_t b_addr) {
+  const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128(b_addr);
+#pragma unroll
+  for (int kk = 0; kk < kHS / 16; ++kk)  // 16 dimensions = 32 bytes = 2 in the address field
+    tc_mma_warp<false>(d, ad + 2 * kk, bd + 2 * kk, kIdescS, kk > 0 ? 1u : 0u);
+}
+
+// D (+)= A B over 128 rows: A a 128 x 128 K-major operand in two swizzle
+// atoms, B a 128-row tile read MN-major (64 contiguous head dimensions per
+// row of K)
+__device__ __forceinline__ void mma_rows(uint32_t d, uint32_t a_addr, uint32_t b_addr, bool first) {
+  const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128_mn(b_addr, 1024);
+#pragma unroll
+  for (int kk = 0; kk < kR / 16; ++kk)  // A: 16 columns = 32 bytes of a 64-column atom; B: 16 rows of 128 bytes
+    tc_mma_warp<false>(d, ad + ((kk >> 2) * (kSq / 2) + (kk & 3) * 32) / 16, bd + kk * (2048 / 16), kIdescAcc,
+                       (!first || kk > 0) ? 1u : 0u);
+}
+
+// kDQ = false: the dK/dV kernel (blockIdx.x = key tile, longest first);
+// kDQ = true: the dQ kernel (blockIdx.x counts query tiles from the last).
+// qkv map: [B][T][3C] bf16, do map: [B][T][C] bf16, boxes of 64 x 128 with
+// the 128-byte swizzle.  Lse, Dv: [B][NH][Tp] fp32, Tp = T rounded up to 128,
+// zero past T.
+template <bool kDQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ CUtensorMap tmap_do,
+                         float* __restrict__ dqkv, const float* __restrict__ Lse, const float* __restrict__ Dv, int T,
+                         int C, int Tp, float scale_log2, float ds_scale) {
+  using L = BwdSmem<kDQ>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
+  uint64_t* fixed_full = bars;
+  uint64_t* st_full = bars + 1;           // [kStages] a streamed tile pair (and its L, D) landed
+  uint64_t* st_empty = st_full + kStages; // [kStages] its last reader is done
+  uint64_t* s_full = st_empty + kStages;  // [2] S of tile u in buffer u % 2
+  uint64_t* dp_full = s_full + 2;         // dP of tile u (phase u % 2)
+  uint64_t* p_full = dp_full + 1;         // the softmax warps have read S (and written P^T) of tile u
+  uint64_t* ds_full = p_full + 1;         // ... read dP and written dS of tile u
+  uint64_t* p_empty = ds_full + 1;        // dV of tile u has read P^T
+  uint64_t* ds_empty = p_empty + 1;       // dK / dQ of tile u has read dS
+  uint64_t* acc_done = ds_empty + 1;      // the accumulators are final
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (T + kR - 1) / kR;
+  const int h = blockIdx.y, b = blockIdx.z, NH = gridDim.y;
+  // fixed tile index; streamed tiles: dK/dV: i = ft + u, u < n_tiles - ft;
+  // dQ: j = u, u <= ft
+  const int ft = kDQ ? n_tiles - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+  const int n = kDQ ? ft + 1 : n_tiles - ft;
+  const size_t bh = static_cast<size_t>(b) * NH + h;
+
+  if (threadIdx.x == 0) {
+    mbar_init(fixed_full, 1u);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&st_full[i], 1u);
+      mbar_init(&st_empty[i], 1u);
+    }
+    mbar_init(&s_full[0], 1u);
+    mbar_init(&s_full[1], 1u);
+    mbar_init(dp_full, 1u);
+    mbar_init(p_full, kSmWarps);
+    mbar_init(ds_full, kSmWarps);
+    mbar_init(p_empty, 1u);
+    mbar_init(ds_empty, 1u);
+    mbar_init(acc_done, 1u);
+    mbar_init(drain, 1u);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmap_qkv);
+    tma_prefetch_desc(&tmap_do);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ loads
+    if (lane == 0) {
+      // fixed: K_j, V_j (dK/dV) or Q_i, dO_i (dQ)
+      mbar_arrive_expect_tx(fixed_full, 2 * kTile);
+      if (!kDQ) {
+        tma_load_3d(smem + L::fixed, &tmap_qkv, fixed_full, C + h * kHS, ft * kR, b);
+        tma_load_3d(smem + L::fixed + kTile, &tmap_qkv, fixed_full, 2 * C + h * kHS, ft * kR, b);
+      } else {
+        tma_load_3d(smem + L::fixed, &tmap_qkv, fixed_full, h * kHS, ft * kR, b);
+        tma_load_3d(smem + L::fixed + kTile, &tmap_do, fixed_full, h * kHS, ft * kR, b);
+      }
+      uint32_t filled = 0, par = 0;  // per stage: ever filled; parity of the last fill
+      for (int u = 0; u < n && !*abort_flag; ++u) {
+        const int st = u % kStages;
+        const uint32_t ph = (u / kStages) & 1;
+        if (!mbar_wait(&st_empty[st], ph ^ 1)) {
+          *abort_flag = 1;
+          break;
+        }
+        uint8_t* dst = smem + L::stage + st * 2 * kTile;
+        if (!kDQ) {  // Q_i, dO_i, L and D of query tile i
+          const int i = ft + u;
+          mbar_arrive_expect_tx(&st_full[st], 2 * kTile + 2 * kR * 4);
+          tma_load_3d(dst, &tmap_qkv, &st_full[st], h * kHS, i * kR, b);
+          tma_load_3d(dst + kTile, &tmap_do, &st_full[st], h * kHS, i * kR, b);
+          float* sd = reinterpret_cast<float*>(smem + L::stats) + st * 2 * kR;
+          bulk_load(sd, Lse + bh * Tp + static_cast<size_t>(i) * kR, kR * 4, &st_full[st]);
+          bulk_load(sd + kR, Dv + bh * Tp + static_cast<size_t>(i) * kR, kR * 4, &st_full[st]);
+        } else {  // K_j, V_j
+          mbar_arrive_expect_tx(&st_full[st], 2 * kTile);
+          tma_load_3d(dst, &tmap_qkv, &st_full[st], C + h * kHS, u * kR, b);
+          tma_load_3d(dst + kTile, &tmap_qkv, &st_full[st], 2 * C + h * kHS, u * kR, b);
+        }
+        filled |= 1u << st;
+        par = (par & ~(1u << st)) | (ph << st);
+      }
+      // the copies issued here land before the CTA may exit: this thread
+      // alone arms the full barriers, so the phase of a stage's last fill
+      // completes exactly when its bytes have landed
+      mbar_wait(fixed_full, 0);
+      for (int st = 0; st < kStages; ++st)
+        if ((filled >> st) & 1u) mbar_wait(&st_full[st], (par >> st) & 1u);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMAs
+    const uint32_t fixed0 = smem_u32(smem + L::fixed), fixed1 = fixed0 + kTile;
+    const uint32_t p_addr = smem_u32(smem + L::p), ds_addr = smem_u32(smem + L::ds);
+    auto stream0 = [&](int u) { return smem_u32(smem + L::stage + (u % kStages) * 2 * kTile); };
+    auto stream1 = [&](int u) { return stream0(u) + kTile; };
+    auto wait_stage = [&](int u) {
+      return __all_sync(0xffffffffu, mbar_wait(&st_full[u % kStages], (u / kStages) & 1));
+    };
+    auto issue_s = [&](int u) {  // S of tile u into buffer u % 2
+      tc_fence_after();
+      mma_dim(tmem + kTmemS + (u & 1) * kR, fixed0, stream0(u));
+      tc_commit_warp(&s_full[u & 1]);
+    };
+    auto issue_dp = [&](int u) {
+      mma_dim(tmem + kTmemDP, fixed1, stream1(u));
+      tc_commit_warp(dp_full);
+    };
+    bool ok = __all_sync(0xffffffffu, mbar_wait(fixed_full, 0));
+    if (ok) ok = wait_stage(0);
+    if (ok) {
+      issue_s(0);
+      issue_dp(0);
+    }
+    if (ok && n > 1) ok = wait_stage(1);
+    if (ok && n > 1) issue_s(1);
+    for (int u = 0; u < n && ok; ++u) {
+      if (!kDQ) {
+        // dV += P^T dO_i once P^T is written (S of tile u has been read:
+        // its buffer takes S of tile u + 2)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, u & 1)))) break;
+        tc_fence_after();
+        mma_rows(tmem + kTmemAcc, p_addr, stream1(u), u == 0);
+        tc_commit_warp(p_empty);
+        if (u + 2 < n) {
+          if (!(ok = wait_stage(u + 2))) break;
+          issue_s(u + 2);
+        }
+      }
+      // dS written and dP read: dP of the next tile, then dK += dS^T Q_i
+      // (or dQ += dS K_j)
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_full, u & 1)))) break;
+      tc_fence_after();
+      if (u + 1 < n) issue_dp(u + 1);
+      mma_rows(tmem + kTmemAcc + (kDQ ? 0 : kHS), ds_addr, stream0(u), u == 0);
+      tc_commit_warp(ds_empty);
+      tc_commit_warp(&st_empty[u % kStages]);
+      if (u == n - 1) tc_commit_warp(acc_done);
+      if (kDQ && u + 2 < n) {  // S of tile u was read before dS was formed
+        if (!(ok = wait_stage(u + 2))) break;
+        issue_s(u + 2);
+      }
+    }
+    if (!ok && lane == 0) *abort_flag = 1;
+    tc_commit_warp(drain);
+    mbar_wait(drain, 0);
+  } else {
+    // ------------------------------------------------------- P and dS
+    const int sw = warp - 2;
+    const int qw = warp & 3;        // TMEM lane quadrant this warp may access
+    const int hf = sw >> 2;         // columns [64 hf, 64 hf + 64)
+    const int row = qw * 32 + lane; // row of the tile = TMEM lane
+    const int col0 = hf * 64;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    float l_row = 0.f, d_row = 0.f;  // dQ kernel: the row's L and D
+    if (kDQ) {
+      const size_t at = bh * Tp + static_cast<size_t>(ft) * kR + row;
+      l_row = __ldg(Lse + at);
+      d_row = __ldg(Dv + at);
+    }
+    // stores 64 bf16 values (32 packed pairs) of this thread's row into a
+    // 128 x 128 K-major operand: the row's half hf is swizzle atom hf
+    auto store_row = [&](uint8_t* base, const uint32_t(&pk)[32]) {
+      uint8_t* prow = base + hf * (kSq / 2) + row * 128;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
+            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+    };
+    bool ok = true;
+    for (int u = 0; u < n; ++u) {
+      const int sb = u & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (u >> 1) & 1)))) break;
+      const float* stats = nullptr;  // dK/dV: L and D of the query tile, per column
+      if (!kDQ) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&st_full[u % kStages], (u / kStages) & 1))))
+          break;  // (complete already: S of tile u was issued after it)
+        stats = reinterpret_cast<const float*>(smem + L::stats) + (u % kStages) * 2 * kR;
+      }
+      tc_fence_after();
+      // visible columns [lo, hi) of this row
+      int lo, hi;
+      if (!kDQ) {  // row = key ft * 128 + row; column = query (ft + u) * 128 + c: c >= row on the diagonal, < T
+        lo = u == 0 ? row : 0;
+        hi = min(T - (ft + u) * kR, kR);
+      } else {  // row = query ft * 128 + row; column = key u * 128 + c <= query
+        lo = 0;
+        hi = max(0, min(ft * kR + row - u * kR + 1, kR));
+      }
+      const bool all_valid = lo <= col0 && hi >= col0 + 64;
+      uint32_t sv[2][32];
+      tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0, sv[0]);
+      tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0 + 32, sv[1]);
+      tmem_ld_wait();
+      // P = exp2(S log2(e)/8 - L), zero outside [lo, hi); kept in sv as fp32
+      const float2 sc = make_float2(scale_log2, scale_log2);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 nl;
+          if (kDQ) {
+            nl = make_float2(-l_row, -l_row);
+          } else {
+            const float2 lv = *reinterpret_cast<const float2*>(stats + col0 + c * 32 + e);
+            nl = make_float2(-lv.x, -lv.y);
+          }
+          float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sc, nl);
+          if (!all_valid) {
+            const int cc = col0 + c * 32 + e;
+            if (cc < lo || cc >= hi) x.x = -INFINITY;
+            if (cc + 1 < lo || cc + 1 >= hi) x.y = -INFINITY;
+          }
+          sv[c][e] = __float_as_uint(ex2(x.x));
+          sv[c][e + 1] = __float_as_uint(ex2(x.y));
+        }
+      }
+      if (!kDQ) {
+        // P^T into shared memory for dV (its buffer is free once dV of the
+        // previous tile has read it)
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(sv[e >> 4][(e & 15) * 2]), __uint_as_float(sv[e >> 4][(e & 15) * 2 + 1]));
+        if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(p_empty, (u - 1) & 1)))) break;
+        store_row(smem + L::p, pk);
+        fence_proxy_async_smem();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (!kDQ && lane == 0) mbar_arrive(p_full);
+      // dS = P (dP - D) / 8
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1)))) break;
+      tc_fence_after();
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dv[32];
+        tmem_ld_32x32b_x32(lane_base + kTmemDP + col0 + c * 32, dv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float2 d2;
+          if (kDQ) {
+            d2 = make_float2(d_row, d_row);
+          } else {
+            d2 = *reinterpret_cast<const float2*>(stats + kR + col0 + c * 32 + e);
+          }
+          const float g0 = (__uint_as_float(dv[e]) - d2.x) * ds_scale;
+          const float g1 = (__uint_as_float(dv[e + 1]) - d2.y) * ds_scale;
+          pk[c * 16 + e / 2] = pack_bf16x2(__uint_as_float(sv[c][e]) * g0, __uint_as_float(sv[c][e + 1]) * g1);
+        }
+      }
+      if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (u - 1) & 1)))) break;
+      store_row(smem + L::ds, pk);
+      fence_proxy_async_smem();  // dS written by this thread becomes visible to the MMA
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0));
+    if (ok) {
+      tc_fence_after();
+      // dK/dV: warps of half 0 write dV, half 1 dK (64 columns each); dQ:
+      // each half 32 of dQ's columns
+      const int r_glob = ft * kR + row;
+      const int n_chunks = kDQ ? 1 : 2;
+      const uint32_t t_col = kTmemAcc + (kDQ ? hf * 32 : hf * kHS);
+      const int g_col = kDQ ? h * kHS + hf * 32 : (hf == 0 ? 2 * C : C) + h * kHS;
+#pragma unroll 1
+      for (int c = 0; c < n_chunks; ++c) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(lane_base + t_col + c * 32, o);
+        tmem_ld_wait();
+        if (r_glob < T) {
+          float* dst = dqkv + (static_cast<size_t>(b) * T + r_glob) * 3 * C + g_col + c * 32;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<uint4*>(dst)[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dO [B,T,C] fp32 -> bf16 copy; D[b][h][t] = sum over the head's 64
+// columns of dO * O; D and L are zero for t in [T, Tp).  Eight threads per
+// head and row, eight columns each.
+__global__ void attn_bwd_prep_kernel(__nv_bfloat16* __restrict__ do16, float* __restrict__ Dv, float* __restrict__ Lse,
+                                     const float* __restrict__ dout, const float* __restrict__ out, int B, int T, int C,
+                                     int NH, int Tp) {
+  const long long per_row = C / 8;
+  const long long total = static_cast<long long>(B) * Tp * per_row;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool live = idx < total;
+  const long long r = live ? idx / per_row : 0;
+  const int c8 = live ? static_cast<int>(idx % per_row) : 0;
+  const int b = static_cast<int>(r / Tp), t = static_cast<int>(r % Tp);
+  float dot = 0.f;
+  if (live && t < T) {
+    const size_t at = (static_cast<size_t>(b) * T + t) * C + c8 * 8;
+    const float4 g0 = *reinterpret_cast<const float4*>(dout + at), g1 = *reinterpret_cast<const float4*>(dout + at + 4);
+    const float4 o0 = *reinterpret_cast<const float4*>(out + at), o1 = *reinterpret_cast<const float4*>(out + at + 4);
+    dot = g0.x * o0.x + g0.y * o0.y + g0.z * o0.z + g0.w * o0.w + g1.x * o1.x + g1.y * o1.y + g1.z * o1.z +
+          g1.w * o1.w;
+    *reinterpret_cast<uint4*>(do16 + at) =
+        make_uint4(pack_bf16x2(g0.x, g0.y), pack_bf16x2(g0.z, g0.w), pack_bf16x2(g1.x, g1.y), pack_bf16x2(g1.z, g1.w));
+  }
+  // the eight threads of a head are eight aligned lanes of one warp
+  dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+  dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+  dot += __shfl_xor_sync(0xffffffffu, dot, 4);
+  if (live && (c8 & 7) == 0) {
+    const size_t at = (static_cast<size_t>(b) * NH + c8 / 8) * Tp + t;
+    Dv[at] = dot;
+    if (t >= T) Lse[at] = 0.f;
+  }
+}
+
+template <bool kDQ>
+int set_smem_attr() {
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
+  if (!attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc05_kernel<kDQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               BwdSmem<kDQ>::alloc);
+    if (e != cudaSuccess) return note_cuda_error(e);
+    attr_set[dev] = true;
+  }
+  return GPT2_OK;
+}
+
+}  // namespace
+
+int attn_bwd_padded_len(int T) { return (T + kR - 1) / kR * kR; }
+
+void launch_attn_bwd_prep(void* do16, float* Dv, float* Lse, const float* dout, const float* out, int B, int T, int C,
+                          int NH, cudaStream_t s) {
+  const int Tp = attn_bwd_padded_len(T);
+  const long long total = static_cast<long long>(B) * Tp * (C / 8);
+  const int threads = 256;
+  attn_bwd_prep_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, s>>>(
+      static_cast<__nv_bfloat16*>(do16), Dv, Lse, dout, out, B, T, C, NH, Tp);
+}
+
+int launch_attention_backward_tc05(float* dqkv, const void* qkv16, const void* do16, const float* Lse,
+                                   const float* Dv, int B, int T, int C, int NH, cudaStream_t s) {
+  if (C / NH != kHS || C % 8 != 0) return GPT2_ERR_UNSUPPORTED;
+  int rc = set_smem_attr<false>();
+  if (rc == GPT2_OK) rc = set_smem_attr<true>();
+  if (rc != GPT2_OK) return rc;
+  CUtensorMap map_qkv, map_do;
+  const uint32_t box[3] = {kHS, kR, 1};
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(3 * C), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(3 * C) * 2, static_cast<uint64_t>(T) * 3 * C * 2};
+    if (!encode_tensor_map(&map_qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, qkv16, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return GPT2_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(C), static_cast<uint64_t>(T), static_cast<uint64_t>(B)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(C) * 2, static_cast<uint64_t>(T) * C * 2};
+    if (!encode_tensor_map(&map_do, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, do16, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+      return GPT2_ERR_CUDA;
+  }
+  const int Tp = attn_bwd_padded_len(T);
+  const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
+  const float ds_scale = 0.125f;                        // 1 / sqrt(64)
+  const dim3 grid((T + kR - 1) / kR, NH, B);
+  attn_bwd_tc05_kernel<false><<<grid, kThreads, BwdSmem<false>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
+                                                                            scale_log2, ds_scale);
+  attn_bwd_tc05_kernel<true><<<grid, kThreads, BwdSmem<true>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
+                                                                          scale_log2, ds_scale);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
+}
+
+}  // namespace gpt2

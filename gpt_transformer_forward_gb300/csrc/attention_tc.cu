@@ -102,8 +102,8 @@ struct Schedule {
 // holding three warps caps a thread at 168 registers.
 template <typename T16, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, OutT* __restrict__ out, int T, int C,
-                     float scale_log2) {
+    attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, OutT* __restrict__ out, float* __restrict__ lse,
+                     int T, int C, int Tp, float scale_log2) {
   using L = Smem;
   constexpr int kKV = L::kKV;
   extern __shared__ uint8_t smem_raw[];
@@ -417,6 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n_x > 0) {
       tc_fence_after();
       const float inv = 1.0f / l_run;
+      // the row's log-sum-exp in log2 units, m + log2(l), for the backward
+      if (lse != nullptr && t < T)
+        lse[(static_cast<size_t>(b) * gridDim.y + h) * Tp + t] = m_run + __log2f(l_run);
 #pragma unroll 1
       for (int c = 0; c < kHS / 32; ++c) {  // O / l, 32 columns at a time
         uint32_t o[32];
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <typename T16, typename OutT>
-int launch_typed(void* out, const CUtensorMap& map, int B, int T, int C, int NH, cudaStream_t s) {
+int launch_typed(void* out, float* lse, const CUtensorMap& map, int B, int T, int C, int NH, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};  // per template instance and device
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
@@ -481,15 +484,18 @@ int launch_typed(void* out, const CUtensorMap& map, int B, int T, int C, int NH,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl_on() ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, static_cast<OutT*>(out), T, C, scale_log2);
+  const int Tp = (T + kTQ - 1) / kTQ * kTQ;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, static_cast<OutT*>(out), lse, T, C, Tp, scale_log2);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 }  // namespace
 
 // qkv [B,T,3C] of the 16-bit operand type op; out [B,T,C] of that type
-// (out16) or fp32.  Head size 64 only.
+// (out16) or fp32; lse (optional) [B][NH][Tp], Tp = T rounded up to 128:
+// each row's log-sum-exp of the scaled scores in log2 units.  Head size 64
+// only.
 int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
-                          cudaStream_t s) {
+                          cudaStream_t s, float* lse) {
   if (C / NH != kHS || C % 8 != 0) return GPT2_ERR_UNSUPPORTED;
   // [B][T][3C] viewed as tiles of 64 dimensions x 128 rows with the 128-byte
   // swizzle: Q, K (K-major operands) and V (an MN-major operand) alike
@@ -500,10 +506,10 @@ int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B,
   const CUtensorMapDataType dt = op == kOpF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!encode_tensor_map(&map, dt, 3, qkv, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return GPT2_ERR_CUDA;
   if (op == kOpF16)
-    return out16 ? launch_typed<__half, __half>(out, map, B, T, C, NH, s)
-                 : launch_typed<__half, float>(out, map, B, T, C, NH, s);
-  return out16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(out, map, B, T, C, NH, s)
-               : launch_typed<__nv_bfloat16, float>(out, map, B, T, C, NH, s);
+    return out16 ? launch_typed<__half, __half>(out, lse, map, B, T, C, NH, s)
+                 : launch_typed<__half, float>(out, lse, map, B, T, C, NH, s);
+  return out16 ? launch_typed<__nv_bfloat16, __nv_bfloat16>(out, lse, map, B, T, C, NH, s)
+               : launch_typed<__nv_bfloat16, float>(out, lse, map, B, T, C, NH, s);
 }
 
 }  // namespace gpt2

@@ -145,9 +145,11 @@ void launch_gemm_simt(float* out, const float* A, const float* W, const float* b
 // the operand type when out16.
 int launch_attention_16(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
                         cudaStream_t s);
-// The same on tcgen05/TMEM (attention_tc.cu), head size 64 only.
+// The same on tcgen05/TMEM (attention_tc.cu), head size 64 only; lse
+// (optional): [B][NH][attn_bwd_padded_len(T)] floats, each row's
+// log-sum-exp of the scaled scores in log2 units (m + log2 l).
 int launch_attention_tc05(void* out, bool out16, const void* qkv, int op, int B, int T, int C, int NH,
-                          cudaStream_t s);
+                          cudaStream_t s, float* lse = nullptr);
 // fp32 CUDA-core causal attention (head size 16, 32 or 64).
 int launch_attention_f32(float* out, const float* qkv, int B, int T, int C, int NH, cudaStream_t s);
 // Decode attention: one query per sequence (row b of qkv [B,3C]) against the
@@ -163,6 +165,19 @@ void launch_decode_attention_f32(float* out, const float* qkv, float* kcache, fl
 // [B][NH][T] floats of scratch (the forward's row statistic, rowsum dO*O).
 int launch_attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, float* Lrow,
                               float* Drow, int B, int T, int C, int NH, cudaStream_t s);
+
+// attention_bwd_tc.cu: the backward of causal attention on tcgen05, head
+// size 64, bf16 operands.  attn_bwd_padded_len(T): T rounded up to 128, the
+// row length of the [B][NH][Tp] statistics.  launch_attn_bwd_prep: dO16
+// [B,T,C] bf16 = dout, Dv = rowsum(dout * out) per head, Dv and Lse zero
+// past T.  launch_attention_backward_tc05: dqkv [B,T,3C] fp32 (every
+// element written) from qkv16 [B,T,3C] and do16 [B,T,C] bf16, Lse from the
+// forward (launch_attention_tc05) and Dv.
+int attn_bwd_padded_len(int T);
+void launch_attn_bwd_prep(void* do16, float* Dv, float* Lse, const float* dout, const float* out, int B, int T, int C,
+                          int NH, cudaStream_t s);
+int launch_attention_backward_tc05(float* dqkv, const void* qkv16, const void* do16, const float* Lse,
+                                   const float* Dv, int B, int T, int C, int NH, cudaStream_t s);
 
 // train.cu: the training step's kernels (fp32).  column_parts(rows): the
 // partial sums a column reduction over `rows` rows keeps in scratch.

@@ -170,25 +170,36 @@ GPT2_API size_t attention_workspace_size(int B, int T, int C, int precision);
 GPT2_API int attention_forward(float* out, const float* qkv, int B, int T, int C, int NH, int precision, void* workspace,
                       size_t ws_bytes, void* stream);
 
-/* Scratch bytes attention_backward needs: two [B][NH][T] fp32 arrays (the
- * forward's per-row softmax statistic and rowsum(dout * out)). */
-GPT2_API size_t attention_backward_workspace_size(int B, int T, int C, int NH);
+/* Scratch bytes attention_backward needs at this precision; 0 for a
+ * precision or head size it does not support.  GPT2_FP32: two [B][NH][T]
+ * fp32 arrays (the forward's per-row softmax statistic and rowsum(dout *
+ * out)).  GPT2_TF32 / GPT2_BF16 (head size 64): bf16 copies of qkv and dout,
+ * a bf16 [B,T,C] scratch output and two [B][NH][Tp] fp32 arrays (Tp = T
+ * rounded up to 128). */
+GPT2_API size_t attention_backward_workspace_size(int B, int T, int C, int NH, int precision);
 
 /* The backward pass of causal multi-head attention ["Understand
  * FlashAttention (II)": the backward algorithms of Algorithms 0 and 1; the
- * llm.c table's attention backward kernels], in fp32 on CUDA cores:
+ * llm.c table's attention backward kernels]:
  *   with S = q k^T / sqrt(hs) (causal), P = softmax_rows(S), out = P v and
  *   dout = dL/dout:  dv = P^T dout,  dP = dout v^T,
  *   dS = P (dP - rowsum(dout * out)),  dq = dS k / sqrt(hs),
  *   dk = dS^T q / sqrt(hs),
  * per (sequence, head), written into dqkv [B,T,3C] in the column blocks of
  * q, k and v (every element written).  qkv [B,T,3C] and out [B,T,C] are
- * the forward's input and output (out as attention_forward computes it in
- * GPT2_FP32), dout [B,T,C].  P is recomputed tile by tile from a per-row
- * statistic, never stored; the results do not depend on timing.  Requires
- * hs in {16, 32, 64}; workspace of attention_backward_workspace_size bytes. */
+ * the forward's input and output, dout [B,T,C].  P is recomputed tile by
+ * tile from a per-row statistic, never stored; the results do not depend
+ * on timing.
+ *   GPT2_FP32: fp32 CUDA-core arithmetic, hs in {16, 32, 64}; the statistic
+ *     is recomputed from qkv.
+ *   GPT2_TF32, GPT2_BF16: tcgen05 tensor cores, hs = 64: q, k, v, dout, P
+ *     and dS rounded to bf16, fp32 accumulation; the statistic comes from a
+ *     run of the tensor-core forward (its output discarded), rowsum(dout *
+ *     out) from the given fp32 out.
+ *   GPT2_FP16 (and another hs in a 16-bit mode): GPT2_ERR_UNSUPPORTED.
+ * Workspace of attention_backward_workspace_size bytes, 16-byte aligned. */
 GPT2_API int attention_backward(float* dqkv, const float* dout, const float* qkv, const float* out, int B, int T,
-                                int C, int NH, void* workspace, size_t ws_bytes, void* stream);
+                                int C, int NH, int precision, void* workspace, size_t ws_bytes, void* stream);
 
 /* tanh-GELU [ECE408 "GELU"; llm.c gelu_forward]:
  *   out = 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), n elements. */

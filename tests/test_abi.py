@@ -126,3 +126,22 @@ def test_training_calls_check_their_arguments_on_the_host(lib):
     with pytest.raises(ab.GPT2Error) as e:
         ab.gpt2_adamw(fake, fake, fake, fake, 10, 1e-3, 0.9, 0.95, 1e-8, 0.0, 0, stream=0)  # t starts at 1
     assert e.value.code == -1
+
+
+def test_attention_backward_precisions_on_the_host(lib):
+    B, T, C, NH = 2, 300, 768, 12
+    Tp = 384  # T rounded up to 128
+    assert ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_FP32) == 2 * ((B * NH * T * 4 + 255) // 256 * 256)
+    w16 = ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_BF16)
+    assert w16 >= B * T * (3 * C + 2 * C) * 2 + 2 * B * NH * Tp * 4
+    assert ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_TF32) == w16
+    assert ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_FP16) == 0  # not supported
+    assert ab.attention_backward_workspace_size(B, T, 256, 8, ab.GPT2_BF16) == 0  # head size 32
+    fake = 1 << 20
+    for precision, nh in ((ab.GPT2_FP16, NH), (ab.GPT2_BF16, 24)):
+        with pytest.raises(ab.GPT2Error) as e:
+            ab.attention_backward(fake, fake, fake, fake, B, T, C, nh, precision, fake, 1 << 30, stream=0)
+        assert e.value.code == -7
+    with pytest.raises(ab.GPT2Error) as e:  # workspace too small for the 16-bit path
+        ab.attention_backward(fake, fake, fake, fake, B, T, C, NH, ab.GPT2_BF16, fake, w16 - 1, stream=0)
+    assert e.value.code == -4

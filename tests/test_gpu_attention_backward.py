@@ -33,9 +33,9 @@ def run_backward(B, T, C, NH, seed, qk_std=1.0, std=0.55):
     dout = inputs.make_normal(600 + seed, (B, T, C), 1.0).astype(np.float32).astype(np.float64)
     out = oracle.attention(qkv, NH).astype(np.float32)
     dq = torch.full((B, T, 3 * C), float("nan"), dtype=torch.float32, device="cuda")
-    wsz = ab.attention_backward_workspace_size(B, T, C, NH)
+    wsz = ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_FP32)
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
-    ab.attention_backward(dq, dev(dout, torch.float32), dev(qkv, torch.float32), dev(out), B, T, C, NH, ws, wsz)
+    ab.attention_backward(dq, dev(dout, torch.float32), dev(qkv, torch.float32), dev(out), B, T, C, NH, ab.GPT2_FP32, ws, wsz)
     no_device_error()
     return host(dq), oracle.attention_backward(qkv, dout, NH)
 
@@ -63,9 +63,9 @@ def test_attention_backward_after_the_gpu_forward():
     out = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
     ab.attention_forward(out, dev(qkv), B, T, C, NH, ab.GPT2_FP32, None, 0)
     dq = torch.empty((B, T, 3 * C), dtype=torch.float32, device="cuda")
-    wsz = ab.attention_backward_workspace_size(B, T, C, NH)
+    wsz = ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_FP32)
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
-    ab.attention_backward(dq, dev(dout), dev(qkv), out, B, T, C, NH, ws, wsz)
+    ab.attention_backward(dq, dev(dout), dev(qkv), out, B, T, C, NH, ab.GPT2_FP32, ws, wsz)
     no_device_error()
     ref = oracle.attention_backward(qkv, dout, NH)
     assert_close(host(dq), ref, atol=1e-5 * max(1.0, np.abs(ref).max()), what="forward then backward")
@@ -77,11 +77,11 @@ def test_attention_backward_is_deterministic():
     dout = dev(inputs.make_normal(704, (B, T, C), 1.0), torch.float32)
     out = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
     ab.attention_forward(out, qkv, B, T, C, NH, ab.GPT2_FP32, None, 0)
-    wsz = ab.attention_backward_workspace_size(B, T, C, NH)
+    wsz = ab.attention_backward_workspace_size(B, T, C, NH, ab.GPT2_FP32)
     ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
     res = []
     for _ in range(2):
         dq = torch.empty((B, T, 3 * C), dtype=torch.float32, device="cuda")
-        ab.attention_backward(dq, dout, qkv, out, B, T, C, NH, ws, wsz)
+        ab.attention_backward(dq, dout, qkv, out, B, T, C, NH, ab.GPT2_FP32, ws, wsz)
         res.append(host(dq))
     np.testing.assert_array_equal(res[0], res[1])

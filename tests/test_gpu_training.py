@@ -69,6 +69,19 @@ def test_ragged_sequence_length(precision):
 
 
 @pytest.mark.parametrize("precision", [ab.GPT2_FP32, ab.GPT2_TF32])
+@pytest.mark.parametrize("T", [100, 150])
+def test_head_size_64_ragged_tiles(precision, T):
+    # head size 64: in tf32 mode attention forward and backward run on the
+    # tensor cores (128-row tiles: T = 100 one ragged tile, 150 two)
+    cfg = inputs.GPT2Config(max_seq_len=160, vocab_size=512, padded_vocab_size=512, num_layers=2, num_heads=2,
+                            channels=128)
+    params = inputs.make_params(cfg, 33, "perturbed")
+    tok = inputs.make_tokens(34, 2, T, cfg.vocab_size)
+    tgt = inputs.make_tokens(35, 2, T, cfg.vocab_size)
+    check(cfg, params, tok, tgt, precision, f"hs64 T={T}")
+
+
+@pytest.mark.parametrize("precision", [ab.GPT2_FP32, ab.GPT2_TF32])
 def test_124m_width_one_layer(precision):
     cfg = dataclasses.replace(inputs.GPT2_124M, num_layers=1)
     params = inputs.make_params(cfg, 27)
