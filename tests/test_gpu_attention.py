@@ -76,6 +76,36 @@ def test_attention_fp32_peaked():
     assert_close(got, ref, atol=5e-5, what="peaked fp32")
 
 
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16])
+@pytest.mark.parametrize("late", [40, 70, 100, 127, 250])
+def test_attention_late_dominant_key(precision, late):
+    # Every query is u and every key small except key `late`, which scores
+    # about 17 log2 units above the others.  Rows t >= late meet it after
+    # the 32-key chunks before it have been exponentiated against a lower
+    # maximum: the kernel raises the maximum inside the tile and rescales the
+    # probabilities already written (the key in the second, third or fourth
+    # chunk of the first key tile, or in the second key tile, where O is
+    # rescaled as well).  On the 16-bit grid; the probabilities rescaled a
+    # second time are below 2^-17 of the largest, so the bound is that of
+    # one rounding, u * max|v|, to within a factor 1 + 2^-6.
+    B, T, C, NH = 1, 256, 128, 2
+    hs = C // NH
+    qkv = inputs.make_normal(410, (B, T, 3 * C), 0.3)
+    u = np.full(hs, 0.5)
+    for h in range(NH):
+        qkv[0, :, h * hs:(h + 1) * hs] = u
+        qkv[0, late, C + h * hs:C + (h + 1) * hs] = 6 * u
+    qkv = inputs.on_grid(qkv, GRID[precision])
+    out = torch.full((B, T, C), float("nan"), dtype=torch.float32, device="cuda")
+    wsz = ab.attention_workspace_size(B, T, C, precision)
+    ws = torch.empty(wsz, dtype=torch.uint8, device="cuda")
+    ab.attention_forward(out, dev(qkv), B, T, C, NH, precision, ws, wsz)
+    no_device_error()
+    ref = oracle.attention(qkv, NH)
+    vmax = np.abs(qkv[..., 2 * C:]).max()
+    assert_close(host(out), ref, atol=UNIT[precision] * vmax * (1 + 2.0 ** -6), what=f"dominant key at {late}")
+
+
 def test_attention_causal_bitwise():
     B, T, C, NH = 1, 150, 768, 12
     qkv = inputs.make_normal(9, (B, T, 3 * C), 0.55)
