@@ -9,18 +9,21 @@
 //   dQ = dS K / sqrt(64),  dK = dS^T Q / sqrt(64),
 // and P = exp2(S log2(e) - L) from L = m + log2(l), the log-sum-exp of the
 // forward's softmax in log2 units (written by the forward kernel).  The
-// factor 1/sqrt(64) = 2^-3 is applied to dS before it is rounded to bf16
-// (exact: a power of two).
+// kernels compute P' = P / 8 = exp2(S log2(e) - L - 3) (L' = L + 3 is taken
+// once, in the kernel that prepares D), so that dS' = P' (dP - D) is dS
+// scaled by 1/sqrt(64) = 2^-3 with no multiply, and multiply dV by 8 once at
+// the end (exact: powers of two).
 //
 // Two kernels, each a CTA (one per SM) over one 128-row tile of one
 // (sequence, head), so that every gradient element is accumulated in one
 // place and written once (no atomics; results do not depend on timing):
 //   dK/dV  per key tile j: streams the query tiles i >= j (Q_i, dO_i and
 //          their L and D), computes S^T = K Q_i^T and dP^T = V dO_i^T in
-//          TMEM, P^T and dS^T (rows = keys) into shared memory, and
-//          accumulates dV += P^T dO_i and dK += dS^T Q_i in TMEM;
+//          TMEM, P^T and dS^T (rows = keys) written back into TMEM over
+//          the S^T and dP^T they came from, and accumulates dV += P^T dO_i
+//          and dK += dS^T Q_i with those as A operands read from TMEM;
 //   dQ     per query tile i: streams the key tiles j <= i (K_j, V_j),
-//          computes S = Q K_j^T and dP = dO V_j^T, dS into shared memory,
+//          computes S = Q K_j^T and dP = dO V_j^T, dS into TMEM over dP,
 //          and accumulates dQ += dS K_j.
 // In both, the "fixed" pair of tiles (K, V or Q, dO) stays in shared memory
 // and the "streamed" pair (Q_i, dO_i or K_j, V_j) passes through a ring of
@@ -34,7 +37,12 @@
 // buffers (S of tile u + 2 is issued while tile u + 1 is processed), one dP
 // buffer, the accumulators.  The softmax warps first turn S into P (kept
 // in fp32 registers; stored as bf16 for dV), then wait for dP and form dS,
-// so the dP product overlaps the exponentials.
+// so the dP product overlaps the exponentials.  The two warps of a TMEM
+// lane quadrant share its lanes: each reads its half of the columns, and a
+// 64-thread named barrier orders both reads before either writes P or dS
+// over them (packed, the 128 columns of P fit in the first 64).  With P and
+// dS in TMEM there are no shared-memory stores of them and no proxy fences
+// (measured through shared memory: 64 KB of stores per tile pair).
 // Every wait is bounded; a timeout sets the device error word and the CTA
 // drains its copies and MMAs, frees TMEM and returns.
 #include "kernels.cuh"
@@ -45,7 +53,6 @@ namespace {
 constexpr int kR = 128;               // rows of a tile (keys or queries) = TMEM lanes
 constexpr int kHS = 64;               // head size
 constexpr int kTile = kR * kHS * 2;   // 16 KB: 128 rows of 128 bytes
-constexpr int kSq = kR * kR * 2;      // 32 KB: a 128 x 128 bf16 operand, two 64-column swizzle atoms
 constexpr int kStages = 3;
 constexpr int kSmWarps = 8;
 constexpr int kThreads = 64 + 32 * kSmWarps;
@@ -66,13 +73,11 @@ template <bool kDQ>
 struct BwdSmem {
   static constexpr int fixed = 0;                                 // two tiles
   static constexpr int stage = fixed + 2 * kTile;                 // kStages x two tiles
-  static constexpr int p = stage + kStages * 2 * kTile;           // P^T (dK/dV kernel)
-  static constexpr int ds = p + (kDQ ? 0 : kSq);                  // dS^T or dS
-  static constexpr int stats = ds + kSq;                          // dK/dV: kStages x (L[128], D[128])
+  static constexpr int stats = stage + kStages * 2 * kTile;       // dK/dV: kStages x (L'[128], D[128])
   static constexpr int bars = stats + (kDQ ? 0 : kStages * 2 * kR * 4);
   // fixed_full; st_full[kStages], st_empty[kStages]; s_full[2]; dp_full,
-  // p_full, ds_full, p_empty, ds_empty, acc_done, drain
-  static constexpr int n_bars = 1 + 2 * kStages + 2 + 7;
+  // p_full, ds_full, acc_done, drain
+  static constexpr int n_bars = 1 + 2 * kStages + 2 + 5;
   static constexpr int misc = bars + n_bars * 8;
   static constexpr int total = misc + 16;
   static constexpr int alloc = total + 1024;
@@ -87,15 +92,14 @@ __device__ __forceinline__ void mma_dim(uint32_t d, uint32_t a_addr, uint32_t b_
     tc_mma_warp<false>(d, ad + 2 * kk, bd + 2 * kk, kIdescS, kk > 0 ? 1u : 0u);
 }
 
-// D (+)= A B over 128 rows: A a 128 x 128 K-major operand in two swizzle
-// atoms, B a 128-row tile read MN-major (64 contiguous head dimensions per
-// row of K)
-__device__ __forceinline__ void mma_rows(uint32_t d, uint32_t a_addr, uint32_t b_addr, bool first) {
-  const uint64_t ad = smem_desc_sw128(a_addr), bd = smem_desc_sw128_mn(b_addr, 1024);
+// D (+)= A B over 128 rows: A a 128 x 128 bf16 operand in TMEM (rows in
+// lanes, two values per column: 64 columns from a_tmem), B a 128-row tile
+// read MN-major (64 contiguous head dimensions per row of K)
+__device__ __forceinline__ void mma_rows(uint32_t d, uint32_t a_tmem, uint32_t b_addr, bool first) {
+  const uint64_t bd = smem_desc_sw128_mn(b_addr, 1024);
 #pragma unroll
-  for (int kk = 0; kk < kR / 16; ++kk)  // A: 16 columns = 32 bytes of a 64-column atom; B: 16 rows of 128 bytes
-    tc_mma_warp<false>(d, ad + ((kk >> 2) * (kSq / 2) + (kk & 3) * 32) / 16, bd + kk * (2048 / 16), kIdescAcc,
-                       (!first || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kR / 16; ++kk)  // A: 16 columns = 8 TMEM columns; B: 16 rows of 128 bytes
+    tc_mma_ts_warp(d, a_tmem + kk * 8, bd + kk * (2048 / 16), kIdescAcc, (!first || kk > 0) ? 1u : 0u);
 }
 
 // kDQ = false: the dK/dV kernel (blockIdx.x = key tile, longest first);
@@ -107,7 +111,7 @@ template <bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ CUtensorMap tmap_do,
                          float* __restrict__ dqkv, const float* __restrict__ Lse, const float* __restrict__ Dv, int T,
-                         int C, int Tp, float scale_log2, float ds_scale) {
+                         int C, int Tp, float scale_log2) {
   using L = BwdSmem<kDQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -117,11 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* st_empty = st_full + kStages; // [kStages] its last reader is done
   uint64_t* s_full = st_empty + kStages;  // [2] S of tile u in buffer u % 2
   uint64_t* dp_full = s_full + 2;         // dP of tile u (phase u % 2)
-  uint64_t* p_full = dp_full + 1;         // the softmax warps have read S (and written P^T) of tile u
-  uint64_t* ds_full = p_full + 1;         // ... read dP and written dS of tile u
-  uint64_t* p_empty = ds_full + 1;        // dV of tile u has read P^T
-  uint64_t* ds_empty = p_empty + 1;       // dK / dQ of tile u has read dS
-  uint64_t* acc_done = ds_empty + 1;      // the accumulators are final
+  uint64_t* p_full = dp_full + 1;         // the P warps have written P^T of tile u into TMEM (dK/dV)
+  uint64_t* ds_full = p_full + 1;         // ... read dP and written dS of tile u into TMEM
+  uint64_t* acc_done = ds_full + 1;       // the accumulators are final
   uint64_t* drain = acc_done + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
@@ -146,8 +148,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1u);
     mbar_init(p_full, kSmWarps);
     mbar_init(ds_full, kSmWarps);
-    mbar_init(p_empty, 1u);
-    mbar_init(ds_empty, 1u);
     mbar_init(acc_done, 1u);
     mbar_init(drain, 1u);
     *abort_flag = 0;
@@ -213,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMAs
     const uint32_t fixed0 = smem_u32(smem + L::fixed), fixed1 = fixed0 + kTile;
-    const uint32_t p_addr = smem_u32(smem + L::p), ds_addr = smem_u32(smem + L::ds);
     auto stream0 = [&](int u) { return smem_u32(smem + L::stage + (u % kStages) * 2 * kTile); };
     auto stream1 = [&](int u) { return stream0(u) + kTile; };
     auto wait_stage = [&](int u) {
@@ -238,26 +237,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n > 1) issue_s(1);
     for (int u = 0; u < n && ok; ++u) {
       if (!kDQ) {
-        // dV += P^T dO_i once P^T is written (S of tile u has been read:
-        // its buffer takes S of tile u + 2)
+        // dV += P'^T dO_i once P^T is in TMEM over S^T of tile u; S of tile
+        // u + 2 then goes into that buffer (the products run in issue order)
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, u & 1)))) break;
         tc_fence_after();
-        mma_rows(tmem + kTmemAcc, p_addr, stream1(u), u == 0);
-        tc_commit_warp(p_empty);
+        mma_rows(tmem + kTmemAcc, tmem + kTmemS + (u & 1) * kR, stream1(u), u == 0);
         if (u + 2 < n) {
           if (!(ok = wait_stage(u + 2))) break;
           issue_s(u + 2);
         }
       }
-      // dS written and dP read: dP of the next tile, then dK += dS^T Q_i
-      // (or dQ += dS K_j)
+      // dS in TMEM over dP: dK += dS^T Q_i (or dQ += dS K_j), then dP of the
+      // next tile into the same columns (issued after: the products run in
+      // issue order)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_full, u & 1)))) break;
       tc_fence_after();
-      if (u + 1 < n) issue_dp(u + 1);
-      mma_rows(tmem + kTmemAcc + (kDQ ? 0 : kHS), ds_addr, stream0(u), u == 0);
-      tc_commit_warp(ds_empty);
+      mma_rows(tmem + kTmemAcc + (kDQ ? 0 : kHS), tmem + kTmemDP, stream0(u), u == 0);
       tc_commit_warp(&st_empty[u % kStages]);
       if (u == n - 1) tc_commit_warp(acc_done);
+      if (u + 1 < n) issue_dp(u + 1);
       if (kDQ && u + 2 < n) {  // S of tile u was read before dS was formed
         if (!(ok = wait_stage(u + 2))) break;
         issue_s(u + 2);
@@ -273,33 +271,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hf = sw >> 2;         // columns [64 hf, 64 hf + 64)
     const int row = qw * 32 + lane; // row of the tile = TMEM lane
     const int col0 = hf * 64;
+    const int pair_bar = 1 + qw;    // the named barrier of this quadrant's two warps
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    float l_row = 0.f, d_row = 0.f;  // dQ kernel: the row's L and D
+    float l_row = 0.f, d_row = 0.f;  // dQ kernel: the row's L' and D
     if (kDQ) {
       const size_t at = bh * Tp + static_cast<size_t>(ft) * kR + row;
       l_row = __ldg(Lse + at);
       d_row = __ldg(Dv + at);
     }
-    // stores 64 bf16 values (32 packed pairs) of this thread's row into a
-    // 128 x 128 K-major operand: the row's half hf is swizzle atom hf
-    auto store_row = [&](uint8_t* base, const uint32_t(&pk)[32]) {
-      uint8_t* prow = base + hf * (kSq / 2) + row * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-    };
     bool ok = true;
     for (int u = 0; u < n; ++u) {
       const int sb = u & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (u >> 1) & 1)))) break;
-      const float* stats = nullptr;  // dK/dV: L and D of the query tile, per column
+      bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (u >> 1) & 1));
+      const float* stats = nullptr;  // dK/dV: L' and D of the query tile, per column
       if (!kDQ) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&st_full[u % kStages], (u / kStages) & 1))))
-          break;  // (complete already: S of tile u was issued after it)
+        // (complete already: S of tile u was issued after it)
+        got = __all_sync(0xffffffffu, got && mbar_wait(&st_full[u % kStages], (u / kStages) & 1));
         stats = reinterpret_cast<const float*>(smem + L::stats) + (u % kStages) * 2 * kR;
       }
-      tc_fence_after();
       // visible columns [lo, hi) of this row
       int lo, hi;
       if (!kDQ) {  // row = key ft * 128 + row; column = query (ft + u) * 128 + c: c >= row on the diagonal, < T
@@ -311,71 +300,101 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool all_valid = lo <= col0 && hi >= col0 + 64;
       uint32_t sv[2][32];
-      tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0, sv[0]);
-      tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0 + 32, sv[1]);
-      tmem_ld_wait();
-      // P = exp2(S log2(e)/8 - L), zero outside [lo, hi); kept in sv as fp32
+      if (got) {
+        tc_fence_after();
+        tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0, sv[0]);
+        tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0 + 32, sv[1]);
+        tmem_ld_wait();
+      }
+      // both warps of the quadrant have read their S columns (or one gave up)
+      if (bar_or(pair_bar, 64, !got)) {
+        ok = false;
+        break;
+      }
+      // P' = exp2(S log2(e)/8 - L'), zero outside [lo, hi); kept in sv as fp32
       const float2 sc = make_float2(scale_log2, scale_log2);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 nl;
+        for (int e = 0; e < 32; e += 4) {
+          float4 nl4;
           if (kDQ) {
-            nl = make_float2(-l_row, -l_row);
+            nl4 = make_float4(-l_row, -l_row, -l_row, -l_row);
           } else {
-            const float2 lv = *reinterpret_cast<const float2*>(stats + col0 + c * 32 + e);
-            nl = make_float2(-lv.x, -lv.y);
+            const float4 lv = *reinterpret_cast<const float4*>(stats + col0 + c * 32 + e);
+            nl4 = make_float4(-lv.x, -lv.y, -lv.z, -lv.w);
           }
-          float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sc, nl);
+          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sc,
+                                 make_float2(nl4.x, nl4.y));
+          float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), sc,
+                                 make_float2(nl4.z, nl4.w));
           if (!all_valid) {
             const int cc = col0 + c * 32 + e;
-            if (cc < lo || cc >= hi) x.x = -INFINITY;
-            if (cc + 1 < lo || cc + 1 >= hi) x.y = -INFINITY;
+            if (cc < lo || cc >= hi) x0.x = -INFINITY;
+            if (cc + 1 < lo || cc + 1 >= hi) x0.y = -INFINITY;
+            if (cc + 2 < lo || cc + 2 >= hi) x1.x = -INFINITY;
+            if (cc + 3 < lo || cc + 3 >= hi) x1.y = -INFINITY;
           }
-          sv[c][e] = __float_as_uint(ex2(x.x));
-          sv[c][e + 1] = __float_as_uint(ex2(x.y));
+          sv[c][e] = __float_as_uint(ex2(x0.x));
+          sv[c][e + 1] = __float_as_uint(ex2(x0.y));
+          sv[c][e + 2] = __float_as_uint(ex2(x1.x));
+          sv[c][e + 3] = __float_as_uint(ex2(x1.y));
         }
       }
       if (!kDQ) {
-        // P^T into shared memory for dV (its buffer is free once dV of the
-        // previous tile has read it)
+        // P'^T (bf16 pairs) over this warp's half of the first 64 columns of
+        // S^T's buffer: the A operand of dV
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           pk[e] = pack_bf16x2(__uint_as_float(sv[e >> 4][(e & 15) * 2]), __uint_as_float(sv[e >> 4][(e & 15) * 2 + 1]));
-        if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(p_empty, (u - 1) & 1)))) break;
-        store_row(smem + L::p, pk);
-        fence_proxy_async_smem();
+        tmem_st_32x32b_x32(lane_base + kTmemS + sb * kR + hf * 32, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (!kDQ && lane == 0) mbar_arrive(p_full);
-      // dS = P (dP - D) / 8
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1)))) break;
-      tc_fence_after();
+      // dS' = P' (dP - D), one 32-column chunk of dP at a time; the second
+      // chunk's load completes this warp's reads of dP before the barrier
+      got = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1));
+      if (got) tc_fence_after();
       uint32_t pk[32];
+      bool gave_up = false;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t dv[32];
-        tmem_ld_32x32b_x32(lane_base + kTmemDP + col0 + c * 32, dv);
-        tmem_ld_wait();
+        if (got) {
+          tmem_ld_32x32b_x32(lane_base + kTmemDP + col0 + c * 32, dv);
+          tmem_ld_wait();
+        }
+        if (c == 1 && bar_or(pair_bar, 64, !got)) {  // both warps of the quadrant have read their dP
+          gave_up = true;
+          break;
+        }
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float2 d2;
+        for (int e = 0; e < 32; e += 4) {
+          float4 d4;
           if (kDQ) {
-            d2 = make_float2(d_row, d_row);
+            d4 = make_float4(d_row, d_row, d_row, d_row);
           } else {
-            d2 = *reinterpret_cast<const float2*>(stats + kR + col0 + c * 32 + e);
+            d4 = *reinterpret_cast<const float4*>(stats + kR + col0 + c * 32 + e);
           }
-          const float g0 = (__uint_as_float(dv[e]) - d2.x) * ds_scale;
-          const float g1 = (__uint_as_float(dv[e + 1]) - d2.y) * ds_scale;
-          pk[c * 16 + e / 2] = pack_bf16x2(__uint_as_float(sv[c][e]) * g0, __uint_as_float(sv[c][e + 1]) * g1);
+          const float2 g0 = __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                       make_float2(-d4.x, -d4.y));
+          const float2 g1 = __fadd2_rn(make_float2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                                       make_float2(-d4.z, -d4.w));
+          const float2 q0 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), g0);
+          const float2 q1 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), g1);
+          pk[c * 16 + e / 2] = pack_bf16x2(q0.x, q0.y);
+          pk[c * 16 + e / 2 + 1] = pack_bf16x2(q1.x, q1.y);
         }
       }
-      if (u > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(ds_empty, (u - 1) & 1)))) break;
-      store_row(smem + L::ds, pk);
-      fence_proxy_async_smem();  // dS written by this thread becomes visible to the MMA
+      if (gave_up) {
+        ok = false;
+        break;
+      }
+      tmem_st_32x32b_x32(lane_base + kTmemDP + hf * 32, pk);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
@@ -396,9 +415,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         if (r_glob < T) {
           float* dst = dqkv + (static_cast<size_t>(b) * T + r_glob) * 3 * C + g_col + c * 32;
+          const float f = (!kDQ && hf == 0) ? 8.0f : 1.0f;  // dV accumulated P' = P / 8
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            reinterpret_cast<uint4*>(dst)[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+            reinterpret_cast<float4*>(dst)[q] =
+                make_float4(__uint_as_float(o[4 * q]) * f, __uint_as_float(o[4 * q + 1]) * f,
+                            __uint_as_float(o[4 * q + 2]) * f, __uint_as_float(o[4 * q + 3]) * f);
         }
       }
     } else {
@@ -415,8 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // dO [B,T,C] fp32 -> bf16 copy; D[b][h][t] = sum over the head's 64
-// columns of dO * O; D and L are zero for t in [T, Tp).  Eight threads per
-// head and row, eight columns each.
+// columns of dO * O; the forward's L becomes L' = L + 3 in place (the
+// backward kernels compute P / 8); D and L' are zero for t in [T, Tp).
+// Eight threads per head and row, eight columns each.
 __global__ void attn_bwd_prep_kernel(__nv_bfloat16* __restrict__ do16, float* __restrict__ Dv, float* __restrict__ Lse,
                                      const float* __restrict__ dout, const float* __restrict__ out, int B, int T, int C,
                                      int NH, int Tp) {
@@ -444,7 +467,7 @@ __global__ void attn_bwd_prep_kernel(__nv_bfloat16* __restrict__ do16, float* __
   if (live && (c8 & 7) == 0) {
     const size_t at = (static_cast<size_t>(b) * NH + c8 / 8) * Tp + t;
     Dv[at] = dot;
-    if (t >= T) Lse[at] = 0.f;
+    Lse[at] = t < T ? Lse[at] + 3.0f : 0.f;
   }
 }
 
@@ -499,12 +522,11 @@ int launch_attention_backward_tc05(float* dqkv, const void* qkv16, const void* d
   }
   const int Tp = attn_bwd_padded_len(T);
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
-  const float ds_scale = 0.125f;                        // 1 / sqrt(64)
   const dim3 grid((T + kR - 1) / kR, NH, B);
   attn_bwd_tc05_kernel<false><<<grid, kThreads, BwdSmem<false>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
-                                                                            scale_log2, ds_scale);
+                                                                            scale_log2);
   attn_bwd_tc05_kernel<true><<<grid, kThreads, BwdSmem<true>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
-                                                                          scale_log2, ds_scale);
+                                                                          scale_log2);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
