@@ -161,13 +161,28 @@ __global__ void __launch_bounds__(1024) mean_kernel(float* __restrict__ out, con
 // part[p][c] = sum of in[r][c] over rows r in [p * rows_per_part, ...);
 // grid (column blocks of 256, parts)
 __global__ void column_partial_kernel(float* __restrict__ part, const float* __restrict__ in, int rows, int cols,
-                                      int rows_per_part) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+                                      int rows_per_part, int vec) {
   const int r0 = blockIdx.y * rows_per_part, r1 = min(rows, r0 + rows_per_part);
-  float s = 0.f;
-  for (int r = r0; r < r1; ++r) s += in[static_cast<size_t>(r) * cols + c];
-  part[static_cast<size_t>(blockIdx.y) * cols + c] = s;
+  if (vec) {  // four columns per thread, 16-byte loads
+    const int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (c >= cols) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(in + static_cast<size_t>(r) * cols + c));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(part + static_cast<size_t>(blockIdx.y) * cols + c) = acc;
+  } else {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.f;
+    for (int r = r0; r < r1; ++r) acc += in[static_cast<size_t>(r) * cols + c];
+    part[static_cast<size_t>(blockIdx.y) * cols + c] = acc;
+  }
 }
 
 // out[c] = (out[c] +) sum over the parts of part[p][c], in part order
@@ -215,18 +230,41 @@ __global__ void __launch_bounds__(256) layernorm_backward_dx_kernel(float* __res
 __global__ void layernorm_backward_wb_kernel(float* __restrict__ part_w, float* __restrict__ part_b,
                                              const float* __restrict__ dy, const float* __restrict__ x,
                                              const float* __restrict__ mean, const float* __restrict__ rstd, int N,
-                                             int C, int rows_per_part) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
+                                             int C, int rows_per_part, int vec) {
   const int r0 = blockIdx.y * rows_per_part, r1 = min(N, r0 + rows_per_part);
-  float sw = 0.f, sb = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    const float d = dy[static_cast<size_t>(r) * C + c];
-    sw += d * (x[static_cast<size_t>(r) * C + c] - mean[r]) * rstd[r];
-    sb += d;
+  if (vec) {  // four columns per thread, 16-byte loads
+    const int c = 4 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (c >= C) return;
+    float4 sw = make_float4(0.f, 0.f, 0.f, 0.f), sb = sw;
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      const size_t at = static_cast<size_t>(r) * C + c;
+      const float4 d = __ldg(reinterpret_cast<const float4*>(dy + at));
+      const float4 xv = __ldg(reinterpret_cast<const float4*>(x + at));
+      const float mr = __ldg(mean + r), rr = __ldg(rstd + r);
+      sw.x += d.x * (xv.x - mr) * rr;
+      sw.y += d.y * (xv.y - mr) * rr;
+      sw.z += d.z * (xv.z - mr) * rr;
+      sw.w += d.w * (xv.w - mr) * rr;
+      sb.x += d.x;
+      sb.y += d.y;
+      sb.z += d.z;
+      sb.w += d.w;
+    }
+    *reinterpret_cast<float4*>(part_w + static_cast<size_t>(blockIdx.y) * C + c) = sw;
+    *reinterpret_cast<float4*>(part_b + static_cast<size_t>(blockIdx.y) * C + c) = sb;
+  } else {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float sw = 0.f, sb = 0.f;
+    for (int r = r0; r < r1; ++r) {
+      const float d = dy[static_cast<size_t>(r) * C + c];
+      sw += d * (x[static_cast<size_t>(r) * C + c] - mean[r]) * rstd[r];
+      sb += d;
+    }
+    part_w[static_cast<size_t>(blockIdx.y) * C + c] = sw;
+    part_b[static_cast<size_t>(blockIdx.y) * C + c] = sb;
   }
-  part_w[static_cast<size_t>(blockIdx.y) * C + c] = sw;
-  part_b[static_cast<size_t>(blockIdx.y) * C + c] = sb;
 }
 
 // dinp = dout * GELU'(inp), GELU in the tanh form
@@ -265,17 +303,40 @@ __global__ void encoder_backward_wte_kernel(float* __restrict__ dwte, const floa
 
 // AdamW: m = b1 m + (1 - b1) g, v = b2 v + (1 - b2) g^2,
 // p -= lr (m / c1 / (sqrt(v / c2) + eps) + wd p), c1 = 1 - b1^t, c2 = 1 - b2^t
+__device__ __forceinline__ void adamw_one(float& p, float g, float& m, float& v, float lr, float b1, float b2,
+                                          float eps, float wd, float c1, float c2) {
+  m = b1 * m + (1.f - b1) * g;
+  v = b2 * v + (1.f - b2) * g * g;
+  p -= lr * ((m / c1) / (sqrtf(v / c2) + eps) + wd * p);
+}
+
+// vec (the four buffers 16-byte aligned): four parameters per iteration
+// with 16-byte accesses, then the tail of n % 4; else one at a time
 __global__ void adamw_kernel(float* __restrict__ p, const float* __restrict__ g, float* __restrict__ m,
                              float* __restrict__ v, long long n, float lr, float b1, float b2, float eps, float wd,
-                             float c1, float c2) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float gi = g[i];
-    const float mi = b1 * m[i] + (1.f - b1) * gi;
-    const float vi = b2 * v[i] + (1.f - b2) * gi * gi;
-    m[i] = mi;
-    v[i] = vi;
-    p[i] -= lr * ((mi / c1) / (sqrtf(vi / c2) + eps) + wd * p[i]);
+                             float c1, float c2, int vec) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if (!vec) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride)
+      adamw_one(p[i], g[i], m[i], v[i], lr, b1, b2, eps, wd, c1, c2);
+    return;
+  }
+  const long long n4 = n / 4;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+    float4 pi = reinterpret_cast<float4*>(p)[i], mi = reinterpret_cast<float4*>(m)[i],
+           vi = reinterpret_cast<float4*>(v)[i];
+    const float4 gi = __ldg(reinterpret_cast<const float4*>(g) + i);
+    adamw_one(pi.x, gi.x, mi.x, vi.x, lr, b1, b2, eps, wd, c1, c2);
+    adamw_one(pi.y, gi.y, mi.y, vi.y, lr, b1, b2, eps, wd, c1, c2);
+    adamw_one(pi.z, gi.z, mi.z, vi.z, lr, b1, b2, eps, wd, c1, c2);
+    adamw_one(pi.w, gi.w, mi.w, vi.w, lr, b1, b2, eps, wd, c1, c2);
+    reinterpret_cast<float4*>(p)[i] = pi;
+    reinterpret_cast<float4*>(m)[i] = mi;
+    reinterpret_cast<float4*>(v)[i] = vi;
+  }
+  if (blockIdx.x == 0 && threadIdx.x < n - 4 * n4) {
+    const long long i = 4 * n4 + threadIdx.x;
+    adamw_one(p[i], g[i], m[i], v[i], lr, b1, b2, eps, wd, c1, c2);
   }
 }
 
@@ -285,7 +346,7 @@ unsigned grid_for(long long n, int threads) {
   return static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
-constexpr int kPartRows = 256;  // rows per partial sum of a column reduction
+constexpr int kPartRows = 64;  // rows per partial sum of a column reduction
 
 }  // namespace
 
@@ -308,7 +369,13 @@ void launch_crossentropy(float* logits, float* losses, float* loss, const int* t
 
 void launch_column_sum(float* out, float* part, const float* in, int rows, int cols, bool accumulate, cudaStream_t s) {
   const int parts = column_parts(rows);
-  column_partial_kernel<<<dim3((cols + 255) / 256, parts), 256, 0, s>>>(part, in, rows, cols, kPartRows);
+  const int vec = (cols % 4 == 0 && (reinterpret_cast<uintptr_t>(in) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(part) & 15u) == 0)
+                      ? 1
+                      : 0;
+  const int per_block = vec ? 1024 : 256;  // columns per block of 256 threads
+  column_partial_kernel<<<dim3((cols + per_block - 1) / per_block, parts), 256, 0, s>>>(part, in, rows, cols,
+                                                                                       kPartRows, vec);
   column_sum_kernel<<<(cols + 255) / 256, 256, 0, s>>>(out, part, parts, cols, accumulate ? 1 : 0);
 }
 
@@ -319,8 +386,13 @@ void launch_layernorm_backward(float* dx, float* dw, float* db, float* part, con
   const int parts = column_parts(N);
   float* part_w = part;
   float* part_b = part + static_cast<size_t>(parts) * C;
-  layernorm_backward_wb_kernel<<<dim3((C + 255) / 256, parts), 256, 0, s>>>(part_w, part_b, dy, x, mean, rstd, N, C,
-                                                                            kPartRows);
+  const int vec = (C % 4 == 0 && (reinterpret_cast<uintptr_t>(dy) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (reinterpret_cast<uintptr_t>(part) & 15u) == 0)
+                      ? 1
+                      : 0;
+  const int per_block = vec ? 1024 : 256;
+  layernorm_backward_wb_kernel<<<dim3((C + per_block - 1) / per_block, parts), 256, 0, s>>>(
+      part_w, part_b, dy, x, mean, rstd, N, C, kPartRows, vec);
   column_sum_kernel<<<(C + 255) / 256, 256, 0, s>>>(dw, part_w, parts, C, 0);
   column_sum_kernel<<<(C + 255) / 256, 256, 0, s>>>(db, part_b, parts, C, 0);
 }
@@ -339,7 +411,12 @@ void launch_encoder_backward(float* dwte, float* dwpe, const float* dx, const in
 void launch_adamw(float* p, const float* g, float* m, float* v, long long n, float lr, float b1, float b2, float eps,
                   float wd, int t, cudaStream_t s) {
   const float c1 = 1.f - powf(b1, static_cast<float>(t)), c2 = 1.f - powf(b2, static_cast<float>(t));
-  adamw_kernel<<<grid_for(n, 256), 256, 0, s>>>(p, g, m, v, n, lr, b1, b2, eps, wd, c1, c2);
+  const int vec = ((reinterpret_cast<uintptr_t>(p) | reinterpret_cast<uintptr_t>(g) | reinterpret_cast<uintptr_t>(m) |
+                    reinterpret_cast<uintptr_t>(v)) &
+                   15u) == 0
+                      ? 1
+                      : 0;
+  adamw_kernel<<<grid_for(vec ? n / 4 + 1 : n, 256), 256, 0, s>>>(p, g, m, v, n, lr, b1, b2, eps, wd, c1, c2, vec);
 }
 
 }  // namespace gpt2
