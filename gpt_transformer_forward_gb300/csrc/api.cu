@@ -286,8 +286,12 @@ struct StageProfiler {
 // scratch; offsets in bytes, each 256-byte aligned.
 struct TrainLayout {
   size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj, dx,
-      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, total;
+      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, splitk, total;
 };
+
+// the K-split partial products of the weight gradients: up to 16 slices of
+// the largest one (4C x C)
+size_t kSplitkFloats(size_t C) { return 16 * 4 * C * C; }
 
 TrainLayout train_layout(const GPT2Config* c, int B, int T) {
   const size_t N = static_cast<size_t>(B) * T, C = c->channels, L = c->num_layers, Vp = c->padded_vocab_size;
@@ -329,6 +333,7 @@ TrainLayout train_layout(const GPT2Config* c, int B, int T) {
   t.part = take(2 * static_cast<size_t>(column_parts(static_cast<int>(N))) * wide);
   t.attn = take(2 * static_cast<size_t>(B) * c->num_heads * attn_bwd_padded_len(T));
   t.lse = take(L * static_cast<size_t>(B) * c->num_heads * attn_bwd_padded_len(T));
+  t.splitk = take(kSplitkFloats(C));
   t.total = p;
   return t;
 }
@@ -866,7 +871,7 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   float *lnf = buf(tl.lnf), *lnfm = buf(tl.lnfm), *lnfr = buf(tl.lnfr), *logits = buf(tl.logits);
   float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
   float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
-  float *part = buf(tl.part), *attn = buf(tl.attn), *lse = buf(tl.lse);
+  float *part = buf(tl.part), *attn = buf(tl.attn), *lse = buf(tl.lse), *splitk = buf(tl.splitk);
   // the tf32 mode's bf16 copy of one layer's qkv, and of the attention
   // output's gradient, in the backward's scratch (free while they are used)
   void* qkv16 = dt;
@@ -920,7 +925,11 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
     TRY(gemm(precision, dinp, dy, Wt, nullptr, N, K, OC, kEpiF32, s));
     launch_transpose(tA, dy, N, OC, s);  // [OC][N]
     launch_transpose(tB, x, N, K, s);    // [K][N]
-    TRY(gemm(precision, dW, tA, tB, nullptr, OC, K, N, kEpiF32, s));
+    if (precision == GPT2_FP32) {
+      TRY(gemm(precision, dW, tA, tB, nullptr, OC, K, N, kEpiF32, s));
+    } else {  // an [OC][K] product over all N tokens: few, long tiles, so the K range is split
+      TRY(launch_gemm_tc_splitk(dW, splitk, kSplitkFloats(C), tA, tB, OC, K, N, op_of(precision), s));
+    }
     if (db != nullptr) launch_column_sum(db, part, dy, N, OC, false, s);
     return check_launch();
   };

@@ -81,7 +81,8 @@ template <int kEpi, int kOp, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
-                   int K, int tiles_m, int num_tiles, int n_fast, float2* __restrict__ row_stats, int V) {
+                   int K, int tiles_m, int num_tiles, int n_fast, float2* __restrict__ row_stats, int V,
+                   int tiles_mn, int kb_per_split) {
   using L = Layout<kPair>;
   constexpr int kStages = L::kStages;
   constexpr int kAStageBytes = L::kAStageBytes;
@@ -113,12 +114,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operand format field: fp16 0, bf16 1 (kind::f16), tf32 2 (kind::tf32)
   constexpr uint32_t kIdesc = make_idesc(kOp == kOpF16 ? 0u : (kTF32 ? 2u : 1u), kTileM, kBN);
   const int num_kb = (K + kBKElems - 1) / kBKElems;
-  // tile index -> (row block, column block): M-fastest (concurrent tiles
-  // share a weight tile) or, with n_fast, N-fastest (they share an
-  // activation block: for a large A and a small B)
-  const int tiles_n = num_tiles / tiles_m;
-  auto tile_m = [&](int tile) { return n_fast ? tile / tiles_n : tile % tiles_m; };
-  auto tile_n = [&](int tile) { return n_fast ? tile % tiles_n : tile / tiles_m; };
+  // unit index -> (split of the K range, tile); tile -> (row block, column
+  // block): M-fastest (concurrent tiles share a weight tile) or, with
+  // n_fast, N-fastest (they share an activation block: for a large A and a
+  // small B).  Without a K split there is one split and units are tiles.
+  const int tiles_n = tiles_mn / tiles_m;
+  auto tile_m = [&](int unit_) {
+    const int tile = unit_ % tiles_mn;
+    return n_fast ? tile / tiles_n : tile % tiles_m;
+  };
+  auto tile_n = [&](int unit_) {
+    const int tile = unit_ % tiles_mn;
+    return n_fast ? tile % tiles_n : tile / tiles_m;
+  };
+  auto kb_begin = [&](int unit_) { return (unit_ / tiles_mn) * kb_per_split; };
+  auto kb_end = [&](int unit_) { return min(num_kb, (unit_ / tiles_mn + 1) * kb_per_split); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -170,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int a_row = m_blk * kTileM + static_cast<int>(rank) * kBM;
         const int b_row = n_blk * kBN + static_cast<int>(rank) * L::kBRows;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb_begin(tile); kb < kb_end(tile); ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             ok = false;
             break;
@@ -224,7 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int kb0 = kb_begin(tile);
+        for (int kb = kb0; kb < kb_end(tile); ++kb) {
           if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase))) {
             ok = false;
             break;
@@ -236,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBKElems / kMmaK; ++k) {
             if constexpr (kPair)
               tc_mma_pair_warp<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32),
-                                      kIdesc, (kb | k) != 0 ? 1u : 0u);
+                                      kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
             else
               tc_mma_warp<kTF32>(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), kIdesc,
-                                 (kb | k) != 0 ? 1u : 0u);
+                                 (kb != kb0 || k != 0) ? 1u : 0u);
           }
           // frees the smem slot (in both CTAs of a pair) once these MMAs have read it
           if constexpr (kPair)
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             bulk_wait_group_read<0>();  // the previous store has read the buffer
             mbar_arrive_expect_tx(&res_bar[ew], kStageBufBytes);
-            tma_load_2d(stg, &tmap_out, &res_bar[ew], col0, m0);
+            tma_load_3d(stg, &tmap_out, &res_bar[ew], col0, m0, 0);
           }
         }
         float v[kChunkCols];
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmap_out, stg, col0, m0);
+          tma_store_3d(&tmap_out, stg, col0, m0, tile / tiles_mn);  // the split's slice of the output
           bulk_commit_group();
         }
         if (!ok) {
@@ -489,6 +500,17 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int el
   return encode_tensor_map_sw128(map, dt, 2, base, dims, strides, box);
 }
 
+// The output: `depth` slices of [rows][cols] one after another (the slices
+// of a K split; depth 1 otherwise)
+bool make_out_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int rows, int cols,
+                  int depth, int box_cols, int box_rows) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(depth)};
+  const uint64_t strides[2] = {static_cast<uint64_t>(cols) * elem_bytes,
+                               static_cast<uint64_t>(rows) * cols * elem_bytes};
+  const uint32_t box[3] = {static_cast<uint32_t>(box_cols), static_cast<uint32_t>(box_rows), 1};
+  return encode_tensor_map_sw128(map, dt, 3, base, dims, strides, box);
+}
+
 }  // namespace
 
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
@@ -518,7 +540,7 @@ namespace {
 
 template <int kEpi, int kOp, bool kPair>
 int launch_impl(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
-                float2* row_stats, int V) {
+                float2* row_stats, int V, int splits = 1) {
   using L = Layout<kPair>;
   CUtensorMap ta, tb, to;
   constexpr bool kTF32 = (kOp == kOpTF32);
@@ -530,15 +552,19 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
   if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
   if (!make_map(&tb, B, dt_in, eb, N, K, bk, L::kBRows)) return GPT2_ERR_CUDA;
+  const int num_kb = (K + bk - 1) / bk;
+  const int kb_per_split = (num_kb + splits - 1) / splits;
+  splits = (num_kb + kb_per_split - 1) / kb_per_split;  // no empty split
   if (kOutF32) {
-    if (!make_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 32, 32)) return GPT2_ERR_CUDA;
+    if (!make_out_map(&to, out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, splits, 32, 32)) return GPT2_ERR_CUDA;
   } else {
-    if (!make_map(&to, out, dt16, 2, M, N, 64, 32)) return GPT2_ERR_CUDA;
+    if (!make_out_map(&to, out, dt16, 2, M, N, splits, 64, 32)) return GPT2_ERR_CUDA;
   }
   constexpr int kTileM = kPair ? 2 * kBM : kBM;
   const int tiles_m = (M + kTileM - 1) / kTileM;
   const int tiles_n = (N + kBN - 1) / kBN;
-  const int num_tiles = tiles_m * tiles_n;
+  const int tiles_mn = tiles_m * tiles_n;
+  const int num_tiles = tiles_mn * splits;  // units: (split, tile)
   const size_t a_bytes = static_cast<size_t>(M) * K * eb, b_bytes = static_cast<size_t>(N) * K * eb;
   const int n_fast = (a_bytes > (48u << 20) && b_bytes < (32u << 20)) ? 1 : 0;
   auto kern = gemm_tc_kernel<kEpi, kOp, kPair>;
@@ -576,9 +602,36 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const int units = num_tiles < resident[dev] ? num_tiles : resident[dev];
   cfg.gridDim = dim3(kPair ? 2 * units : units);
   cfg.numAttrs = pdl_on() ? 2 : 1;
-  const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, n_fast, row_stats, V);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, n_fast,
+                                           row_stats, V, tiles_mn, kb_per_split);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
+}
+
+// out = the sum of the `splits` slices of part ([splits][n] fp32), in slice
+// order (the result does not depend on timing); vec: 16-byte accesses
+__global__ void splitk_sum_kernel(float* __restrict__ out, const float* __restrict__ part, long long n, int splits,
+                                  int vec) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if (vec) {
+    const long long n4 = n / 4;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+      float4 acc = __ldg(reinterpret_cast<const float4*>(part) + i);
+      for (int sp = 1; sp < splits; ++sp) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(part + sp * n) + i);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      reinterpret_cast<float4*>(out)[i] = acc;
+    }
+  } else {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n; i += stride) {
+      float acc = part[i];
+      for (int sp = 1; sp < splits; ++sp) acc += part[sp * n + i];
+      out[i] = acc;
+    }
+  }
 }
 
 template <int kEpi, int kOp>
@@ -619,6 +672,54 @@ int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, i
       break;
   }
   return GPT2_ERR_UNSUPPORTED;
+}
+
+int splitk_choose(int M, int N, int K, int op, size_t partial_floats) {
+  if (M <= kBM || M <= kSkinnyMaxRows) return 1;  // the pair kernel only
+  const int bk = kRowBytes / (op == kOpTF32 ? 4 : 2);
+  const int num_kb = (K + bk - 1) / bk;
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + kBN - 1) / kBN);
+  const int resident = num_sms() / 2;  // CTA pairs
+  // fewest rounds x k-blocks per split, each split at least 8 k-blocks,
+  // within the partial buffer
+  int best = 1;
+  long long best_cost = static_cast<long long>((tiles + resident - 1) / resident) * num_kb;
+  for (int sp = 2; sp <= 32 && sp * 8 <= num_kb; ++sp) {
+    if (static_cast<size_t>(sp) * M * N > partial_floats) break;
+    const int kbps = (num_kb + sp - 1) / sp;
+    const long long cost = static_cast<long long>((tiles * sp + resident - 1) / resident) * kbps;
+    if (cost < best_cost) {
+      best = sp;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+int launch_gemm_tc_splitk(float* out, float* partials, size_t partial_floats, const void* A, const void* B, int M,
+                          int N, int K, int op, cudaStream_t s) {
+  if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
+  const int splits = splitk_choose(M, N, K, op, partial_floats);
+  if (splits == 1) return launch_gemm_tc(out, A, B, nullptr, M, N, K, kEpiF32, op, s);
+  int rc = GPT2_ERR_UNSUPPORTED;
+  switch (op) {
+    case kOpBF16: rc = launch_impl<kEpiF32, kOpBF16, true>(partials, A, B, nullptr, M, N, K, s, nullptr, 0, splits); break;
+    case kOpF16: rc = launch_impl<kEpiF32, kOpF16, true>(partials, A, B, nullptr, M, N, K, s, nullptr, 0, splits); break;
+    case kOpTF32: rc = launch_impl<kEpiF32, kOpTF32, true>(partials, A, B, nullptr, M, N, K, s, nullptr, 0, splits); break;
+  }
+  if (rc != GPT2_OK) return rc;
+  const long long n = static_cast<long long>(M) * N;
+  const int vec = (n % 4 == 0 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(partials) & 15u) == 0)
+                      ? 1
+                      : 0;
+  const long long work = vec ? n / 4 : n;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  const long long want = (work + 255) / 256;
+  const unsigned blocks = static_cast<unsigned>(want < cap ? want : cap);
+  splitk_sum_kernel<<<blocks, 256, 0, s>>>(out, partials, n, splits, vec);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 
 int launch_gemm_logits(float* logits, float2* row_stats, const void* A, const void* B, int M, int N, int K, int V,

@@ -116,6 +116,17 @@ enum OperandType { kOpBF16 = 0, kOpF16 = 1, kOpTF32 = 2 };
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s);
 
+// The same product (fp32 out, no bias) with the K range split over
+// concurrently running units when the tiles alone would leave most SMs
+// idle (few, long tiles: a weight gradient, K = the tokens): each split's
+// fp32 product goes to its slice of `partials` ([splits][M][N], at most
+// partial_floats floats), then one kernel sums the slices in order into out
+// (deterministic).  Falls back to one launch when splitting does not pay.
+int launch_gemm_tc_splitk(float* out, float* partials, size_t partial_floats, const void* A, const void* B, int M,
+                          int N, int K, int op, cudaStream_t s);
+// the number of K splits that launch chooses
+int splitk_choose(int M, int N, int K, int op, size_t partial_floats);
+
 // gemm_skinny.cu: the same product for M <= 64 rows (not the LM-head
 // epilogue): weight blocks of 128 rows, K split over the CTAs of a cluster,
 // reduced through distributed shared memory.  launch_gemm_tc routes small M

@@ -136,3 +136,20 @@ def test_training_lowers_the_loss_and_is_repeatable():
     n_wte = cfg.padded_vocab_size * cfg.channels
     np.testing.assert_array_equal(g1[n_wte:], g2[n_wte:])
     np.testing.assert_allclose(g1[:n_wte], g2[:n_wte], atol=1e-6 * np.abs(g1).max())
+
+
+def test_split_k_weight_gradients():
+    # 1024 tokens: the tf32 weight-gradient products (K = the tokens, 32
+    # k-blocks) run with their K range split over four units each, partial
+    # products summed in a fixed order; against the oracle, and bitwise
+    # repeatable
+    cfg = inputs.GPT2Config(max_seq_len=256, vocab_size=512, padded_vocab_size=512, num_layers=2, num_heads=4,
+                            channels=256)
+    params = inputs.make_params(cfg, 36, "perturbed")
+    tok = inputs.make_tokens(37, 4, 256, cfg.vocab_size)
+    tgt = inputs.make_tokens(38, 4, 256, cfg.vocab_size)
+    check(cfg, params, tok, tgt, ab.GPT2_TF32, "split K")
+    _, g1 = gpu_step(cfg, params, tok, tgt, ab.GPT2_TF32)
+    _, g2 = gpu_step(cfg, params, tok, tgt, ab.GPT2_TF32)
+    n_wte = cfg.padded_vocab_size * cfg.channels
+    np.testing.assert_array_equal(g1[n_wte:], g2[n_wte:])
