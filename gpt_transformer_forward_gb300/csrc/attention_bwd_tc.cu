@@ -54,6 +54,12 @@ constexpr int kR = 128;               // rows of a tile (keys or queries) = TMEM
 constexpr int kHS = 64;               // head size
 constexpr int kTile = kR * kHS * 2;   // 16 KB: 128 rows of 128 bytes
 constexpr int kStages = 3;
+// Buffers of the fixed tiles: the S products run up to two tiles ahead,
+// which with one-tile items reaches the item after next; with three buffers
+// the one it needs was last used three items back, long released (with two
+// it is the current item's, released only after the products that wait for
+// it: a deadlock)
+constexpr int kFixed = 3;
 constexpr int kSmWarps = 8;
 constexpr int kThreads = 64 + 32 * kSmWarps;
 constexpr uint32_t kTmemCols = 512;
@@ -71,13 +77,14 @@ __device__ __forceinline__ float ex2(float x) {
 
 template <bool kDQ>
 struct BwdSmem {
-  static constexpr int fixed = 0;                                 // two tiles
-  static constexpr int stage = fixed + 2 * kTile;                 // kStages x two tiles
+  static constexpr int fixed = 0;                                 // kFixed buffers of two tiles
+  static constexpr int stage = fixed + kFixed * 2 * kTile;        // kStages x two tiles
   static constexpr int stats = stage + kStages * 2 * kTile;       // dK/dV: kStages x (L'[128], D[128])
   static constexpr int bars = stats + (kDQ ? 0 : kStages * 2 * kR * 4);
-  // fixed_full; st_full[kStages], st_empty[kStages]; s_full[2]; dp_full,
-  // p_full, ds_full, acc_done, drain
-  static constexpr int n_bars = 1 + 2 * kStages + 2 + 5;
+  // fixed_full[kFixed], fixed_empty[kFixed]; st_full[kStages],
+  // st_empty[kStages]; s_full[2]; dp_full, p_full, p_empty, ds_full,
+  // acc_done, acc_free, drain
+  static constexpr int n_bars = 2 * kFixed + 2 * kStages + 2 + 7;
   static constexpr int misc = bars + n_bars * 8;
   static constexpr int total = misc + 16;
   static constexpr int alloc = total + 1024;
@@ -102,53 +109,110 @@ __device__ __forceinline__ void mma_rows(uint32_t d, uint32_t a_tmem, uint32_t b
     tc_mma_ts_warp(d, a_tmem + kk * 8, bd + kk * (2048 / 16), kIdescAcc, (!first || kk > 0) ? 1u : 0u);
 }
 
-// kDQ = false: the dK/dV kernel (blockIdx.x = key tile, longest first);
-// kDQ = true: the dQ kernel (blockIdx.x counts query tiles from the last).
-// qkv map: [B][T][3C] bf16, do map: [B][T][C] bf16, boxes of 64 x 128 with
-// the 128-byte swizzle.  Lse, Dv: [B][NH][Tp] fp32, Tp = T rounded up to 128,
-// zero past T.
+// Work items: a fixed tile of one (sequence, head), numbered by decreasing
+// length (the number of streamed tiles), then b, then h; CTA c of G takes
+// items c, 2G - 1 - c, 2G + c, ... (alternate rounds backwards).
+template <bool kDQ>
+struct BwdItems {
+  int c, G, n_items, per, NH, n_tiles;
+  __device__ int id(int i) const {
+    const int k = i * G + ((i & 1) ? G - 1 - c : c);
+    return k < n_items ? k : -1;
+  }
+  // dK/dV: key tile ft, streamed query tiles ft .. n_tiles - 1; dQ: query
+  // tile ft, streamed key tiles 0 .. ft
+  __device__ void get(int k, int& ft, int& b, int& h, int& n) const {
+    const int r = k / per, bh = k % per;
+    b = bh / NH;
+    h = bh % NH;
+    ft = kDQ ? n_tiles - 1 - r : r;
+    n = kDQ ? ft + 1 : n_tiles - ft;
+  }
+  __device__ int length(int k) const { return n_tiles - k / per; }  // longest first: r = 0 streams all tiles
+};
+
+// A position in a CTA's sequence of streamed tiles over its items: item i
+// (list index), its tile u of n, and the tiles before the item (g0).
+template <bool kDQ>
+struct BwdCursor {
+  const BwdItems<kDQ>* it;
+  int i, k, u, g0, n;
+  __device__ explicit BwdCursor(const BwdItems<kDQ>* items) : it(items), i(0), u(0), g0(0), n(0) {
+    k = it->id(0);
+    if (k >= 0) n = it->length(k);
+  }
+  __device__ bool valid() const { return k >= 0; }
+  __device__ int g() const { return g0 + u; }
+  __device__ void advance() {
+    if (++u < n) return;
+    g0 += n;
+    u = 0;
+    k = it->id(++i);
+    if (k >= 0) n = it->length(k);
+  }
+};
+
+// kDQ = false: the dK/dV kernel; kDQ = true: the dQ kernel.  Persistent:
+// one CTA per SM over its items, the fixed tiles of the next item loading
+// into a second buffer, the streamed tiles' ring and the TMEM buffers
+// continuing across items (measured: a CTA per item spent about 5800 cycles
+// before its first S).  qkv map: [B][T][3C] bf16, do map: [B][T][C] bf16,
+// boxes of 64 x 128 with the 128-byte swizzle.  Lse (L + 3), Dv:
+// [B][NH][Tp] fp32, Tp = T rounded up to 128, zero past T.
 template <bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ CUtensorMap tmap_do,
-                         float* __restrict__ dqkv, const float* __restrict__ Lse, const float* __restrict__ Dv, int T,
-                         int C, int Tp, float scale_log2) {
+                         float* __restrict__ dqkv, const float* __restrict__ Lse, const float* __restrict__ Dv, int B,
+                         int T, int NH, int Tp, float scale_log2) {
   using L = BwdSmem<kDQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bars);
-  uint64_t* fixed_full = bars;
-  uint64_t* st_full = bars + 1;           // [kStages] a streamed tile pair (and its L, D) landed
-  uint64_t* st_empty = st_full + kStages; // [kStages] its last reader is done
-  uint64_t* s_full = st_empty + kStages;  // [2] S of tile u in buffer u % 2
-  uint64_t* dp_full = s_full + 2;         // dP of tile u (phase u % 2)
-  uint64_t* p_full = dp_full + 1;         // the P warps have written P^T of tile u into TMEM (dK/dV)
-  uint64_t* ds_full = p_full + 1;         // ... read dP and written dS of tile u into TMEM
-  uint64_t* acc_done = ds_full + 1;       // the accumulators are final
-  uint64_t* drain = acc_done + 1;
+  uint64_t* fixed_full = bars;                  // [kFixed] the fixed tiles of item i (buffer i % kFixed) landed
+  uint64_t* fixed_empty = fixed_full + kFixed;  // [kFixed] item i's products have read them
+  uint64_t* st_full = fixed_empty + kFixed;     // [kStages] a streamed tile pair (and its L, D) landed
+  uint64_t* st_empty = st_full + kStages;  // [kStages] its last reader is done
+  uint64_t* s_full = st_empty + kStages;   // [2] S of tile g in buffer g % 2
+  uint64_t* dp_full = s_full + 2;          // dP of tile g (phase g % 2)
+  uint64_t* p_full = dp_full + 1;          // the P warps have written P^T of tile g into TMEM (dK/dV)
+  // dV of tile g is done (dK/dV): the P warps wait for it before writing P^T
+  // of tile g + 1, so that p_full is never two phases ahead of the MMA warp
+  // (P^T of g + 1 needs only S of g + 1, issued before dV of g)
+  uint64_t* p_empty = p_full + 1;
+  uint64_t* ds_full = p_empty + 1;         // ... read dP and written dS of tile g into TMEM
+  uint64_t* acc_done = ds_full + 1;        // item i's accumulators are final (phase i % 2)
+  uint64_t* acc_free = acc_done + 1;       // ... and read by the epilogue
+  uint64_t* drain = acc_free + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::misc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = (T + kR - 1) / kR;
-  const int h = blockIdx.y, b = blockIdx.z, NH = gridDim.y;
-  // fixed tile index; streamed tiles: dK/dV: i = ft + u, u < n_tiles - ft;
-  // dQ: j = u, u <= ft
-  const int ft = kDQ ? n_tiles - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int n = kDQ ? ft + 1 : n_tiles - ft;
-  const size_t bh = static_cast<size_t>(b) * NH + h;
+  const int C = NH * kHS;
+  BwdItems<kDQ> items;
+  items.c = blockIdx.x;
+  items.G = gridDim.x;
+  items.NH = NH;
+  items.per = B * NH;
+  items.n_tiles = (T + kR - 1) / kR;
+  items.n_items = items.n_tiles * items.per;
 
   if (threadIdx.x == 0) {
-    mbar_init(fixed_full, 1u);
+    for (int i = 0; i < kFixed; ++i) {
+      mbar_init(&fixed_full[i], 1u);
+      mbar_init(&fixed_empty[i], 1u);
+    }
+    mbar_init(&s_full[0], 1u);
+    mbar_init(&s_full[1], 1u);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&st_full[i], 1u);
       mbar_init(&st_empty[i], 1u);
     }
-    mbar_init(&s_full[0], 1u);
-    mbar_init(&s_full[1], 1u);
     mbar_init(dp_full, 1u);
     mbar_init(p_full, kSmWarps);
+    mbar_init(p_empty, 1u);
     mbar_init(ds_full, kSmWarps);
     mbar_init(acc_done, 1u);
+    mbar_init(acc_free, kSmWarps);
     mbar_init(drain, 1u);
     *abort_flag = 0;
     fence_barrier_init();
@@ -169,96 +233,145 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ loads
     if (lane == 0) {
-      // fixed: K_j, V_j (dK/dV) or Q_i, dO_i (dQ)
-      mbar_arrive_expect_tx(fixed_full, 2 * kTile);
-      if (!kDQ) {
-        tma_load_3d(smem + L::fixed, &tmap_qkv, fixed_full, C + h * kHS, ft * kR, b);
-        tma_load_3d(smem + L::fixed + kTile, &tmap_qkv, fixed_full, 2 * C + h * kHS, ft * kR, b);
-      } else {
-        tma_load_3d(smem + L::fixed, &tmap_qkv, fixed_full, h * kHS, ft * kR, b);
-        tma_load_3d(smem + L::fixed + kTile, &tmap_do, fixed_full, h * kHS, ft * kR, b);
-      }
-      uint32_t filled = 0, par = 0;  // per stage: ever filled; parity of the last fill
-      for (int u = 0; u < n && !*abort_flag; ++u) {
-        const int st = u % kStages;
-        const uint32_t ph = (u / kStages) & 1;
-        if (!mbar_wait(&st_empty[st], ph ^ 1)) {
+      uint32_t filled = 0, par = 0;    // per stage: ever filled; parity of the last fill
+      uint32_t ffilled = 0, fpar = 0;  // the same per fixed buffer
+      int f = 0;                       // streamed tile pairs loaded so far
+      for (int i = 0;; ++i) {
+        const int k = items.id(i);
+        if (k < 0 || *abort_flag) break;
+        int ft, b, h, n;
+        items.get(k, ft, b, h, n);
+        const size_t bh = static_cast<size_t>(b) * NH + h;
+        // fixed: K_j, V_j (dK/dV) or Q_i, dO_i (dQ), into buffer i % kFixed
+        // once item i - kFixed's products have read it
+        const int fb = i % kFixed;
+        const uint32_t fph = (i / kFixed) & 1;
+        if (!mbar_wait(&fixed_empty[fb], fph ^ 1)) {
           *abort_flag = 1;
           break;
         }
-        uint8_t* dst = smem + L::stage + st * 2 * kTile;
-        if (!kDQ) {  // Q_i, dO_i, L and D of query tile i
-          const int i = ft + u;
-          mbar_arrive_expect_tx(&st_full[st], 2 * kTile + 2 * kR * 4);
-          tma_load_3d(dst, &tmap_qkv, &st_full[st], h * kHS, i * kR, b);
-          tma_load_3d(dst + kTile, &tmap_do, &st_full[st], h * kHS, i * kR, b);
-          float* sd = reinterpret_cast<float*>(smem + L::stats) + st * 2 * kR;
-          bulk_load(sd, Lse + bh * Tp + static_cast<size_t>(i) * kR, kR * 4, &st_full[st]);
-          bulk_load(sd + kR, Dv + bh * Tp + static_cast<size_t>(i) * kR, kR * 4, &st_full[st]);
-        } else {  // K_j, V_j
-          mbar_arrive_expect_tx(&st_full[st], 2 * kTile);
-          tma_load_3d(dst, &tmap_qkv, &st_full[st], C + h * kHS, u * kR, b);
-          tma_load_3d(dst + kTile, &tmap_qkv, &st_full[st], 2 * C + h * kHS, u * kR, b);
+        uint8_t* fdst = smem + L::fixed + fb * 2 * kTile;
+        mbar_arrive_expect_tx(&fixed_full[fb], 2 * kTile);
+        if (!kDQ) {
+          tma_load_3d(fdst, &tmap_qkv, &fixed_full[fb], C + h * kHS, ft * kR, b);
+          tma_load_3d(fdst + kTile, &tmap_qkv, &fixed_full[fb], 2 * C + h * kHS, ft * kR, b);
+        } else {
+          tma_load_3d(fdst, &tmap_qkv, &fixed_full[fb], h * kHS, ft * kR, b);
+          tma_load_3d(fdst + kTile, &tmap_do, &fixed_full[fb], h * kHS, ft * kR, b);
         }
-        filled |= 1u << st;
-        par = (par & ~(1u << st)) | (ph << st);
+        ffilled |= 1u << fb;
+        fpar = (fpar & ~(1u << fb)) | (fph << fb);
+        bool ok = true;
+        for (int u = 0; u < n; ++u, ++f) {
+          const int st = f % kStages;
+          const uint32_t ph = (f / kStages) & 1;
+          if (!mbar_wait(&st_empty[st], ph ^ 1)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = smem + L::stage + st * 2 * kTile;
+          if (!kDQ) {  // Q_i, dO_i, L' and D of query tile i
+            const int qi = ft + u;
+            mbar_arrive_expect_tx(&st_full[st], 2 * kTile + 2 * kR * 4);
+            tma_load_3d(dst, &tmap_qkv, &st_full[st], h * kHS, qi * kR, b);
+            tma_load_3d(dst + kTile, &tmap_do, &st_full[st], h * kHS, qi * kR, b);
+            float* sd = reinterpret_cast<float*>(smem + L::stats) + st * 2 * kR;
+            bulk_load(sd, Lse + bh * Tp + static_cast<size_t>(qi) * kR, kR * 4, &st_full[st]);
+            bulk_load(sd + kR, Dv + bh * Tp + static_cast<size_t>(qi) * kR, kR * 4, &st_full[st]);
+          } else {  // K_j, V_j
+            mbar_arrive_expect_tx(&st_full[st], 2 * kTile);
+            tma_load_3d(dst, &tmap_qkv, &st_full[st], C + h * kHS, u * kR, b);
+            tma_load_3d(dst + kTile, &tmap_qkv, &st_full[st], 2 * C + h * kHS, u * kR, b);
+          }
+          filled |= 1u << st;
+          par = (par & ~(1u << st)) | (ph << st);
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
       }
       // the copies issued here land before the CTA may exit: this thread
-      // alone arms the full barriers, so the phase of a stage's last fill
+      // alone arms the full barriers, so the phase of a buffer's last fill
       // completes exactly when its bytes have landed
-      mbar_wait(fixed_full, 0);
+      for (int fb = 0; fb < kFixed; ++fb)
+        if ((ffilled >> fb) & 1u) mbar_wait(&fixed_full[fb], (fpar >> fb) & 1u);
       for (int st = 0; st < kStages; ++st)
         if ((filled >> st) & 1u) mbar_wait(&st_full[st], (par >> st) & 1u);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMAs
-    const uint32_t fixed0 = smem_u32(smem + L::fixed), fixed1 = fixed0 + kTile;
-    auto stream0 = [&](int u) { return smem_u32(smem + L::stage + (u % kStages) * 2 * kTile); };
-    auto stream1 = [&](int u) { return stream0(u) + kTile; };
-    auto wait_stage = [&](int u) {
-      return __all_sync(0xffffffffu, mbar_wait(&st_full[u % kStages], (u / kStages) & 1));
-    };
-    auto issue_s = [&](int u) {  // S of tile u into buffer u % 2
+    // The CTA's tiles in one sequence over its items: a cursor for S (two
+    // tiles ahead), one for dP (one ahead), one for the gradient products.
+    auto fixed0 = [&](int i) { return smem_u32(smem + L::fixed + (i % kFixed) * 2 * kTile); };
+    auto stream0 = [&](int f) { return smem_u32(smem + L::stage + (f % kStages) * 2 * kTile); };
+    // S of the cursor's tile into buffer g % 2 (the item's first waits for
+    // its fixed tiles; every S waits for its streamed pair)
+    auto issue_s = [&](const BwdCursor<kDQ>& c) -> bool {
+      const int g = c.g();
+      if (c.u == 0 && !__all_sync(0xffffffffu, mbar_wait(&fixed_full[c.i % kFixed], (c.i / kFixed) & 1)))
+        return false;
+      if (!__all_sync(0xffffffffu, mbar_wait(&st_full[g % kStages], (g / kStages) & 1))) return false;
       tc_fence_after();
-      mma_dim(tmem + kTmemS + (u & 1) * kR, fixed0, stream0(u));
-      tc_commit_warp(&s_full[u & 1]);
+      mma_dim(tmem + kTmemS + (g & 1) * kR, fixed0(c.i), stream0(g));
+      tc_commit_warp(&s_full[g & 1]);
+      return true;
     };
-    auto issue_dp = [&](int u) {
-      mma_dim(tmem + kTmemDP, fixed1, stream1(u));
+    // dP of the cursor's tile (its S, issued earlier, waited for its loads)
+    auto issue_dp = [&](const BwdCursor<kDQ>& c) {
+      const int g = c.g();
+      mma_dim(tmem + kTmemDP, fixed0(c.i) + kTile, stream0(g) + kTile);
       tc_commit_warp(dp_full);
     };
-    bool ok = __all_sync(0xffffffffu, mbar_wait(fixed_full, 0));
-    if (ok) ok = wait_stage(0);
-    if (ok) {
-      issue_s(0);
-      issue_dp(0);
+    BwdCursor<kDQ> cs(&items), cd(&items);
+    bool ok = true;
+    if (cs.valid()) {
+      ok = issue_s(cs);
+      cs.advance();
     }
-    if (ok && n > 1) ok = wait_stage(1);
-    if (ok && n > 1) issue_s(1);
-    for (int u = 0; u < n && ok; ++u) {
+    if (ok && cd.valid()) {
+      issue_dp(cd);
+      cd.advance();
+    }
+    if (ok && cs.valid()) {
+      ok = issue_s(cs);
+      cs.advance();
+    }
+    for (BwdCursor<kDQ> c(&items); c.valid() && ok; c.advance()) {
+      const int g = c.g();
+      // the item's first gradient product overwrites the accumulators: the
+      // previous item's epilogue must have read them
+      if (c.u == 0 && c.i > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(acc_free, (c.i - 1) & 1)))) break;
       if (!kDQ) {
-        // dV += P'^T dO_i once P^T is in TMEM over S^T of tile u; S of tile
-        // u + 2 then goes into that buffer (the products run in issue order)
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, u & 1)))) break;
+        // dV += P'^T dO_i once P^T is in TMEM over S^T of tile g; S two tiles
+        // on then goes into that buffer (the products run in issue order)
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(p_full, g & 1)))) break;
         tc_fence_after();
-        mma_rows(tmem + kTmemAcc, tmem + kTmemS + (u & 1) * kR, stream1(u), u == 0);
-        if (u + 2 < n) {
-          if (!(ok = wait_stage(u + 2))) break;
-          issue_s(u + 2);
+        mma_rows(tmem + kTmemAcc, tmem + kTmemS + (g & 1) * kR, stream0(g) + kTile, c.u == 0);
+        tc_commit_warp(p_empty);
+        if (cs.valid()) {
+          if (!(ok = issue_s(cs))) break;
+          cs.advance();
         }
       }
       // dS in TMEM over dP: dK += dS^T Q_i (or dQ += dS K_j), then dP of the
       // next tile into the same columns (issued after: the products run in
       // issue order)
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_full, u & 1)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(ds_full, g & 1)))) break;
       tc_fence_after();
-      mma_rows(tmem + kTmemAcc + (kDQ ? 0 : kHS), tmem + kTmemDP, stream0(u), u == 0);
-      tc_commit_warp(&st_empty[u % kStages]);
-      if (u == n - 1) tc_commit_warp(acc_done);
-      if (u + 1 < n) issue_dp(u + 1);
-      if (kDQ && u + 2 < n) {  // S of tile u was read before dS was formed
-        if (!(ok = wait_stage(u + 2))) break;
-        issue_s(u + 2);
+      mma_rows(tmem + kTmemAcc + (kDQ ? 0 : kHS), tmem + kTmemDP, stream0(g), c.u == 0);
+      tc_commit_warp(&st_empty[g % kStages]);
+      if (c.u == c.n - 1) {
+        tc_commit_warp(acc_done);
+        tc_commit_warp(&fixed_empty[c.i % kFixed]);
+      }
+      if (cd.valid()) {
+        issue_dp(cd);
+        cd.advance();
+      }
+      if (kDQ && cs.valid()) {  // S of tile g was read before dS was formed
+        if (!(ok = issue_s(cs))) break;
+        cs.advance();
       }
     }
     if (!ok && lane == 0) *abort_flag = 1;
@@ -273,159 +386,186 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = hf * 64;
     const int pair_bar = 1 + qw;    // the named barrier of this quadrant's two warps
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    float l_row = 0.f, d_row = 0.f;  // dQ kernel: the row's L' and D
-    if (kDQ) {
-      const size_t at = bh * Tp + static_cast<size_t>(ft) * kR + row;
-      l_row = __ldg(Lse + at);
-      d_row = __ldg(Dv + at);
-    }
     bool ok = true;
-    for (int u = 0; u < n; ++u) {
-      const int sb = u & 1;
-      bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (u >> 1) & 1));
-      const float* stats = nullptr;  // dK/dV: L' and D of the query tile, per column
-      if (!kDQ) {
-        // (complete already: S of tile u was issued after it)
-        got = __all_sync(0xffffffffu, got && mbar_wait(&st_full[u % kStages], (u / kStages) & 1));
-        stats = reinterpret_cast<const float*>(smem + L::stats) + (u % kStages) * 2 * kR;
+    int g0 = 0;  // tiles of the items before this one
+    for (int i = 0; ok; ++i) {
+      const int k = items.id(i);
+      if (k < 0) break;
+      int ft, b, h, n;
+      items.get(k, ft, b, h, n);
+      const size_t bh = static_cast<size_t>(b) * NH + h;
+      const int f0 = g0;  // the streamed pairs run with the tiles
+      float l_row = 0.f, d_row = 0.f;  // dQ kernel: the row's L' and D
+      if (kDQ) {
+        const size_t at = bh * Tp + static_cast<size_t>(ft) * kR + row;
+        l_row = __ldg(Lse + at);
+        d_row = __ldg(Dv + at);
       }
-      // visible columns [lo, hi) of this row
-      int lo, hi;
-      if (!kDQ) {  // row = key ft * 128 + row; column = query (ft + u) * 128 + c: c >= row on the diagonal, < T
-        lo = u == 0 ? row : 0;
-        hi = min(T - (ft + u) * kR, kR);
-      } else {  // row = query ft * 128 + row; column = key u * 128 + c <= query
-        lo = 0;
-        hi = max(0, min(ft * kR + row - u * kR + 1, kR));
-      }
-      const bool all_valid = lo <= col0 && hi >= col0 + 64;
-      uint32_t sv[2][32];
-      if (got) {
-        tc_fence_after();
-        tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0, sv[0]);
-        tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0 + 32, sv[1]);
-        tmem_ld_wait();
-      }
-      // both warps of the quadrant have read their S columns (or one gave up)
-      if (bar_or(pair_bar, 64, !got)) {
-        ok = false;
-        break;
-      }
-      // P' = exp2(S log2(e)/8 - L'), zero outside [lo, hi); kept in sv as fp32
-      const float2 sc = make_float2(scale_log2, scale_log2);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float4 nl4;
-          if (kDQ) {
-            nl4 = make_float4(-l_row, -l_row, -l_row, -l_row);
-          } else {
-            const float4 lv = *reinterpret_cast<const float4*>(stats + col0 + c * 32 + e);
-            nl4 = make_float4(-lv.x, -lv.y, -lv.z, -lv.w);
-          }
-          float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sc,
-                                 make_float2(nl4.x, nl4.y));
-          float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), sc,
-                                 make_float2(nl4.z, nl4.w));
-          if (!all_valid) {
-            const int cc = col0 + c * 32 + e;
-            if (cc < lo || cc >= hi) x0.x = -INFINITY;
-            if (cc + 1 < lo || cc + 1 >= hi) x0.y = -INFINITY;
-            if (cc + 2 < lo || cc + 2 >= hi) x1.x = -INFINITY;
-            if (cc + 3 < lo || cc + 3 >= hi) x1.y = -INFINITY;
-          }
-          sv[c][e] = __float_as_uint(ex2(x0.x));
-          sv[c][e + 1] = __float_as_uint(ex2(x0.y));
-          sv[c][e + 2] = __float_as_uint(ex2(x1.x));
-          sv[c][e + 3] = __float_as_uint(ex2(x1.y));
+      for (int u = 0; u < n && ok; ++u) {
+        const int g = g0 + u, f = f0 + u;  // this tile's place in the CTA's sequence
+        const int sb = g & 1;
+        bool got = __all_sync(0xffffffffu, mbar_wait(&s_full[sb], (g >> 1) & 1));
+        const float* stats = nullptr;  // dK/dV: L' and D of the query tile, per column
+        if (!kDQ) {
+          // (complete already: S of tile u was issued after it)
+          got = __all_sync(0xffffffffu, got && mbar_wait(&st_full[f % kStages], (f / kStages) & 1));
+          stats = reinterpret_cast<const float*>(smem + L::stats) + (f % kStages) * 2 * kR;
         }
-      }
-      if (!kDQ) {
-        // P'^T (bf16 pairs) over this warp's half of the first 64 columns of
-        // S^T's buffer: the A operand of dV
-        uint32_t pk[32];
+        // visible columns [lo, hi) of this row
+        int lo, hi;
+        if (!kDQ) {  // row = key ft * 128 + row; column = query (ft + u) * 128 + c: c >= row on the diagonal, < T
+          lo = u == 0 ? row : 0;
+          hi = min(T - (ft + u) * kR, kR);
+        } else {  // row = query ft * 128 + row; column = key u * 128 + c <= query
+          lo = 0;
+          hi = max(0, min(ft * kR + row - u * kR + 1, kR));
+        }
+        const bool all_valid = lo <= col0 && hi >= col0 + 64;
+        uint32_t sv[2][32];
+        if (got) {
+          tc_fence_after();
+          tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0, sv[0]);
+          tmem_ld_32x32b_x32(lane_base + kTmemS + sb * kR + col0 + 32, sv[1]);
+          tmem_ld_wait();
+        }
+        // both warps of the quadrant have read their S columns (or one gave up)
+        if (bar_or(pair_bar, 64, !got)) {
+          ok = false;
+          break;
+        }
+        // P' = exp2(S log2(e)/8 - L'), zero outside [lo, hi); kept in sv as fp32
+        const float2 sc = make_float2(scale_log2, scale_log2);
+  #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+  #pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 nl4;
+            if (kDQ) {
+              nl4 = make_float4(-l_row, -l_row, -l_row, -l_row);
+            } else {
+              const float4 lv = *reinterpret_cast<const float4*>(stats + col0 + c * 32 + e);
+              nl4 = make_float4(-lv.x, -lv.y, -lv.z, -lv.w);
+            }
+            float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), sc,
+                                   make_float2(nl4.x, nl4.y));
+            float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), sc,
+                                   make_float2(nl4.z, nl4.w));
+            if (!all_valid) {
+              const int cc = col0 + c * 32 + e;
+              if (cc < lo || cc >= hi) x0.x = -INFINITY;
+              if (cc + 1 < lo || cc + 1 >= hi) x0.y = -INFINITY;
+              if (cc + 2 < lo || cc + 2 >= hi) x1.x = -INFINITY;
+              if (cc + 3 < lo || cc + 3 >= hi) x1.y = -INFINITY;
+            }
+            sv[c][e] = __float_as_uint(ex2(x0.x));
+            sv[c][e + 1] = __float_as_uint(ex2(x0.y));
+            sv[c][e + 2] = __float_as_uint(ex2(x1.x));
+            sv[c][e + 3] = __float_as_uint(ex2(x1.y));
+          }
+        }
+        bool p_ok = true;
+        if (!kDQ) {
+          // P'^T (bf16 pairs) over this warp's half of the first 64 columns of
+          // S^T's buffer: the A operand of dV (once dV of the CTA's previous
+          // tile is done: p_empty)
+          uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(sv[e >> 4][(e & 15) * 2]), __uint_as_float(sv[e >> 4][(e & 15) * 2 + 1]));
-        tmem_st_32x32b_x32(lane_base + kTmemS + sb * kR + hf * 32, pk);
+          for (int e = 0; e < 32; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(sv[e >> 4][(e & 15) * 2]), __uint_as_float(sv[e >> 4][(e & 15) * 2 + 1]));
+          if (g > 0) p_ok = __all_sync(0xffffffffu, mbar_wait(p_empty, (g - 1) & 1));
+          if (p_ok) {
+            tmem_st_32x32b_x32(lane_base + kTmemS + sb * kR + hf * 32, pk);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+          }
+        }
+        // dS' = P' (dP - D), one 32-column chunk of dP at a time; the second
+        // chunk's load completes this warp's reads of dP before the barrier
+        // (a wait given up above reaches the quadrant's barrier below as a failure)
+        got = p_ok && __all_sync(0xffffffffu, mbar_wait(dp_full, g & 1));
+        if (got) tc_fence_after();
+        uint32_t pk[32];
+        bool gave_up = false;
+  #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dv[32];
+          if (got) {
+            tmem_ld_32x32b_x32(lane_base + kTmemDP + col0 + c * 32, dv);
+            tmem_ld_wait();
+          }
+          if (c == 1 && bar_or(pair_bar, 64, !got)) {  // both warps of the quadrant have read their dP
+            gave_up = true;
+            break;
+          }
+  #pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            float4 d4;
+            if (kDQ) {
+              d4 = make_float4(d_row, d_row, d_row, d_row);
+            } else {
+              d4 = *reinterpret_cast<const float4*>(stats + kR + col0 + c * 32 + e);
+            }
+            const float2 g0 = __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                         make_float2(-d4.x, -d4.y));
+            const float2 g1 = __fadd2_rn(make_float2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
+                                         make_float2(-d4.z, -d4.w));
+            const float2 q0 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), g0);
+            const float2 q1 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), g1);
+            pk[c * 16 + e / 2] = pack_bf16x2(q0.x, q0.y);
+            pk[c * 16 + e / 2 + 1] = pack_bf16x2(q1.x, q1.y);
+          }
+        }
+        if (gave_up) {
+          ok = false;
+          break;
+        }
+        tmem_st_32x32b_x32(lane_base + kTmemDP + hf * 32, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(ds_full);
       }
-      // dS' = P' (dP - D), one 32-column chunk of dP at a time; the second
-      // chunk's load completes this warp's reads of dP before the barrier
-      got = __all_sync(0xffffffffu, mbar_wait(dp_full, u & 1));
-      if (got) tc_fence_after();
-      uint32_t pk[32];
-      bool gave_up = false;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dv[32];
-        if (got) {
-          tmem_ld_32x32b_x32(lane_base + kTmemDP + col0 + c * 32, dv);
-          tmem_ld_wait();
-        }
-        if (c == 1 && bar_or(pair_bar, 64, !got)) {  // both warps of the quadrant have read their dP
-          gave_up = true;
-          break;
-        }
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float4 d4;
-          if (kDQ) {
-            d4 = make_float4(d_row, d_row, d_row, d_row);
-          } else {
-            d4 = *reinterpret_cast<const float4*>(stats + kR + col0 + c * 32 + e);
-          }
-          const float2 g0 = __fadd2_rn(make_float2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
-                                       make_float2(-d4.x, -d4.y));
-          const float2 g1 = __fadd2_rn(make_float2(__uint_as_float(dv[e + 2]), __uint_as_float(dv[e + 3])),
-                                       make_float2(-d4.z, -d4.w));
-          const float2 q0 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), g0);
-          const float2 q1 = __fmul2_rn(make_float2(__uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3])), g1);
-          pk[c * 16 + e / 2] = pack_bf16x2(q0.x, q0.y);
-          pk[c * 16 + e / 2 + 1] = pack_bf16x2(q1.x, q1.y);
-        }
-      }
-      if (gave_up) {
+      if (!ok) break;
+      // both warps of the quadrant agree on the outcome before either goes
+      // on to the next item's barriers
+      const bool acc_ok = __all_sync(0xffffffffu, mbar_wait(acc_done, i & 1));
+      if (bar_or(pair_bar, 64, !acc_ok)) {
         ok = false;
         break;
       }
-      tmem_st_32x32b_x32(lane_base + kTmemDP + hf * 32, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0));
-    if (ok) {
-      tc_fence_after();
-      // dK/dV: warps of half 0 write dV, half 1 dK (64 columns each); dQ:
-      // each half 32 of dQ's columns
-      const int r_glob = ft * kR + row;
-      const int n_chunks = kDQ ? 1 : 2;
-      const uint32_t t_col = kTmemAcc + (kDQ ? hf * 32 : hf * kHS);
-      const int g_col = kDQ ? h * kHS + hf * 32 : (hf == 0 ? 2 * C : C) + h * kHS;
-#pragma unroll 1
-      for (int c = 0; c < n_chunks; ++c) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(lane_base + t_col + c * 32, o);
-        tmem_ld_wait();
-        if (r_glob < T) {
-          float* dst = dqkv + (static_cast<size_t>(b) * T + r_glob) * 3 * C + g_col + c * 32;
-          const float f = (!kDQ && hf == 0) ? 8.0f : 1.0f;  // dV accumulated P' = P / 8
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(dst)[q] =
-                make_float4(__uint_as_float(o[4 * q]) * f, __uint_as_float(o[4 * q + 1]) * f,
-                            __uint_as_float(o[4 * q + 2]) * f, __uint_as_float(o[4 * q + 3]) * f);
+      {
+        tc_fence_after();
+        // dK/dV: warps of half 0 write dV, half 1 dK (64 columns each); dQ:
+        // each half 32 of dQ's columns
+        const int r_glob = ft * kR + row;
+        const int n_chunks = kDQ ? 1 : 2;
+        const uint32_t t_col = kTmemAcc + (kDQ ? hf * 32 : hf * kHS);
+        const int g_col = kDQ ? h * kHS + hf * 32 : (hf == 0 ? 2 * C : C) + h * kHS;
+  #pragma unroll 1
+        for (int c = 0; c < n_chunks; ++c) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(lane_base + t_col + c * 32, o);
+          tmem_ld_wait();
+          if (r_glob < T) {
+            float* dst = dqkv + (static_cast<size_t>(b) * T + r_glob) * 3 * C + g_col + c * 32;
+            const float f = (!kDQ && hf == 0) ? 8.0f : 1.0f;  // dV accumulated P' = P / 8
+  #pragma unroll
+            for (int q = 0; q < 8; ++q)
+              reinterpret_cast<float4*>(dst)[q] =
+                  make_float4(__uint_as_float(o[4 * q]) * f, __uint_as_float(o[4 * q + 1]) * f,
+                              __uint_as_float(o[4 * q + 2]) * f, __uint_as_float(o[4 * q + 3]) * f);
+          }
         }
+        // the accumulators have been read: the next item may overwrite them
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_free);
       }
-    } else {
-      *abort_flag = 1;
+      g0 += n;
     }
+    if (!ok) *abort_flag = 1;
   }
 
   tc_fence_before();
@@ -522,11 +662,21 @@ int launch_attention_backward_tc05(float* dqkv, const void* qkv16, const void* d
   }
   const int Tp = attn_bwd_padded_len(T);
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // log2(e) / sqrt(64)
-  const dim3 grid((T + kR - 1) / kR, NH, B);
-  attn_bwd_tc05_kernel<false><<<grid, kThreads, BwdSmem<false>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
-                                                                            scale_log2);
-  attn_bwd_tc05_kernel<true><<<grid, kThreads, BwdSmem<true>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, T, C, Tp,
-                                                                          scale_log2);
+  // persistent: one CTA per SM (at most one per item)
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GPT2_ERR_CUDA;
+  if (sms[dev] == 0) {
+    const cudaError_t e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return note_cuda_error(e);
+  }
+  const long long n_items = static_cast<long long>((T + kR - 1) / kR) * B * NH;
+  if (n_items > 0x7fffffffLL) return GPT2_ERR_SHAPE;
+  const dim3 grid(static_cast<unsigned>(n_items < sms[dev] ? n_items : sms[dev]));
+  attn_bwd_tc05_kernel<false><<<grid, kThreads, BwdSmem<false>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, B, T, NH,
+                                                                            Tp, scale_log2);
+  attn_bwd_tc05_kernel<true><<<grid, kThreads, BwdSmem<true>::alloc, s>>>(map_qkv, map_do, dqkv, Lse, Dv, B, T, NH,
+                                                                          Tp, scale_log2);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
