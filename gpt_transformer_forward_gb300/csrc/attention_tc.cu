@@ -47,14 +47,18 @@
 //               scale - m) with the running maximum m as it stands (on the
 //               first tile, the maximum of its first chunk), rounded to the
 //               16-bit type into TMEM over the chunk's S columns already read
-//               (the A operand of P V), and the running sum.  A score above
-//               m + 8 (log2 units) in chunk c stops the pass: the maximum of
+//               (the A operand of P V), and the running sum.  A chunk c whose
+//               exponentials sum above 2^8 in a row (as any score above m + 8,
+//               log2 units, makes them) stops the pass: the maximum of
 //               chunks c.. (those before it are below m + 8), the rescale of
 //               O in TMEM, of the sum and of the P chunks already written by
-//               2^(m - m_new) (values that shrink by more than 2^8, so their
-//               second rounding is negligible), then the exponentials of
+//               2^(m - m_new) where it grows by more than 8 (values that
+//               shrink by more than 2^8, so their second rounding is
+//               negligible), then the exponentials of
 //               chunks c...  Exact either way: the final division by the sum
-//               uses the same m as the numerators.  At the end each warp
+//               uses the same m as the numerators.  A unit's output is
+//               written after the group's first step of its next unit (or at
+//               the end), when the unit's last P V has finished: each warp
 //               stages its 32 rows of O / l in shared memory and writes them
 //               to [B, T, C] with one TMA store (rows past T are clipped):
 //               a thread storing its own row to global memory made every
@@ -82,6 +86,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;
 constexpr uint32_t kTmemO = kRing * kTK;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kRescaleSum = 256.0f;      // 2^kRescaleThreshold
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -373,6 +378,84 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     bool ok = true;
     int g0 = 0, before = 0;  // global steps and this group's units before the current unit
+    // A unit's output is written after this group's first step of its next
+    // unit (or at the end): by then the unit's last P V has long finished,
+    // where waiting for it right after the last step held the group up about
+    // 1700 cycles per unit (measured).  O is released as soon as it has been
+    // read (the next unit's first P V, which overwrites it, waits for that);
+    // O / l goes through the warp's staging rows to [B, T, C] with TMA
+    // stores.
+    struct Done {
+      int k;       // the unit (its number in the unit list), or -1: none pending
+      float m, l;  // its rows' final maximum and sum
+    };
+    Done pend{-1, 0.f, 0.f};
+    // `before` counts this group's units up to and including the pending
+    // one, whose o_final phase is therefore (before - 1) mod 2
+    auto epilogue = [&](Done& dn) -> bool {
+      const Unit d = ul.get(dn.k);
+      dn.k = -1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&o_final[x], (before - 1) & 1))) return false;
+      tc_fence_after();
+      const int t = (2 * d.u + x) * kTQ + row;
+      const float inv = 1.0f / dn.l;
+      // the row's log-sum-exp in log2 units, m + log2(l), for the backward
+      if (lse != nullptr && t < T) lse[(static_cast<size_t>(d.b) * NH + d.h) * Tp + t] = dn.m + __log2f(dn.l);
+      if (lane == 0) bulk_wait_group_read<0>();  // the previous unit's store has read the staging rows
+      __syncwarp();
+      // boxes of 32 rows x 128 bytes (64 16-bit or 32 fp32 columns) in the
+      // 128-byte swizzle the TMA store undoes (16-byte piece q of row r at
+      // position q ^ (r mod 8): the warp's stores spread over the banks)
+      constexpr int kBoxCols = 128 / static_cast<int>(sizeof(OutT));
+      constexpr int kBoxes = kHS / kBoxCols;
+      uint8_t* stg = smem + L::stage + (warp - 2) * L::kStageBytes;
+      auto stage = [&](int c, const uint32_t(&o)[32]) {  // columns 32 c .. 32 c + 31
+        if constexpr (std::is_same<OutT, float>::value) {  // one box row, 8 pieces
+          uint8_t* srow = stg + c * 4096 + lane * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(srow + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(__float_as_uint(__uint_as_float(o[4 * q + 0]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv),
+                           __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv));
+        } else {  // half a box row, pieces 4c .. 4c + 3
+          uint8_t* srow = stg + lane * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v;
+            v.x = pack2<T16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
+            v.y = pack2<T16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+            v.z = pack2<T16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
+            v.w = pack2<T16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+            *reinterpret_cast<uint4*>(srow + (((4 * c + q) ^ (lane & 7)) << 4)) = v;
+          }
+        }
+      };
+      {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(lane_base + kTmemO + x * kHS, o);
+        tmem_ld_wait_regs(o);
+        stage(0, o);
+        tmem_ld_32x32b_x32(lane_base + kTmemO + x * kHS + 32, o);
+        tmem_ld_wait_regs(o);
+        // O has been read: the next unit's P V may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&o_free[x]);
+        stage(1, o);
+      }
+      fence_proxy_async_smem();  // the staged rows become visible to the TMA store
+      __syncwarp();
+      const int row0 = (2 * d.u + x) * kTQ + qw * 32;  // the warp's first row; rows past T are clipped
+      if (lane == 0 && row0 < T) {
+#pragma unroll
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_store_3d(&tmap_out, stg + bx * 4096, d.h * kHS + bx * kBoxCols, row0, d.b);
+        bulk_commit_group();
+      }
+      return true;
+    };
     for (int i = 0; ok; ++i) {
       const int k = ul.id(i);
       if (k < 0) break;
@@ -407,11 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto store_p = [&](int c, const uint32_t(&pk)[16]) { tmem_st_32x32b_x16(lane_base + s_col + 16 * c, pk); };
         // x = s * scale - m for the 32 keys of a chunk (-inf for masked
         // keys), then p = exp2(x) on the SFU in fp32, rounded to the 16-bit
-        // type into P, and their fp32 sum added to sum2.  The exponentials do
-        // not wait for the overflow test: a chunk with a key above m + 8
-        // (log2 units; a maximum that must be raised) is computed, found, and
-        // neither stored nor summed, and the function returns false.  Four
-        // independent chains for the maximum and the sum keep the SFU fed.
+        // type into P, and their fp32 sum added to sum2.  A chunk whose
+        // exponentials sum to more than 2^8 in some row is neither stored nor
+        // summed, and the function returns false: every key above m + 8 (log2
+        // units; a maximum that must be raised) is caught so, since its own
+        // exponential is part of the sum, by one test on a sum the chunk
+        // forms anyway (a test of each key against m + 8 took 16 more
+        // instructions per chunk); a chunk caught without such a key is
+        // recomputed with the same m below.  Four independent chains for the
+        // sum keep the SFU fed.
         auto softmax_chunk = [&](int c, const uint32_t(&cur)[32], bool check) -> bool {
           const float2 sc = make_float2(scale_log2, scale_log2), nm = make_float2(-m_run, -m_run);
           float2 xv[16];
@@ -425,20 +512,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (c * 32 + 2 * i + 1 >= valid) xv[i].y = -INFINITY;
             }
           }
-          float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
           float2 sq[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
           uint32_t pk[16];
   #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            mq[i & 3] = fmax3(mq[i & 3], xv[i].x, xv[i].y);
             const float2 p = make_float2(ex2(xv[i].x), ex2(xv[i].y));
             sq[i & 3] = __fadd2_rn(sq[i & 3], p);
             pk[i] = pack2<T16>(p.x, p.y);
           }
-          if (check &&
-              __any_sync(0xffffffffu, fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) > kRescaleThreshold))
-            return false;
-          sum2 = __fadd2_rn(sum2, __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3])));
+          const float2 cs = __fadd2_rn(__fadd2_rn(sq[0], sq[1]), __fadd2_rn(sq[2], sq[3]));
+          if (check && __any_sync(0xffffffffu, cs.x + cs.y > kRescaleSum)) return false;
+          sum2 = __fadd2_rn(sum2, cs);
           store_p(c, pk);
           return true;
         };
@@ -451,9 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Single pass over the live chunks with the running maximum as it
         // stands, the next chunk's TMEM load in flight while one is
         // processed.  On the first tile the running maximum starts as the
-        // maximum of the first chunk's visible scores.  A score above m + 8
-        // (log2 units; a maximum that must be raised) stops it, and the rest
-        // of the tile is done below with the raised maximum.
+        // maximum of the first chunk's visible scores.  A chunk that may hold
+        // a score above m + 8 (log2 units; a maximum that must be raised)
+        // stops it, and the rest of the tile is done below with the maximum
+        // raised where it must be.
         bool done = false;
         int fail = kTK / 32;  // the chunk that stopped the single pass
         {
@@ -554,66 +639,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[r]);
+        if (j == 0 && pend.k >= 0 && !(ok = epilogue(pend))) break;
       }
-      if (ok && n_x > 0) ok = __all_sync(0xffffffffu, mbar_wait(&o_final[x], before & 1));
-      if (ok && n_x > 0) {
-        tc_fence_after();
-        const float inv = 1.0f / l_run;
-        // the row's log-sum-exp in log2 units, m + log2(l), for the backward
-        if (lse != nullptr && t < T) lse[(static_cast<size_t>(b) * NH + h) * Tp + t] = m_run + __log2f(l_run);
-        if (lane == 0) bulk_wait_group_read<0>();  // the previous unit's store has read the staging rows
-        __syncwarp();
-        // O / l of this thread's row into the warp's staging rows: boxes of
-        // 32 rows x 128 bytes (64 16-bit or 32 fp32 columns) in the 128-byte
-        // swizzle the TMA store undoes (16-byte piece q of row r at position
-        // q ^ (r mod 8): the warp's stores spread over the banks)
-        constexpr int kBoxCols = 128 / static_cast<int>(sizeof(OutT));
-        constexpr int kBoxes = kHS / kBoxCols;
-        uint8_t* stg = smem + L::stage + (warp - 2) * L::kStageBytes;
-  #pragma unroll 1
-        for (int c = 0; c < kHS / 32; ++c) {  // 32 columns at a time
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(lane_base + kTmemO + x * kHS + c * 32, o);
-          tmem_ld_wait();
-          if constexpr (std::is_same<OutT, float>::value) {  // 32 columns = one box row, 8 pieces
-            uint8_t* srow = stg + c * 4096 + lane * 128;
-  #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(srow + ((q ^ (lane & 7)) << 4)) =
-                  make_uint4(__float_as_uint(__uint_as_float(o[4 * q + 0]) * inv),
-                             __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv),
-                             __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv),
-                             __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv));
-          } else {  // 32 columns = half a box row, pieces 4c .. 4c + 3
-            uint8_t* srow = stg + lane * 128;
-  #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack2<T16>(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-              v.y = pack2<T16>(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-              v.z = pack2<T16>(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-              v.w = pack2<T16>(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
-              *reinterpret_cast<uint4*>(srow + (((4 * c + q) ^ (lane & 7)) << 4)) = v;
-            }
-          }
-        }
-        // O has been read: the next unit's P V may overwrite it
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&o_free[x]);
-        fence_proxy_async_smem();  // the staged rows become visible to the TMA store
-        __syncwarp();
-        const int row0 = (2 * w.u + x) * kTQ + qw * 32;  // the warp's first row; rows past T are clipped
-        if (lane == 0 && row0 < T) {
-#pragma unroll
-          for (int bx = 0; bx < kBoxes; ++bx)
-            tma_store_3d(&tmap_out, stg + bx * 4096, h * kHS + bx * kBoxCols, row0, b);
-          bulk_commit_group();
-        }
+      if (!ok) break;
+      if (pend.k >= 0 && !(ok = epilogue(pend))) break;  // no step of this group in this unit
+      if (n_x > 0) {
+        pend = Done{k, m_run, l_run};
         ++before;
       }
       g0 += sch.n_steps;
     }
+    if (ok && pend.k >= 0) ok = epilogue(pend);
     if (!ok) *abort_flag = 1;
     if (lane == 0) bulk_wait_group_read<0>();  // the staging rows are read before the CTA exits
     __syncwarp();
