@@ -365,14 +365,18 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     return ((static_cast<size_t>(tbl_s[j >> rows.lbs]) * NH + h) << rows.lbs) + (j & ((1 << rows.lbs) - 1));
   };
   if (pos_ok) {
-    // The cache rows before pos were written by earlier steps: this warp's
-    // first chunk of them is fetched into L2 while the QKV projection before
-    // this kernel finishes (a prefetch has no other effect).
-    for (int i = 0; i < kIt; ++i) {
-      const int j = warp * kChunk + i * kRPI + g;
-      if (j < pos && dg == 0) {
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(kcache + row(j) * HS));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(vcache + row(j) * HS));
+    // The cache rows before pos were written by earlier steps: all of them
+    // (one layer's cache at a few hundred positions is tens of MB, well
+    // within L2) are requested into L2 while the QKV projection before this
+    // kernel finishes and leaves HBM mostly idle (a prefetch has no other
+    // effect; measured in a decode step against prefetching each warp's
+    // first chunk only, 1 % faster).  A row of 64 16-bit elements is one
+    // 128-byte line.
+    for (int j = threadIdx.x; j < pos; j += blockDim.x) {
+      const size_t rj = row(j) * HS;
+      for (int off = 0; off < HS * static_cast<int>(sizeof(E)); off += 128) {
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(kcache + rj) + off));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(vcache + rj) + off));
       }
     }
   }
@@ -402,9 +406,10 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 #pragma unroll
   for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
   const int nchunk = pos / kChunk + 1;  // chunks covering positions 0 .. pos
-  for (int c = warp; c < nchunk; c += kDecWarps) {
+  // K and V rows of chunk c into registers (zero past pos; row pos from the
+  // QKV row)
+  auto load = [&](int c, uint4(&kr)[kIt], uint4(&vr)[kIt]) {
     const int j0 = c * kChunk + g;
-    uint4 kr[kIt], vr[kIt];
 #pragma unroll
     for (int i = 0; i < kIt; ++i) {
       const int j = j0 + i * kRPI;
@@ -420,6 +425,10 @@ __global__ void __launch_bounds__(32 * kDecWarps)
         vr[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
+  };
+  // the online softmax over chunk c's rows
+  auto consume = [&](int c, const uint4(&kr)[kIt], const uint4(&vr)[kIt]) {
+    const int j0 = c * kChunk + g;
     // scores (log2 units) of this lane's kIt rows; the row's kLPR lanes
     // each hold a partial dot product and sum it by shuffles
     float sc[kIt];
@@ -452,6 +461,15 @@ __global__ void __launch_bounds__(32 * kDecWarps)
       for (int k = 0; k < kPer; ++k) acc[k] = fmaf(p, to_f32(e[k]), acc[k]);
     }
     m = m_new;
+  };
+  // this warp's chunks c = warp, warp + kDecWarps, ...  (measured in a
+  // decode step: a second register buffer, loading the next chunk while one
+  // is used, with chunks half as long to keep three CTAs per SM, made the
+  // step no faster)
+  for (int c = warp; c < nchunk; c += kDecWarps) {
+    uint4 kr[kIt], vr[kIt];
+    load(c, kr, vr);
+    consume(c, kr, vr);
   }
   // sum over the rows of an instruction: every lane then holds the warp's
   // sum and its dimensions' output
