@@ -48,14 +48,15 @@ from gpt_transformer_forward_gb300 import inputs  # noqa: E402
 METRIC = "GPT-2 124M forward tokens/s (B=16,T=1024) on 1 GB300; % of roofline"
 
 
-def metric_name(w):
+def metric_name(w, probs="fp32"):
     """The metric string of a forward workload: the headline string for the
-    124M B=16 T=1024 pass, the same wording with its own model and shape for
-    every other one."""
-    if w.name == "gpt2-124m-b16":
+    124M B=16 T=1024 pass with fp32 probabilities, the same wording with its
+    own model, shape and probabilities type for every other one."""
+    if w.name == "gpt2-124m-b16" and probs == "fp32":
         return METRIC
     model = {12: "124M", 24: "medium"}.get(w.cfg.num_layers, f"L{w.cfg.num_layers}")
-    return f"GPT-2 {model} forward tokens/s (B={w.B},T={w.T}) on 1 GB300; % of roofline"
+    extra = "" if probs == "fp32" else f", {probs} probabilities"
+    return f"GPT-2 {model} forward tokens/s (B={w.B},T={w.T}{extra}) on 1 GB300; % of roofline"
 
 UNIT = "tokens/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -63,11 +64,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 
 # ----------------------------------------------------------- algorithmic cost
-def stage_costs(cfg, B, T, act_bytes=2):
+def stage_costs(cfg, B, T, act_bytes=2, probs_bytes=4):
     """Algorithmic FLOPs and bytes of each stage of one forward pass (every
     layer summed): bytes count each input read once and each output written
     once, with operand buffers of act_bytes (2 for bf16/fp16), the residual
-    stream, logits and probabilities fp32, weights 16-bit, and the causal
+    stream and logits fp32, probabilities of probs_bytes, weights 16-bit, and the causal
     attention FLOPs only (j <= t).  With 16-bit operands the two projections
     write their output y in 16 bits and the residual add x += y runs in the
     LayerNorm that follows (layer 0's first LayerNorm has no y to add; the
@@ -92,7 +93,7 @@ def stage_costs(cfg, B, T, act_bytes=2):
         "fcproj": (L * 2 * N * 4 * C * C, L * (N * 4 * C * a + 4 * C * C * w + C * 4 + proj_out)),
         "lnf": (0, ln_bytes + (N * C * a if fused else 0)),
         "lm_head": (2 * N * C * Vp, N * C * a + Vp * C * w + N * Vp * 4),
-        "softmax": (0, 2 * N * Vp * 4),
+        "softmax": (0, N * Vp * (4 + probs_bytes)),
     }
 
 
@@ -306,7 +307,7 @@ def run_reference(args):
     dt = time.perf_counter() - t0
     value = args.steps * T_s / dt
     sample = f"per step: 1 sequence x {T_s} tokens of {w.name} (double precision, logits and probs)"
-    line = {"impl": "reference", "metric": metric_name(w), "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": metric_name(w, args.probs), "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T},
@@ -571,7 +572,8 @@ def run_ours(args):
     params, tok = inputs.workload_inputs(w)
     tok = rank_tokens(w, tok, rank)  # replicas: each rank its own batch of token ids
     model = GPT2Model(w.cfg, params, w.B, w.T, precision)
-    logits, probs = model.new_outputs(w.B, w.T)
+    probs_dtype = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}[args.probs]
+    logits, probs = model.new_outputs(w.B, w.T, probs_dtype=probs_dtype)
     tok_d = torch.from_numpy(tok).cuda()
     stream = torch.cuda.current_stream()
 
@@ -608,8 +610,8 @@ def run_ours(args):
     # timed region, the last one included.
     tok_h = torch.from_numpy(tok).pin_memory()
     logits_h = torch.empty(logits.shape, dtype=torch.float32, pin_memory=True)
-    probs_h = torch.empty(probs.shape, dtype=torch.float32, pin_memory=True)
-    bufs = [(logits, probs), model.new_outputs(w.B, w.T)]
+    probs_h = torch.empty(probs.shape, dtype=probs_dtype, pin_memory=True)
+    bufs = [(logits, probs), model.new_outputs(w.B, w.T, probs_dtype=probs_dtype)]
     copy_stream = torch.cuda.Stream()
     copied = [None, None]  # event: the copy out of buffer set b is done
     e2e_steps = max(3, min(args.steps, 20))
@@ -644,7 +646,8 @@ def run_ours(args):
         for k, v in model.forward_profile(tok_d, logits, probs).items():
             stage_ms[k] += v / prof_runs
     peaks, peak_src = load_peaks()
-    costs = stage_costs(w.cfg, w.B, w.T, act_bytes=2 if precision in (ab.GPT2_BF16, ab.GPT2_FP16) else 4)
+    costs = stage_costs(w.cfg, w.B, w.T, act_bytes=2 if precision in (ab.GPT2_BF16, ab.GPT2_FP16) else 4,
+                        probs_bytes=probs.element_size())
     hbm = peaks["hbm_gbs"] * 1e9
     tensor = peaks["bf16_tflops_sustained"] * 1e12
     stages, roof_ms = {}, 0.0
@@ -664,7 +667,8 @@ def run_ours(args):
         achieved = nbytes / launches / (per_launch_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(dom) if args.workload == "gpt2-124m-b16" else None
+    # the committed DRAM records are of the headline pass (fp32 probabilities)
+    roof["traffic"] = measured_traffic(dom) if args.workload == "gpt2-124m-b16" and args.probs == "fp32" else None
     roof["algorithmic_per_launch"] = flops / launches if roof["bound"] == "tensor" else nbytes / launches
     roof["kernel"] = dom
     roof["peak_source"] = peak_src
@@ -676,15 +680,17 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, params, tok)
     line = {
-        "metric": metric_name(w), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric_name(w, args.probs), "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.precision, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "layers": w.cfg.num_layers,
                    "channels": w.cfg.channels, "heads": w.cfg.num_heads, "vocab": w.cfg.vocab_size,
-                   "padded_vocab": w.cfg.padded_vocab_size, "outputs": "logits+probs",
+                   "padded_vocab": w.cfg.padded_vocab_size,
+                   "outputs": "logits+probs" if args.probs == "fp32" else f"logits (fp32) + probs ({args.probs})",
                    "l2": "no flush: working set > 7 GB, L2 129 MB", "parallelism": f"replicas{world}"},
         "e2e": {"value": job_tokens_per_s(world, tokens, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": int(tok.nbytes), "d2h_bytes_per_step": int(logits.numel() * 4 * 2)},
+                "h2d_bytes_per_step": int(tok.nbytes),
+                "d2h_bytes_per_step": int(logits.numel() * 4 + probs.numel() * probs.element_size())},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roof,
         "pass_roofline": {"roofline_ms": roof_ms, "measured_ms": ms, "frac": roof_ms / ms,
@@ -711,6 +717,8 @@ def main():
     ap.add_argument("--workload", default="gpt2-124m-b16", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--precision", default="fp16", choices=["fp16", "bf16", "tf32", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--probs", default="fp32", choices=["fp32", "fp16", "bf16"],
+                    help="element type of the forward pass's probabilities output (fp32: the headline)")
     ap.add_argument("--train", action="store_true",
                     help="time training steps (forward, loss, backward, AdamW) at the workload's shape instead")
     ap.add_argument("--attention-forward", action="store_true",

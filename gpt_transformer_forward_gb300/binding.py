@@ -16,6 +16,7 @@ import re
 from . import build as _build
 
 GPT2_FP32, GPT2_TF32, GPT2_BF16, GPT2_FP16 = 0, 1, 2, 3
+GPT2_PROBS_F32, GPT2_PROBS_F16, GPT2_PROBS_BF16 = 0, 1, 2
 PRECISIONS = {"fp32": GPT2_FP32, "tf32": GPT2_TF32, "bf16": GPT2_BF16, "fp16": GPT2_FP16}
 
 GPT2_OK = 0
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "gelu_forward": (_I, [_P, _P, _I, _P]),
     "residual_forward": (_I, [_P, _P, _P, _I, _P]),
     "softmax_forward": (_I, [_P, _P, _I, _I, _I, _P]),
+    "softmax_forward_ex": (_I, [_P, _I, _P, _I, _I, _I, _P]),
     "gpt2_argmax": (_I, [_P, _P, _I, _I, _I, _P]),
     "gpt2_num_parameters": (_Z, [_CFG]),
     "gpt2_packed_weights_size": (_Z, [_CFG, _I]),
@@ -78,6 +80,7 @@ _SIGNATURES = {
     "gpt2_workspace_size": (_Z, [_CFG, _I, _I, _I]),
     "gpt2_kvcache_size": (_Z, [_CFG, _I, _I]),
     "gpt2_forward": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _P, _P, _Z, _I, _P]),
+    "gpt2_forward_ex": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _I, _P, _P, _Z, _I, _P]),
     "gpt2_decode_step": (_I, [_CFG, _P, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _I, _P]),
     "gpt2_train_workspace_size": (_Z, [_CFG, _I, _I, _I]),
     "gpt2_forward_backward": (_I, [_CFG, _P, _P, _P, _P, _I, _I, _P, _P, _Z, _I, _P]),
@@ -86,7 +89,7 @@ _SIGNATURES = {
     "gpt2_paged_kvcache_size": (_Z, [_CFG, _I, _I, _I]),
     "gpt2_prefill_paged": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _PKV, _P, _Z, _I, _P]),
     "gpt2_decode_step_paged": (_I, [_CFG, _P, _P, _PKV, _P, _P, _I, _P, _P, _P, _Z, _I, _P]),
-    "gpt2_forward_profile": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _P, _Z, _I, _P, _P, _I]),
+    "gpt2_forward_profile": (_I, [_CFG, _P, _P, _P, _I, _I, _P, _P, _I, _P, _Z, _I, _P, _P, _I]),
     "gpt2_get_error": (_I, [_P]),
     "gpt2_strerror": (ctypes.c_char_p, [_I]),
     "gpt2_last_cuda_error": (ctypes.c_char_p, []),
@@ -218,6 +221,11 @@ def softmax_forward(probs, logits, N, V, Vp, stream=None):
     _check("softmax_forward", _lib().softmax_forward(_ptr(probs), _ptr(logits), N, V, Vp, _stream(stream)))
 
 
+def softmax_forward_ex(probs, probs_type, logits, N, V, Vp, stream=None):
+    _check("softmax_forward_ex", _lib().softmax_forward_ex(_ptr(probs), probs_type, _ptr(logits), N, V, Vp,
+                                                           _stream(stream)))
+
+
 def gpt2_argmax(next_tok, logits, B, V, Vp, stream=None):
     _check("gpt2_argmax", _lib().gpt2_argmax(_ptr(next_tok), _ptr(logits), B, V, Vp, _stream(stream)))
 
@@ -248,6 +256,13 @@ def gpt2_forward(cfg, params, packed, tok, B, T, logits, probs, kvcache, workspa
     _check("gpt2_forward", _lib().gpt2_forward(_cfg(cfg), _ptr(params), _ptr(packed), _ptr(tok), B, T, _ptr(logits),
                                                _ptr(probs), _ptr(kvcache), _ptr(workspace), ws_bytes, precision,
                                                _stream(stream)))
+
+
+def gpt2_forward_ex(cfg, params, packed, tok, B, T, logits, probs, probs_type, kvcache, workspace, ws_bytes,
+                    precision, stream=None):
+    _check("gpt2_forward_ex", _lib().gpt2_forward_ex(_cfg(cfg), _ptr(params), _ptr(packed), _ptr(tok), B, T,
+                                                     _ptr(logits), _ptr(probs), probs_type, _ptr(kvcache),
+                                                     _ptr(workspace), ws_bytes, precision, _stream(stream)))
 
 
 def gpt2_decode_step(cfg, params, packed, kvcache, tok, B, pos, logits, probs, workspace, ws_bytes, precision,
@@ -301,12 +316,12 @@ def gpt2_decode_step_paged(cfg, params, packed, kv, tok, pos, B, logits, probs, 
 
 
 def gpt2_forward_profile(cfg, params, packed, tok, B, T, logits, probs, workspace, ws_bytes, precision,
-                         stream=None) -> dict:
+                         stream=None, probs_type=GPT2_PROBS_F32) -> dict:
     """Runs one forward pass with per-stage CUDA events; returns {stage: ms}."""
     ms = (ctypes.c_float * len(STAGES))()
     _check("gpt2_forward_profile", _lib().gpt2_forward_profile(
-        _cfg(cfg), _ptr(params), _ptr(packed), _ptr(tok), B, T, _ptr(logits), _ptr(probs), _ptr(workspace),
-        ws_bytes, precision, _stream(stream), ctypes.cast(ms, ctypes.c_void_p), len(STAGES)))
+        _cfg(cfg), _ptr(params), _ptr(packed), _ptr(tok), B, T, _ptr(logits), _ptr(probs), probs_type,
+        _ptr(workspace), ws_bytes, precision, _stream(stream), ctypes.cast(ms, ctypes.c_void_p), len(STAGES)))
     return dict(zip(STAGES, list(ms)))
 
 

@@ -495,13 +495,19 @@ int residual_forward(float* out, const float* a, const float* b, int n, void* st
   return check_launch();
 }
 
-int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, void* stream) {
-  RETURN_IF(!probs || !logits || N < 0 || V <= 0 || Vp < V, GPT2_ERR_ARG);
+static bool valid_probs_type(int t) { return t == GPT2_PROBS_F32 || t == GPT2_PROBS_F16 || t == GPT2_PROBS_BF16; }
+
+int softmax_forward_ex(void* probs, int probs_type, const float* logits, int N, int V, int Vp, void* stream) {
+  RETURN_IF(!probs || !logits || N < 0 || V <= 0 || Vp < V || !valid_probs_type(probs_type), GPT2_ERR_ARG);
   RETURN_IF(Vp % 4 != 0, GPT2_ERR_SHAPE);
   RETURN_IF(!aligned16(probs) || !aligned16(logits), GPT2_ERR_ALIGN);
   if (N == 0) return GPT2_OK;
-  launch_softmax(probs, logits, N, V, Vp, as_stream(stream));
+  launch_softmax(probs, probs_type, logits, N, V, Vp, as_stream(stream));
   return check_launch();
+}
+
+int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, void* stream) {
+  return softmax_forward_ex(probs, GPT2_PROBS_F32, logits, N, V, Vp, stream);
 }
 
 int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, void* stream) {
@@ -562,9 +568,9 @@ size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision) {
 // the B sequences' tokens at position decode_pos, or pos_arr[b] when pos_arr
 // is given (T == 1), attending over and appending to kv.
 static int run_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
-                       bool decode, int decode_pos, const int* pos_arr, float* logits, float* probs,
+                       bool decode, int decode_pos, const int* pos_arr, float* logits, void* probs,
                        const KVLayout* kv, void* workspace, size_t ws_bytes, int precision, cudaStream_t s,
-                       StageProfiler* prof = nullptr) {
+                       StageProfiler* prof = nullptr, int probs_type = GPT2_PROBS_F32) {
   auto mark = [&](int stage) { return prof ? prof->record(stage) : GPT2_OK; };
   const int C = cfg->channels, L = cfg->num_layers, NH = cfg->num_heads, V = cfg->vocab_size;
   const int Vp = cfg->padded_vocab_size, maxT = cfg->max_seq_len;
@@ -690,20 +696,21 @@ static int run_forward(const GPT2Config* cfg, const float* params, const void* p
   TRY(mark(GPT2_STAGE_LMHEAD));
   if (probs != nullptr) {
     if (precision == GPT2_FP32)
-      launch_softmax(probs, logits, N, V, Vp, s);
+      launch_softmax(probs, probs_type, logits, N, V, Vp, s);
     else
-      launch_softmax_from_stats(probs, logits, stats, logits_stat_blocks(Vp), N, V, Vp, s);
+      launch_softmax_from_stats(probs, probs_type, logits, stats, logits_stat_blocks(Vp), N, V, Vp, s);
   }
   TRY(check_launch());
   TRY(mark(GPT2_STAGE_SOFTMAX));
   return GPT2_OK;
 }
 
-int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
-                 float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
-                 void* stream) {
+int gpt2_forward_ex(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                    float* logits, void* probs, int probs_type, void* kvcache, void* workspace, size_t ws_bytes,
+                    int precision, void* stream) {
   TRY(check_config(cfg));
-  RETURN_IF(!params || !tok || !logits || !workspace || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(!params || !tok || !logits || !workspace || !valid_precision(precision) || !valid_probs_type(probs_type),
+            GPT2_ERR_ARG);
   RETURN_IF(B <= 0 || T <= 0, GPT2_ERR_ARG);
   RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(cfg->channels, cfg->num_heads));
@@ -715,14 +722,24 @@ int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed,
   PdlScope pdl(is16(precision));  // every kernel of the 16-bit pass waits for its predecessor itself
   const KVLayout kv = dense_kv(cfg, kvcache, B);
   return run_forward(cfg, params, packed, tok, B, T, false, 0, nullptr, logits, probs,
-                     kvcache != nullptr ? &kv : nullptr, workspace, ws_bytes, precision, as_stream(stream));
+                     kvcache != nullptr ? &kv : nullptr, workspace, ws_bytes, precision, as_stream(stream), nullptr,
+                     probs_type);
+}
+
+int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
+                 float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
+                 void* stream) {
+  return gpt2_forward_ex(cfg, params, packed, tok, B, T, logits, probs, GPT2_PROBS_F32, kvcache, workspace, ws_bytes,
+                         precision, stream);
 }
 
 int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
-                         float* logits, float* probs, void* workspace, size_t ws_bytes, int precision, void* stream,
-                         float* stage_ms, int n_stages) {
+                         float* logits, void* probs, int probs_type, void* workspace, size_t ws_bytes, int precision,
+                         void* stream, float* stage_ms, int n_stages) {
   TRY(check_config(cfg));
-  RETURN_IF(!params || !tok || !logits || !workspace || !stage_ms || !valid_precision(precision), GPT2_ERR_ARG);
+  RETURN_IF(!params || !tok || !logits || !workspace || !stage_ms || !valid_precision(precision) ||
+                !valid_probs_type(probs_type),
+            GPT2_ERR_ARG);
   RETURN_IF(B <= 0 || T <= 0 || n_stages <= 0, GPT2_ERR_ARG);
   RETURN_IF(T > cfg->max_seq_len, GPT2_ERR_SHAPE);
   TRY(check_attention_shape(cfg->channels, cfg->num_heads));
@@ -736,7 +753,7 @@ int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void*
   int rc = prof.begin();
   if (rc == GPT2_OK)
     rc = run_forward(cfg, params, packed, tok, B, T, false, 0, nullptr, logits, probs, nullptr, workspace, ws_bytes,
-                     precision, as_stream(stream), &prof);
+                     precision, as_stream(stream), &prof, probs_type);
   const int rc2 = prof.finish(stage_ms, n_stages);
   return rc != GPT2_OK ? rc : rc2;
 }

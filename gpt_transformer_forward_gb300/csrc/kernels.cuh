@@ -79,7 +79,10 @@ void launch_residual_layernorm_16(float* x, const T16* y, T16* out, const float*
                                   bool write_x, cudaStream_t s);
 void launch_gelu(float* out, const float* inp, int n, cudaStream_t s);
 void launch_residual(float* out, const float* a, const float* b, int n, cudaStream_t s);
-void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s);
+// The type of the probabilities a softmax writes (the values of the C
+// ABI's GPT2_PROBS_*): fp32, or the fp32 value rounded to fp16 or bf16.
+enum ProbsType { kProbsF32 = 0, kProbsF16 = 1, kProbsBF16 = 2 };
+void launch_softmax(void* probs, int probs_type, const float* logits, int N, int V, int Vp, cudaStream_t s);
 void launch_argmax(int* next, const float* logits, int B, int V, int Vp, cudaStream_t s);
 template <typename T>
 void launch_f32_to_16(T* out, const float* in, long long n, cudaStream_t s);
@@ -142,8 +145,8 @@ int launch_gemm_logits(float* logits, float2* row_stats, const void* A, const vo
                        int op, cudaStream_t s);
 int logits_stat_blocks(int N);
 // Softmax from those statistics: one read of the logits, one write.
-void launch_softmax_from_stats(float* probs, const float* logits, const float2* row_stats, int tiles, int N, int V,
-                               int Vp, cudaStream_t s);
+void launch_softmax_from_stats(void* probs, int probs_type, const float* logits, const float2* row_stats, int tiles,
+                               int N, int V, int Vp, cudaStream_t s);
 
 // gemm_simt.cu: fp32 CUDA-core GEMM (GPT2_FP32 mode), out = A W^T + bias,
 // then optional GELU or residual accumulation (out += ...).

@@ -399,8 +399,12 @@ __device__ __forceinline__ float2 block_merge_stats(float m, float s) {
   return result;
 }
 
-// Writes probs for one row given its max and 1/sum: float4 streaming.
-__device__ __forceinline__ void softmax_write_row(float4* __restrict__ prow, const float4* __restrict__ lrow, int V,
+// Writes probs for one row given its max and 1/sum, streaming: four
+// columns per thread and step, as a float4 (P = float) or as four 16-bit
+// values (P = __half or __nv_bfloat16: each the fp32 probability rounded to
+// nearest once, so they equal the fp32 output's values rounded).
+template <typename P>
+__device__ __forceinline__ void softmax_write_row(P* __restrict__ prow, const float4* __restrict__ lrow, int V,
                                                   int c4_lo, int c4_hi, float mx, float inv) {
   for (int c4 = c4_lo + static_cast<int>(threadIdx.x); c4 < c4_hi; c4 += blockDim.x) {
     const float4 x = __ldcs(lrow + c4);
@@ -410,7 +414,11 @@ __device__ __forceinline__ void softmax_write_row(float4* __restrict__ prow, con
     p.y = (c + 1 < V) ? __expf(x.y - mx) * inv : 0.f;
     p.z = (c + 2 < V) ? __expf(x.z - mx) * inv : 0.f;
     p.w = (c + 3 < V) ? __expf(x.w - mx) * inv : 0.f;
-    __stcs(prow + c4, p);
+    if constexpr (std::is_same<P, float>::value) {
+      __stcs(reinterpret_cast<float4*>(prow) + c4, p);
+    } else {
+      __stcs(reinterpret_cast<uint2*>(prow) + c4, make_uint2(pack2<P>(p.x, p.y), pack2<P>(p.z, p.w)));
+    }
   }
 }
 
@@ -418,7 +426,8 @@ __device__ __forceinline__ void softmax_write_row(float4* __restrict__ prow, con
 // row, then the normalised write pass.  The second pass re-reads a row the
 // block has just read; the rows in flight (a few MB) stay in L2, so HBM sees
 // about one read and one write per element.
-__global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float4* __restrict__ probs,
+template <typename P>
+__global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(P* __restrict__ probs,
                                                                         const float4* __restrict__ logits, int V,
                                                                         int Vp4) {
   const size_t row = blockIdx.x;
@@ -440,18 +449,28 @@ __global__ void __launch_bounds__(kSoftmaxThreads) softmax_2pass_kernel(float4* 
     }
   }
   const float2 r = block_merge_stats(m, s);
-  softmax_write_row(probs + row * Vp4, lrow, V, 0, Vp4, r.x, 1.0f / r.y);
+  softmax_write_row(probs + row * Vp4 * 4, lrow, V, 0, Vp4, r.x, 1.0f / r.y);
 }
 
-void launch_softmax(float* probs, const float* logits, int N, int V, int Vp, cudaStream_t s) {
-  softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(reinterpret_cast<float4*>(probs),
-                                                     reinterpret_cast<const float4*>(logits), V, Vp / 4);
+void launch_softmax(void* probs, int probs_type, const float* logits, int N, int V, int Vp, cudaStream_t s) {
+  const float4* l4 = reinterpret_cast<const float4*>(logits);
+  switch (probs_type) {
+    case kProbsF16:
+      softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(static_cast<__half*>(probs), l4, V, Vp / 4);
+      break;
+    case kProbsBF16:
+      softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(static_cast<__nv_bfloat16*>(probs), l4, V, Vp / 4);
+      break;
+    default:
+      softmax_2pass_kernel<<<N, kSoftmaxThreads, 0, s>>>(static_cast<float*>(probs), l4, V, Vp / 4);
+  }
 }
 
 // Softmax after the LM-head GEMM: the row's (max, sum) come from the
 // per-tile statistics the GEMM epilogue left, so the logits are read once.
 constexpr int kStatsThreads = 256;
-__global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(float4* __restrict__ probs,
+template <typename P>
+__global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(P* __restrict__ probs,
                                                                            const float4* __restrict__ logits,
                                                                            const float2* __restrict__ stats,
                                                                            int tiles, int V, int Vp4) {
@@ -468,17 +487,30 @@ __global__ void __launch_bounds__(kStatsThreads) softmax_from_stats_kernel(float
   // there are too few rows to fill the GPU)
   const int per = (Vp4 + static_cast<int>(gridDim.y) - 1) / static_cast<int>(gridDim.y);
   const int lo = static_cast<int>(blockIdx.y) * per;
-  softmax_write_row(probs + row * Vp4, logits + row * Vp4, V, lo, min(Vp4, lo + per), r.x, 1.0f / r.y);
+  softmax_write_row(probs + row * Vp4 * 4, logits + row * Vp4, V, lo, min(Vp4, lo + per), r.x, 1.0f / r.y);
 }
 
-void launch_softmax_from_stats(float* probs, const float* logits, const float2* row_stats, int tiles, int N, int V,
-                               int Vp, cudaStream_t s) {
+void launch_softmax_from_stats(void* probs, int probs_type, const float* logits, const float2* row_stats, int tiles,
+                               int N, int V, int Vp, cudaStream_t s) {
   // a few rows (a decode step): split each row over blocks, about four
   // blocks per SM in all
   int split = N >= 4 * num_sms() ? 1 : (4 * num_sms() + N - 1) / N;
   if (split > 64) split = 64;
-  launch_pdl(softmax_from_stats_kernel, dim3(N, split), dim3(kStatsThreads), 0, s, reinterpret_cast<float4*>(probs),
-             reinterpret_cast<const float4*>(logits), row_stats, tiles, V, Vp / 4);
+  const float4* l4 = reinterpret_cast<const float4*>(logits);
+  const dim3 grid(N, split), block(kStatsThreads);
+  switch (probs_type) {
+    case kProbsF16:
+      launch_pdl(softmax_from_stats_kernel<__half>, grid, block, 0, s, static_cast<__half*>(probs), l4, row_stats,
+                 tiles, V, Vp / 4);
+      break;
+    case kProbsBF16:
+      launch_pdl(softmax_from_stats_kernel<__nv_bfloat16>, grid, block, 0, s, static_cast<__nv_bfloat16*>(probs), l4,
+                 row_stats, tiles, V, Vp / 4);
+      break;
+    default:
+      launch_pdl(softmax_from_stats_kernel<float>, grid, block, 0, s, static_cast<float*>(probs), l4, row_stats,
+                 tiles, V, Vp / 4);
+  }
 }
 
 // ----------------------------------------------------------------- argmax

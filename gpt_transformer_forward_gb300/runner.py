@@ -10,6 +10,14 @@ import torch
 
 from . import binding as ab
 
+# the probabilities' element type from the output tensor's dtype
+_PROBS_TYPE = {torch.float32: ab.GPT2_PROBS_F32, torch.float16: ab.GPT2_PROBS_F16,
+               torch.bfloat16: ab.GPT2_PROBS_BF16}
+
+
+def probs_type(probs) -> int:
+    return ab.GPT2_PROBS_F32 if probs is None else _PROBS_TYPE[probs.dtype]
+
 
 class GPT2Model:
     """Parameters (fp32, plus the packed bf16 weights in GPT2_BF16 mode) and a
@@ -35,11 +43,11 @@ class GPT2Model:
         self.workspace = torch.empty(self.ws_bytes, dtype=torch.uint8, device=self.device)
 
     # ---------------------------------------------------------------- buffers
-    def new_outputs(self, B: int, T: int, probs: bool = True):
+    def new_outputs(self, B: int, T: int, probs: bool = True, probs_dtype=torch.float32):
         Vp = self.cfg.padded_vocab_size
         shape = (B, T, Vp) if T is not None else (B, Vp)
         logits = torch.empty(shape, dtype=torch.float32, device=self.device)
-        pr = torch.empty(shape, dtype=torch.float32, device=self.device) if probs else None
+        pr = torch.empty(shape, dtype=probs_dtype, device=self.device) if probs else None
         return logits, pr
 
     def new_kvcache(self, B: int):
@@ -53,14 +61,16 @@ class GPT2Model:
 
     # ----------------------------------------------------------------- calls
     def forward(self, tok, logits, probs=None, kvcache=None, stream=None):
+        """probs (optional): fp32, fp16 or bf16, [B, T, Vp]."""
         B, T = tok.shape
-        ab.gpt2_forward(self.cfg, self.params, self.packed, tok, B, T, logits, probs, kvcache, self.workspace,
-                        self.ws_bytes, self.precision, stream)
+        ab.gpt2_forward_ex(self.cfg, self.params, self.packed, tok, B, T, logits, probs, probs_type(probs), kvcache,
+                           self.workspace, self.ws_bytes, self.precision, stream)
 
     def forward_profile(self, tok, logits, probs=None, stream=None) -> dict:
         B, T = tok.shape
         return ab.gpt2_forward_profile(self.cfg, self.params, self.packed, tok, B, T, logits, probs,
-                                       self.workspace, self.ws_bytes, self.precision, stream)
+                                       self.workspace, self.ws_bytes, self.precision, stream,
+                                       probs_type=probs_type(probs))
 
     def decode_step(self, kvcache, tok, pos: int, logits, probs=None, stream=None):
         B = tok.shape[0]

@@ -77,6 +77,15 @@ typedef struct {
  * fp32 in every mode. */
 typedef enum { GPT2_FP32 = 0, GPT2_TF32 = 1, GPT2_BF16 = 2, GPT2_FP16 = 3 } GPT2Precision;
 
+/* Element type of a probabilities output (softmax_forward_ex,
+ * gpt2_forward_ex, gpt2_forward_profile) [llm.c "State of the Union": the
+ * classifier row of its kernel table, and its case for fp16/bf16 storage].
+ * GPT2_PROBS_F32 is the default of softmax_forward and gpt2_forward; the
+ * 16-bit types hold each fp32 probability rounded to nearest once (so they
+ * equal the fp32 output rounded) and halve the bytes of the largest write of
+ * the forward pass. */
+typedef enum { GPT2_PROBS_F32 = 0, GPT2_PROBS_F16 = 1, GPT2_PROBS_BF16 = 2 } GPT2ProbsType;
+
 enum {
   GPT2_OK = 0,
   GPT2_ERR_ARG = -1,       /* null pointer or nonsensical argument */
@@ -215,6 +224,12 @@ GPT2_API int residual_forward(float* out, const float* a, const float* b, int n,
  * requires Vp % 4 == 0.  probs must not alias logits. */
 GPT2_API int softmax_forward(float* probs, const float* logits, int N, int V, int Vp, void* stream);
 
+/* softmax_forward with the probabilities stored as probs_type (a
+ * GPT2ProbsType): probs [N,Vp] of that type, 16-byte aligned; a
+ * probs_type outside GPT2ProbsType is GPT2_ERR_ARG. */
+GPT2_API int softmax_forward_ex(void* probs, int probs_type, const float* logits, int N, int V, int Vp,
+                                void* stream);
+
 /* Greedy next token: next[b] = the smallest v < V with the largest
  * logits[b, v].  next [B] int32, logits [B,Vp]. */
 GPT2_API int gpt2_argmax(int* next, const float* logits, int B, int V, int Vp, void* stream);
@@ -268,6 +283,14 @@ GPT2_API size_t gpt2_kvcache_size(const GPT2Config* cfg, int B, int precision);
 GPT2_API int gpt2_forward(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B, int T,
                  float* logits, float* probs, void* kvcache, void* workspace, size_t ws_bytes, int precision,
                  void* stream);
+
+/* gpt2_forward with the probabilities stored as probs_type (a
+ * GPT2ProbsType): probs [B,T,Vp] of that type (16-byte aligned) or NULL;
+ * the logits stay fp32.  A probs_type outside GPT2ProbsType is
+ * GPT2_ERR_ARG.  Other arguments and behaviour as gpt2_forward. */
+GPT2_API int gpt2_forward_ex(const GPT2Config* cfg, const float* params, const void* packed, const int* tok, int B,
+                             int T, float* logits, void* probs, int probs_type, void* kvcache, void* workspace,
+                             size_t ws_bytes, int precision, void* stream);
 
 /* One KV-cached decode step [NTU "KV Caching"]: each of the B sequences has
  * `pos` tokens in kvcache (positions [0, pos)) and gets one new token
@@ -405,14 +428,15 @@ enum {
   GPT2_NUM_STAGES = 11
 };
 
-/* gpt2_forward (without a KV cache) with a CUDA event recorded on `stream`
- * after every stage; waits for the pass to finish and ADDS each stage's
- * milliseconds into stage_ms (HOST array of n_stages floats, indexed by
- * GPT2_STAGE_*).  For measurement only: the events serialise nothing but
- * the call synchronises the stream. */
+/* gpt2_forward_ex (without a KV cache) with a CUDA event recorded on
+ * `stream` after every stage; waits for the pass to finish and ADDS each
+ * stage's milliseconds into stage_ms (HOST array of n_stages floats, indexed
+ * by GPT2_STAGE_*).  probs of probs_type (a GPT2ProbsType) or NULL.  For
+ * measurement only: the events serialise nothing but the call synchronises
+ * the stream. */
 GPT2_API int gpt2_forward_profile(const GPT2Config* cfg, const float* params, const void* packed, const int* tok,
-                                  int B, int T, float* logits, float* probs, void* workspace, size_t ws_bytes,
-                                  int precision, void* stream, float* stage_ms, int n_stages);
+                                  int B, int T, float* logits, void* probs, int probs_type, void* workspace,
+                                  size_t ws_bytes, int precision, void* stream, float* stage_ms, int n_stages);
 
 /* Synchronises `stream`, returns the device error word (a set of
  * GPT2_DEVERR_*_BIT bits, 0 when clean) and clears it; a negative

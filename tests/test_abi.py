@@ -17,7 +17,7 @@ def lib():
 
 def test_every_declared_function_is_exported(lib):
     names = ab.header_functions()
-    assert len(names) == 31
+    assert len(names) == 33
     for n in names:
         assert hasattr(lib, n), n
         assert n in ab._SIGNATURES, n
@@ -61,10 +61,16 @@ def test_argument_errors_before_any_launch(lib):
     # null pointers and bad shapes return an error code before CUDA is touched
     assert lib.encoder_forward(None, None, None, None, 1, 1, 8, 1, None) == -1
     assert lib.softmax_forward(None, None, 1, 5, 4, None) == -1
+    assert lib.softmax_forward_ex(None, ab.GPT2_PROBS_F16, None, 1, 5, 4, None) == -1
+    # a probabilities type outside GPT2ProbsType (aligned, never dereferenced pointers)
+    assert lib.softmax_forward_ex(256, 3, 256, 1, 4, 4, None) == -1
+    assert lib.softmax_forward_ex(256, -1, 256, 1, 4, 4, None) == -1
     cfg = ab.GPT2Config.of(inputs.TINY)
     assert lib.gpt2_forward(ctypes.byref(cfg), None, None, None, 1, 1, None, None, None, None, 0, 2, None) == -1
     bad = ab.GPT2Config(64, 512, 512, 2, 3, 64)
     assert lib.gpt2_forward(ctypes.byref(bad), 16, None, 16, 1, 1, 16, None, None, 16, 0, 2, None) == -2
+    assert lib.gpt2_forward_ex(ctypes.byref(cfg), 256, 256, 256, 1, 8, 256, 256, 5, None, 256, 1 << 30, 2,
+                               None) == -1
     # T > maxT
     assert lib.gpt2_forward(ctypes.byref(cfg), 256, 256, 256, 1, 65, 256, None, None, 256, 1 << 30, 2,
                             None) == -2

@@ -54,6 +54,23 @@ def test_tiny_forward(precision, init):
     assert_close(host(probs), rp, atol=PROB_TOL[precision], what="tiny probs")
 
 
+@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_BF16, ab.GPT2_FP32])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_forward_16bit_probabilities(precision, dtype):
+    # the same pass with the probabilities stored in 16 bits: identical
+    # logits, and each probability the fp32 one rounded to nearest once
+    w = inputs.WORKLOADS["tiny"]
+    params, tok = inputs.workload_inputs(w, "perturbed")
+    m = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    logits32, probs32 = m.new_outputs(w.B, w.T)
+    logits16, probs16 = m.new_outputs(w.B, w.T, probs_dtype=dtype)
+    m.forward(dev(tok), logits32, probs32)
+    m.forward(dev(tok), logits16, probs16)
+    no_device_error()
+    assert torch.equal(logits16, logits32)
+    assert torch.equal(probs16, probs32.to(dtype))
+
+
 @pytest.mark.parametrize("T", [1, 17, 64])
 def test_tiny_forward_short_sequences(T):
     w = inputs.WORKLOADS["tiny"]

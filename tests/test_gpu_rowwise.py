@@ -104,6 +104,30 @@ def test_softmax(N, V, Vp, std):
     assert (got[:, V:] == 0).all()
 
 
+@pytest.mark.parametrize("ptype,dtype", [(ab.GPT2_PROBS_F16, torch.float16), (ab.GPT2_PROBS_BF16, torch.bfloat16)])
+@pytest.mark.parametrize("N,V,Vp,std", [(5, 50257, 50304, 0.55), (7, 5, 8, 2.0), (1, 1000, 1024, 30.0)])
+def test_softmax_16bit_probabilities(N, V, Vp, std, ptype, dtype):
+    # each 16-bit probability is the fp32 one rounded to nearest once
+    # (exactly what a round-to-nearest-even conversion of softmax_forward's
+    # output gives), so within the fp32 bound plus half a 16-bit unit of the
+    # oracle's value
+    lg = inputs.make_normal(13, (N, Vp), std)
+    out32 = torch.empty(N, Vp, dtype=torch.float32, device="cuda")
+    out16 = torch.full((N, Vp), float("nan"), dtype=dtype, device="cuda")
+    ab.softmax_forward(out32, dev(lg), N, V, Vp)
+    ab.softmax_forward_ex(out16, ptype, dev(lg), N, V, Vp)
+    no_device_error()
+    assert torch.equal(out16, out32.to(dtype))
+    u = 2.0 ** -11 if dtype == torch.float16 else 2.0 ** -8
+    ref = oracle.softmax(lg, V)
+    got = out16.float().cpu().numpy().astype(np.float64)
+    # fp16 values below 2^-14 are subnormal: an absolute floor of half the
+    # smallest fp16 step there
+    floor = 2.0 ** -25 if dtype == torch.float16 else 1e-37
+    assert_close(got[:, :V], ref[:, :V], rtol=REL + u, atol=floor, what="16-bit softmax")
+    assert (got[:, V:] == 0).all()
+
+
 # (Vp a multiple of 4: 16-byte loads with a scalar tail; 15: scalar loads)
 @pytest.mark.parametrize("B,V,Vp", [(32, 50257, 50304), (3, 10, 12), (2, 13, 15)])
 def test_argmax(B, V, Vp):
