@@ -104,9 +104,9 @@ struct Smem {
   static constexpr int stage = v + kKV * kVBytes;      // output staging: 32 rows x 64 fp32 per softmax warp
   static constexpr int kStageBytes = 32 * kHS * 4;
   static constexpr int bars = stage + 2 * kSoftmaxWarps * kStageBytes;
-  // q_full[2], q_empty[2]; kv_full[kKV], kv_empty[kKV]; s_full[kRing],
+  // q_full[2], q_empty[2]; kv_full[kKV], kv_empty[kKV]; s_full[2][kRing],
   // p_full[kRing], o_done[kRing]; o_final[2], o_free[2]; drain
-  static constexpr int n_bars = 4 + 2 * kKV + 3 * kRing + 4 + 1;
+  static constexpr int n_bars = 4 + 2 * kKV + 4 * kRing + 4 + 1;
   static constexpr int misc = bars + n_bars * 8;
   static constexpr int total = misc + 16;
   static constexpr int alloc = total + 1024;
@@ -197,9 +197,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_empty = q_full + 2;           // [2] the unit's S products have read them
   uint64_t* kv_full = q_empty + 2;          // [kKV] K and V of a key tile landed
   uint64_t* kv_empty = kv_full + kKV;       // [kKV] the MMAs have read them
-  // ring slot r serves global steps g = r, r + 3, ...: use k of the slot is phase k
-  uint64_t* s_full = kv_empty + kKV;        // [kRing] S of step g is in TMEM
-  uint64_t* p_full = s_full + kRing;        // [kRing] P of step g written (every softmax warp of the group)
+  // ring slot r serves global steps g = r, r + 3, ...: use k of the slot is
+  // phase k of p_full[r] and o_done[r], whose waiters (the issuing warps)
+  // walk every step.  S is signalled per group and slot instead: a group
+  // walks only its own steps, and after a unit without steps of its own
+  // (a last unit with one query tile) it would be two or more phases of a
+  // shared barrier behind, where the parity of the phase it waits for has
+  // completed already (that let group B read a slot holding group A's S,
+  // measured as wrong rows and a timeout).  Phase k of s_full[x][r] is
+  // group x's k-th step in slot r; the S products of its next step there
+  // wait for P V of a step that needs this group's P of the one before, so
+  // no phase completes before the group has waited for the previous one.
+  uint64_t* s_full = kv_empty + kKV;        // [2][kRing] S of step g (of group x) is in TMEM
+  uint64_t* p_full = s_full + 2 * kRing;    // [kRing] P of step g written (every softmax warp of the group)
   uint64_t* o_done = p_full + kRing;        // [kRing] P V of step g done
   uint64_t* o_final = o_done + kRing;       // [group] the group's last P V of a unit done
   uint64_t* o_free = o_final + 2;           // [group] the group's epilogue has read O
@@ -231,8 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&kv_full[i], 1u);
       mbar_init(&kv_empty[i], 1u);
     }
+    for (int r = 0; r < 2 * kRing; ++r) mbar_init(&s_full[r], 1u);
     for (int r = 0; r < kRing; ++r) {
-      mbar_init(&s_full[r], 1u);
       mbar_init(&p_full[r], kSoftmaxWarps);  // the group's softmax warps
       mbar_init(&o_done[r], 1u);
     }
@@ -328,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kHS / 16; ++kk)  // 16 dimensions = 32 bytes = 2 in the descriptor's address field
         tc_mma_warp<false>(tmem + kTmemS + (g % kRing) * kTK, qd + 2 * kk, kd + 2 * kk, kIdescS, kk > 0 ? 1u : 0u);
-      tc_commit_warp(&s_full[g % kRing]);
+      tc_commit_warp(&s_full[x * kRing + g % kRing]);
       if (s == sch.n_steps - 1) tc_commit_warp(&q_empty[qb]);
       return true;
     };
@@ -378,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     bool ok = true;
     int g0 = 0, before = 0;  // global steps and this group's units before the current unit
+    uint32_t s_par = 0;      // bit r: parity of this group's next phase of s_full[x][r]
     // A unit's output is written after this group's first step of its next
     // unit (or at the end): by then the unit's last P V has long finished,
     // where waiting for it right after the last step held the group up about
@@ -469,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < n_x; ++j) {
         const int s = g0 + sch.step(x, j), r = s % kRing;  // the global step
         const uint32_t s_col = kTmemS + r * kTK;
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[r], (s / kRing) & 1)))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x * kRing + r], (s_par >> r) & 1u)))) break;
+        s_par ^= 1u << r;
         tc_fence_after();
         // visible keys of this tile: all 128 or up to the diagonal
         const int valid = max(0, min(t_end - j * kTK, kTK));

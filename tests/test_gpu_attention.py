@@ -106,6 +106,25 @@ def test_attention_late_dominant_key(precision, late):
     assert_close(host(out), ref, atol=UNIT[precision] * vmax * (1 + 2.0 ** -6), what=f"dominant key at {late}")
 
 
+@pytest.mark.parametrize("precision", [ab.GPT2_BF16, ab.GPT2_FP16])
+def test_attention_ragged_launch_with_several_units_per_cta(precision):
+    # B=8, T=1100, 12 heads of 64: 9 query tiles, so 5 units per (sequence,
+    # head), the last without a second query tile; 480 units on 152 CTAs, so
+    # CTAs run several units in a row and write each unit's output during
+    # the next one.  Sequences 0 and 7 against the oracle.
+    B, T, C, NH = 8, 1100, 768, 12
+    qkv = inputs.make_normal(420, (B, T, 3 * C), 0.55)
+    out = torch.full((B, T, C), float("nan"), dtype=torch.float32, device="cuda")
+    wsz = ab.attention_workspace_size(B, T, C, precision)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
+    ab.attention_forward(out, dev(qkv), B, T, C, NH, precision, ws, wsz)
+    no_device_error()
+    got = host(out)
+    assert np.isfinite(got).all()
+    for b in (0, B - 1):
+        assert_close(got[b:b + 1], oracle.attention(qkv[b:b + 1], NH), atol=TOL[precision], what=f"sequence {b}")
+
+
 def test_attention_causal_bitwise():
     B, T, C, NH = 1, 150, 768, 12
     qkv = inputs.make_normal(9, (B, T, 3 * C), 0.55)

@@ -112,6 +112,21 @@ def test_tensor_core_backward_is_deterministic():
     np.testing.assert_array_equal(a, b)
 
 
+def test_ragged_launch_with_several_items_per_cta():
+    # B=8, T=1100, 12 heads: 9 tiles per (sequence, head), 864 items per
+    # kernel on 152 CTAs, the shortest items (the last key tile's dK/dV, the
+    # first query tile's dQ) one tile long and the last tile ragged
+    B, T, C, NH = 8, 1100, 768, 12
+    qkv, dout = make_inputs(B, T, C, seed=6)
+    qkv_d = dev(qkv, torch.float32)
+    out_d = torch.empty((B, T, C), dtype=torch.float32, device="cuda")
+    ab.attention_forward(out_d, qkv_d, B, T, C, NH, ab.GPT2_FP32, None, 0)
+    got = gpu_backward(qkv, dout, host(out_d), NH)
+    for b in (0, B - 1):
+        ref = oracle.attention_backward(qkv[b:b + 1], dout[b:b + 1], NH)
+        check_blocks(got[b:b + 1], ref, C, f"sequence {b}")
+
+
 def test_full_batch_launch_sampled():
     # the B=16 T=1024 launch the training step makes; sequences 0 and 15
     # against the oracle
