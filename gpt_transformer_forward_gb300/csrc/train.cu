@@ -185,14 +185,38 @@ __global__ void column_partial_kernel(float* __restrict__ part, const float* __r
   }
 }
 
-// out[c] = (out[c] +) sum over the parts of part[p][c], in part order
-__global__ void column_sum_kernel(float* __restrict__ out, const float* __restrict__ part, int parts, int cols,
-                                  int accumulate) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
-  float s = accumulate ? out[c] : 0.f;
-  for (int p = 0; p < parts; ++p) s += part[static_cast<size_t>(p) * cols + c];
-  out[c] = s;
+// out[c] = (out[c] +) sum over the parts of part[p][c].  A block of 256
+// threads takes 32 columns: warp g sums parts g, g + 8, ... of its lane's
+// column in part order (each warp load one 128-byte row piece), and the
+// eight sums are added in warp order, a fixed order, so the result does
+// not depend on timing.  (One thread per column, adding all its parts in
+// turn, left a 768-column reduction 3 blocks for the whole GPU: about 20 us
+// per launch, measured.)
+constexpr int kColSumCols = 32;
+constexpr int kColSumGroups = 8;
+__global__ void __launch_bounds__(kColSumCols* kColSumGroups)
+    column_sum_kernel(float* __restrict__ out, const float* __restrict__ part, int parts, int cols, int accumulate) {
+  __shared__ float red[kColSumGroups][kColSumCols + 1];
+  const int cl = threadIdx.x % kColSumCols, g = threadIdx.x / kColSumCols;
+  const int c = blockIdx.x * kColSumCols + cl;
+  float s = 0.f;
+  if (c < cols) {
+#pragma unroll 4
+    for (int p = g; p < parts; p += kColSumGroups) s += __ldg(part + static_cast<size_t>(p) * cols + c);
+  }
+  red[g][cl] = s;
+  __syncthreads();
+  if (g == 0 && c < cols) {
+    float t = accumulate ? out[c] : 0.f;
+#pragma unroll
+    for (int k = 0; k < kColSumGroups; ++k) t += red[k][cl];
+    out[c] = t;
+  }
+}
+
+void launch_column_sum_parts(float* out, const float* part, int parts, int cols, bool accumulate, cudaStream_t s) {
+  column_sum_kernel<<<(cols + kColSumCols - 1) / kColSumCols, kColSumCols * kColSumGroups, 0, s>>>(
+      out, part, parts, cols, accumulate ? 1 : 0);
 }
 
 // LayerNorm backward, one warp per row: with xhat = (x - mean) rstd and
@@ -376,7 +400,7 @@ void launch_column_sum(float* out, float* part, const float* in, int rows, int c
   const int per_block = vec ? 1024 : 256;  // columns per block of 256 threads
   column_partial_kernel<<<dim3((cols + per_block - 1) / per_block, parts), 256, 0, s>>>(part, in, rows, cols,
                                                                                        kPartRows, vec);
-  column_sum_kernel<<<(cols + 255) / 256, 256, 0, s>>>(out, part, parts, cols, accumulate ? 1 : 0);
+  launch_column_sum_parts(out, part, parts, cols, accumulate, s);
 }
 
 void launch_layernorm_backward(float* dx, float* dw, float* db, float* part, const float* dy, const float* x,
@@ -393,8 +417,8 @@ void launch_layernorm_backward(float* dx, float* dw, float* db, float* part, con
   const int per_block = vec ? 1024 : 256;
   layernorm_backward_wb_kernel<<<dim3((C + per_block - 1) / per_block, parts), 256, 0, s>>>(
       part_w, part_b, dy, x, mean, rstd, N, C, kPartRows, vec);
-  column_sum_kernel<<<(C + 255) / 256, 256, 0, s>>>(dw, part_w, parts, C, 0);
-  column_sum_kernel<<<(C + 255) / 256, 256, 0, s>>>(db, part_b, parts, C, 0);
+  launch_column_sum_parts(dw, part_w, parts, C, false, s);
+  launch_column_sum_parts(db, part_b, parts, C, false, s);
 }
 
 void launch_gelu_backward(float* dinp, const float* inp, const float* dout, long long n, cudaStream_t s) {
