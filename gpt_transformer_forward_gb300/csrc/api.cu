@@ -285,8 +285,8 @@ struct StageProfiler {
 // fp32 activations of every layer kept for the backward, and the backward's
 // scratch; offsets in bytes, each 256-byte aligned.
 struct TrainLayout {
-  size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj, dx,
-      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, splitk, total;
+  size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, qkv16, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj,
+      dx, dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, splitk, total;
 };
 
 // the K-split partial products of the weight gradients: up to 16 slices of
@@ -313,6 +313,7 @@ TrainLayout train_layout(const GPT2Config* c, int B, int T) {
   t.ln2m = take(L * N);
   t.ln2r = take(L * N);
   t.qkv = take(L * 3 * NC);
+  t.qkv16 = take((L * 3 * NC + 1) / 2);  // every layer's bf16 copy of qkv (the tf32 mode's attention operands)
   t.att = take(L * NC);
   t.fc = take(L * 4 * NC);
   t.fcg = take(L * 4 * NC);
@@ -889,10 +890,11 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
   float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
   float *part = buf(tl.part), *attn = buf(tl.attn), *lse = buf(tl.lse), *splitk = buf(tl.splitk);
-  // the tf32 mode's bf16 copy of one layer's qkv, and of the attention
-  // output's gradient, in the backward's scratch (free while they are used)
-  void* qkv16 = dt;
-  void* do16 = ws + tl.dt + round_up(3 * NC * 2, 256);
+  // the tf32 mode's bf16 copies of each layer's qkv, made by the forward and
+  // read again by the backward, and of the attention output's gradient, in
+  // the backward's scratch (free while it is used)
+  auto qkv16 = [&](int l) { return static_cast<void*>(ws + tl.qkv16 + l * 3 * NC * 2); };
+  void* do16 = ws + tl.dt;
   // tf32 with head size 64: attention forward and backward on tcgen05, the
   // forward keeping each row's log-sum-exp (per layer) for the backward
   const bool attn_tc = precision == GPT2_TF32 && C / NH == 64;
@@ -911,11 +913,11 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
     if (precision == GPT2_FP32) {
       TRY(launch_attention_f32(att + l * NC, qkv + l * 3 * NC, B, T, C, NH, s));
     } else {  // as in the forward pass's tf32 mode: the bf16 tensor-core kernel on a bf16 copy of qkv
-      to16(GPT2_BF16, qkv16, qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
+      to16(GPT2_BF16, qkv16(l), qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
       if (attn_tc)
-        TRY(launch_attention_tc05(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s, lse + l * SL));
+        TRY(launch_attention_tc05(att + l * NC, false, qkv16(l), kOpBF16, B, T, C, NH, s, lse + l * SL));
       else
-        TRY(launch_attention_16(att + l * NC, false, qkv16, kOpBF16, B, T, C, NH, s));
+        TRY(launch_attention_16(att + l * NC, false, qkv16(l), kOpBF16, B, T, C, NH, s));
     }
     TRY(gemm(precision, proj, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, N, C, C, kEpiF32, s));
     launch_residual(xmid + l * NC, x, proj, static_cast<int>(NC), s);
@@ -965,9 +967,8 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
     // x_mid = x_in + attproj(attention(qkv(LN1(x_in)))); dx = dL/dx_mid
     TRY(mm_bwd(dh, G(po.attprojw) + l * CC, G(po.attprojb) + l * C, dx, att + l * NC, P(po.attprojw) + l * CC, C, C));
     if (attn_tc) {
-      to16(GPT2_BF16, qkv16, qkv + l * 3 * NC, static_cast<long long>(3 * NC), s);
       launch_attn_bwd_prep(do16, attn, lse + l * SL, dh, att + l * NC, B, T, C, NH, s);
-      TRY(launch_attention_backward_tc05(dqkv, qkv16, do16, lse + l * SL, attn, B, T, C, NH, s));
+      TRY(launch_attention_backward_tc05(dqkv, qkv16(l), do16, lse + l * SL, attn, B, T, C, NH, s));
     } else {
       TRY(launch_attention_backward(dqkv, dh, qkv + l * 3 * NC, att + l * NC, attn,
                                     attn + static_cast<size_t>(B) * NH * T, B, T, C, NH, s));
