@@ -285,8 +285,8 @@ struct StageProfiler {
 // fp32 activations of every layer kept for the backward, and the backward's
 // scratch; offsets in bytes, each 256-byte aligned.
 struct TrainLayout {
-  size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, qkv16, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, proj,
-      dx, dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, splitk, total;
+  size_t xin, xmid, ln1, ln2, ln1m, ln1r, ln2m, ln2r, qkv, qkv16, att, fc, fcg, lnf, lnfm, lnfr, logits, losses, dx,
+      dh, dt, dt2, dqkv, tA, tB, Wt, part, attn, lse, splitk, total;
 };
 
 // the K-split partial products of the weight gradients: up to 16 slices of
@@ -322,7 +322,6 @@ TrainLayout train_layout(const GPT2Config* c, int B, int T) {
   t.lnfr = take(N);
   t.logits = take(N * Vp);
   t.losses = take(N);
-  t.proj = take(NC);
   t.dx = take(NC);
   t.dh = take(NC);
   t.dt = take(4 * NC);
@@ -887,7 +886,7 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   float *ln1m = buf(tl.ln1m), *ln1r = buf(tl.ln1r), *ln2m = buf(tl.ln2m), *ln2r = buf(tl.ln2r);
   float *qkv = buf(tl.qkv), *att = buf(tl.att), *fc = buf(tl.fc), *fcg = buf(tl.fcg);
   float *lnf = buf(tl.lnf), *lnfm = buf(tl.lnfm), *lnfr = buf(tl.lnfr), *logits = buf(tl.logits);
-  float *losses = buf(tl.losses), *proj = buf(tl.proj), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
+  float *losses = buf(tl.losses), *dx = buf(tl.dx), *dh = buf(tl.dh), *dt = buf(tl.dt);
   float *dt2 = buf(tl.dt2), *dqkv = buf(tl.dqkv), *tA = buf(tl.tA), *tB = buf(tl.tB), *Wt = buf(tl.Wt);
   float *part = buf(tl.part), *attn = buf(tl.attn), *lse = buf(tl.lse), *splitk = buf(tl.splitk);
   // the tf32 mode's bf16 copies of each layer's qkv, made by the forward and
@@ -902,6 +901,18 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   const ParamOffsets po = param_offsets(cfg);
   auto P = [&](size_t off) { return params + off; };
   auto G = [&](size_t off) { return grads + off; };
+  // out = resid + A W^T + bias over the N rows: on tf32 tensor cores the
+  // residual is added in the GEMM's epilogue (the same two fp32 additions
+  // as a separate pass, without writing and reading the product); else the
+  // product, then the residual add in place
+  auto gemm_residual = [&](float* out, const float* resid, const float* A, const float* W, const float* bias, int OC,
+                           int IC) -> int {
+    if (precision == GPT2_TF32 && N > kSkinnyMaxRows)
+      return launch_gemm_tc(out, A, W, bias, N, OC, IC, kEpiResidF32, kOpTF32, s, resid);
+    TRY(gemm(precision, out, A, W, bias, N, OC, IC, kEpiF32, s));
+    launch_residual(out, resid, out, static_cast<int>(static_cast<size_t>(N) * OC), s);
+    return check_launch();
+  };
   // ---------------------------------------------------------------- forward
   launch_encoder(xin, tok, P(po.wte), P(po.wpe), N, T, C, V, s);
   for (int l = 0; l < L; ++l) {
@@ -919,16 +930,14 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
       else
         TRY(launch_attention_16(att + l * NC, false, qkv16(l), kOpBF16, B, T, C, NH, s));
     }
-    TRY(gemm(precision, proj, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, N, C, C, kEpiF32, s));
-    launch_residual(xmid + l * NC, x, proj, static_cast<int>(NC), s);
+    TRY(gemm_residual(xmid + l * NC, x, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, C, C));
     launch_layernorm_f32(ln2 + l * NC, ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N,
                          xmid + l * NC, P(po.ln2w) + l * C, P(po.ln2b) + l * C, N, C, s);
     TRY(gemm(precision, fc + l * 4 * NC, ln2 + l * NC, P(po.fcw) + l * 4 * CC, P(po.fcb) + l * 4 * C, N, 4 * C, C,
              kEpiF32, s));
     launch_gelu(fcg + l * 4 * NC, fc + l * 4 * NC, static_cast<int>(4 * NC), s);
-    TRY(gemm(precision, proj, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC, P(po.fcprojb) + l * C, N, C, 4 * C,
-             kEpiF32, s));
-    launch_residual(xin + (l + 1) * NC, xmid + l * NC, proj, static_cast<int>(NC), s);
+    TRY(gemm_residual(xin + (l + 1) * NC, xmid + l * NC, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC,
+                      P(po.fcprojb) + l * C, C, 4 * C));
   }
   launch_layernorm_f32(lnf, lnfm, lnfr, xin + L * NC, P(po.lnfw), P(po.lnfb), N, C, s);
   TRY(gemm(precision, logits, lnf, P(po.wte), nullptr, N, Vp, C, kEpiF32, s));

@@ -80,9 +80,9 @@ __host__ __device__ constexpr int stat_blocks(int N) { return 2 * gridDim_n(N); 
 template <int kEpi, int kOp, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const __grid_constant__ CUtensorMap tmap_out, const float* __restrict__ bias, int M, int N,
-                   int K, int tiles_m, int num_tiles, int n_fast, float2* __restrict__ row_stats, int V,
-                   int tiles_mn, int kb_per_split) {
+                   const __grid_constant__ CUtensorMap tmap_out, const __grid_constant__ CUtensorMap tmap_res,
+                   const float* __restrict__ bias, int M, int N, int K, int tiles_m, int num_tiles, int n_fast,
+                   float2* __restrict__ row_stats, int V, int tiles_mn, int kb_per_split) {
   using L = Layout<kPair>;
   constexpr int kStages = L::kStages;
   constexpr int kAStageBytes = L::kAStageBytes;
@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_out);
+    if constexpr (kEpi == kEpiResidF32) tma_prefetch_desc(&tmap_res);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -336,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             bulk_wait_group_read<0>();  // the previous store has read the buffer
             mbar_arrive_expect_tx(&res_bar[ew], kStageBufBytes);
-            tma_load_3d(stg, &tmap_out, &res_bar[ew], col0, m0, 0);
+            tma_load_3d(stg, &tmap_res, &res_bar[ew], col0, m0, 0);
           }
         }
         float v[kChunkCols];
@@ -540,9 +541,9 @@ namespace {
 
 template <int kEpi, int kOp, bool kPair>
 int launch_impl(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
-                float2* row_stats, int V, int splits = 1) {
+                float2* row_stats, int V, int splits = 1, const float* resid = nullptr) {
   using L = Layout<kPair>;
-  CUtensorMap ta, tb, to;
+  CUtensorMap ta, tb, to, tr;
   constexpr bool kTF32 = (kOp == kOpTF32);
   const CUtensorMapDataType dt16 =
       kOp == kOpF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -560,6 +561,11 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   } else {
     if (!make_out_map(&to, out, dt16, 2, M, N, splits, 64, 32)) return GPT2_ERR_CUDA;
   }
+  // the residual epilogue's addend: `resid` when given, else the output
+  // itself (out += ...)
+  tr = to;
+  if (kEpi == kEpiResidF32 && resid != nullptr && resid != out)
+    if (!make_out_map(&tr, resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 1, 32, 32)) return GPT2_ERR_CUDA;
   constexpr int kTileM = kPair ? 2 * kBM : kBM;
   const int tiles_m = (M + kTileM - 1) / kTileM;
   const int tiles_n = (N + kBN - 1) / kBN;
@@ -602,7 +608,7 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const int units = num_tiles < resident[dev] ? num_tiles : resident[dev];
   cfg.gridDim = dim3(kPair ? 2 * units : units);
   cfg.numAttrs = pdl_on() ? 2 : 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, bias, M, N, K, tiles_m, num_tiles, n_fast,
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, to, tr, bias, M, N, K, tiles_m, num_tiles, n_fast,
                                            row_stats, V, tiles_mn, kb_per_split);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
@@ -636,16 +642,17 @@ __global__ void splitk_sum_kernel(float* __restrict__ out, const float* __restri
 
 template <int kEpi, int kOp>
 int launch_typed(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, cudaStream_t s,
-                 float2* row_stats = nullptr, int V = 0) {
-  if (M > kBM) return launch_impl<kEpi, kOp, true>(out, A, B, bias, M, N, K, s, row_stats, V);
-  return launch_impl<kEpi, kOp, false>(out, A, B, bias, M, N, K, s, row_stats, V);
+                 float2* row_stats = nullptr, int V = 0, const float* resid = nullptr) {
+  if (M > kBM) return launch_impl<kEpi, kOp, true>(out, A, B, bias, M, N, K, s, row_stats, V, 1, resid);
+  return launch_impl<kEpi, kOp, false>(out, A, B, bias, M, N, K, s, row_stats, V, 1, resid);
 }
 
 }  // namespace
 
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
-                   cudaStream_t s) {
+                   cudaStream_t s, const float* resid) {
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
+  if (resid != nullptr && resid != out && (epi != kEpiResidF32 || M <= kSkinnyMaxRows)) return GPT2_ERR_UNSUPPORTED;
   if (M <= kSkinnyMaxRows) return launch_gemm_skinny(out, A, B, bias, M, N, K, epi, op, s);
   switch (op) {
     case kOpBF16:
@@ -653,7 +660,7 @@ int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, i
         case kEpiF32: return launch_typed<kEpiF32, kOpBF16>(out, A, B, bias, M, N, K, s);
         case kEpiOut16: return launch_typed<kEpiOut16, kOpBF16>(out, A, B, bias, M, N, K, s);
         case kEpiGelu16: return launch_typed<kEpiGelu16, kOpBF16>(out, A, B, bias, M, N, K, s);
-        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpBF16>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpBF16>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
       }
       break;
     case kOpF16:
@@ -661,13 +668,13 @@ int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, i
         case kEpiF32: return launch_typed<kEpiF32, kOpF16>(out, A, B, bias, M, N, K, s);
         case kEpiOut16: return launch_typed<kEpiOut16, kOpF16>(out, A, B, bias, M, N, K, s);
         case kEpiGelu16: return launch_typed<kEpiGelu16, kOpF16>(out, A, B, bias, M, N, K, s);
-        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpF16>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpF16>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
       }
       break;
     case kOpTF32:
       switch (epi) {
         case kEpiF32: return launch_typed<kEpiF32, kOpTF32>(out, A, B, bias, M, N, K, s);
-        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpTF32>(out, A, B, bias, M, N, K, s);
+        case kEpiResidF32: return launch_typed<kEpiResidF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
       }
       break;
   }
