@@ -947,10 +947,20 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
   // y = x W^T + b with x [N,K], W [OC,K]: dx = dy W (set), dW = dy^T x (set),
   // db = column sums of dy; the GEMM kernels take K-major operands, so W,
   // dy and x are transposed first
+  // dinp = dy W (times GELU'(gelu_in) when given: the gradient through the
+  // GELU that produced x, computed in the tf32 GEMM's epilogue, else by a
+  // separate pass from the scratch dt), dW = dy^T x, db = column sums of dy
   auto mm_bwd = [&](float* dinp, float* dW, float* db, const float* dy, const float* x, const float* W, int OC,
-                    int K) -> int {
+                    int K, const float* gelu_in = nullptr) -> int {
     launch_transpose(Wt, W, OC, K, s);  // [K][OC]
-    TRY(gemm(precision, dinp, dy, Wt, nullptr, N, K, OC, kEpiF32, s));
+    if (gelu_in != nullptr && precision == GPT2_TF32 && N > kSkinnyMaxRows) {
+      TRY(launch_gemm_tc(dinp, dy, Wt, nullptr, N, K, OC, kEpiGeluBwdF32, kOpTF32, s, gelu_in));
+    } else if (gelu_in != nullptr) {  // dy W into the scratch dt (4NC floats), then through the GELU
+      TRY(gemm(precision, dt, dy, Wt, nullptr, N, K, OC, kEpiF32, s));
+      launch_gelu_backward(dinp, gelu_in, dt, static_cast<long long>(N) * K, s);
+    } else {
+      TRY(gemm(precision, dinp, dy, Wt, nullptr, N, K, OC, kEpiF32, s));
+    }
     launch_transpose(tA, dy, N, OC, s);  // [OC][N]
     launch_transpose(tB, x, N, K, s);    // [K][N]
     if (precision == GPT2_FP32) {
@@ -966,9 +976,8 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
                             s);
   for (int l = L - 1; l >= 0; --l) {
     // x_out = x_mid + fcproj(GELU(fc(LN2(x_mid)))); dx = dL/dx_out
-    TRY(mm_bwd(dt, G(po.fcprojw) + l * 4 * CC, G(po.fcprojb) + l * C, dx, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC,
-               C, 4 * C));
-    launch_gelu_backward(dt2, fc + l * 4 * NC, dt, static_cast<long long>(4 * NC), s);
+    TRY(mm_bwd(dt2, G(po.fcprojw) + l * 4 * CC, G(po.fcprojb) + l * C, dx, fcg + l * 4 * NC,
+               P(po.fcprojw) + l * 4 * CC, C, 4 * C, fc + l * 4 * NC));
     TRY(mm_bwd(dh, G(po.fcw) + l * 4 * CC, G(po.fcb) + l * 4 * C, dt2, ln2 + l * NC, P(po.fcw) + l * 4 * CC, 4 * C,
                C));
     launch_layernorm_backward(dx, G(po.ln2w) + l * C, G(po.ln2b) + l * C, part, dh, xmid + l * NC, P(po.ln2w) + l * C,

@@ -600,6 +600,14 @@ __device__ __forceinline__ float gelu_exact(float x) {
   return 0.5f * x * (1.0f + tanhf(k * (x + 0.044715f * x * x * x)));
 }
 
+// d/dx of the tanh-form GELU: with u = sqrt(2/pi) (x + 0.044715 x^3),
+// 0.5 (1 + tanh u) + 0.5 x (1 - tanh^2 u) sqrt(2/pi) (1 + 3 * 0.044715 x^2)
+__device__ __forceinline__ float gelu_grad(float x) {
+  const float k = 0.7978845608028654f;  // sqrt(2/pi)
+  const float th = tanhf(k * (x + 0.044715f * x * x * x));
+  return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * k * (1.f + 3.f * 0.044715f * x * x);
+}
+
 __device__ __forceinline__ float gelu_fast(float x) {
   const float k = 0.7978845608028654f;
   return 0.5f * x * (1.0f + tanh_fast(k * (x + 0.044715f * x * x * x)));

@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_out);
-    if constexpr (kEpi == kEpiResidF32) tma_prefetch_desc(&tmap_res);
+    if constexpr (kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32) tma_prefetch_desc(&tmap_res);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -324,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile;
       const int n0 = n_blk * kBN;
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
-      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
+      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits || kEpi == kEpiGeluBwdF32);
+      constexpr bool kAux = (kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32);  // reads a tile of tmap_res
       constexpr int kChunkCols = kOutF32 ? 32 : 64;  // 128 bytes of output per row
       // logits epilogue: this row's running max and sum of exp over the
       // tile's columns below V
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = col_half * (kBN / kChunkCols / 2); ch < (col_half + 1) * (kBN / kChunkCols / 2); ++ch) {
         const int col0 = n0 + ch * kChunkCols;
         bool ok = true;
-        if constexpr (kEpi == kEpiResidF32) {  // the residual tile into the staging buffer
+        if constexpr (kAux) {  // the residual (or GELU input) tile into the staging buffer
           if (lane == 0) {
             bulk_wait_group_read<0>();  // the previous store has read the buffer
             mbar_arrive_expect_tx(&res_bar[ew], kStageBufBytes);
@@ -390,21 +391,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Stage the chunk (32 rows x 128 bytes, 128-byte swizzle) in this
         // warp's buffer and TMA-store it.  One buffer per warp: the store of
         // the previous chunk has had this chunk's loads and math to read it.
-        if (kEpi != kEpiResidF32 && lane == 0) bulk_wait_group_read<0>();
+        if (!kAux && lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
         const int sw = lane & 7;
         uint8_t* my_row = stg + lane * 128;
         if constexpr (kOutF32) {
-          if constexpr (kEpi == kEpiResidF32) {
+          if constexpr (kAux) {
             ok = __all_sync(0xffffffffu, mbar_wait(&res_bar[ew], res_phase));
             res_phase ^= 1u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const float4 old = *reinterpret_cast<const float4*>(my_row + ((j ^ sw) << 4));
-              v[4 * j] += old.x;
-              v[4 * j + 1] += old.y;
-              v[4 * j + 2] += old.z;
-              v[4 * j + 3] += old.w;
+              if constexpr (kEpi == kEpiResidF32) {
+                v[4 * j] += old.x;
+                v[4 * j + 1] += old.y;
+                v[4 * j + 2] += old.z;
+                v[4 * j + 3] += old.w;
+              } else {  // the gradient through the GELU whose input is old
+                v[4 * j] *= gelu_grad(old.x);
+                v[4 * j + 1] *= gelu_grad(old.y);
+                v[4 * j + 2] *= gelu_grad(old.z);
+                v[4 * j + 3] *= gelu_grad(old.w);
+              }
             }
           }
 #pragma unroll
@@ -550,7 +558,7 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const CUtensorMapDataType dt_in = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt16;
   const int eb = kTF32 ? 4 : 2;
   const int bk = kRowBytes / eb;
-  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits);
+  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits || kEpi == kEpiGeluBwdF32);
   if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
   if (!make_map(&tb, B, dt_in, eb, N, K, bk, L::kBRows)) return GPT2_ERR_CUDA;
   const int num_kb = (K + bk - 1) / bk;
@@ -561,10 +569,10 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   } else {
     if (!make_out_map(&to, out, dt16, 2, M, N, splits, 64, 32)) return GPT2_ERR_CUDA;
   }
-  // the residual epilogue's addend: `resid` when given, else the output
-  // itself (out += ...)
+  // the tile source of the epilogues that read one: `resid` when given,
+  // else the output itself (the residual epilogue's out += ...)
   tr = to;
-  if (kEpi == kEpiResidF32 && resid != nullptr && resid != out)
+  if ((kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32) && resid != nullptr && resid != out)
     if (!make_out_map(&tr, resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 1, 32, 32)) return GPT2_ERR_CUDA;
   constexpr int kTileM = kPair ? 2 * kBM : kBM;
   const int tiles_m = (M + kTileM - 1) / kTileM;
@@ -652,7 +660,10 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s, const float* resid) {
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
-  if (resid != nullptr && resid != out && (epi != kEpiResidF32 || M <= kSkinnyMaxRows)) return GPT2_ERR_UNSUPPORTED;
+  if (resid != nullptr && resid != out && (epi != kEpiResidF32 || M <= kSkinnyMaxRows) && epi != kEpiGeluBwdF32)
+    return GPT2_ERR_UNSUPPORTED;
+  if (epi == kEpiGeluBwdF32 && (resid == nullptr || resid == out || M <= kSkinnyMaxRows || op != kOpTF32))
+    return GPT2_ERR_UNSUPPORTED;
   if (M <= kSkinnyMaxRows) return launch_gemm_skinny(out, A, B, bias, M, N, K, epi, op, s);
   switch (op) {
     case kOpBF16:
@@ -675,6 +686,8 @@ int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, i
       switch (epi) {
         case kEpiF32: return launch_typed<kEpiF32, kOpTF32>(out, A, B, bias, M, N, K, s);
         case kEpiResidF32: return launch_typed<kEpiResidF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
+        case kEpiGeluBwdF32:
+          return launch_typed<kEpiGeluBwdF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
       }
       break;
   }

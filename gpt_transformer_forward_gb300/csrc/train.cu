@@ -294,14 +294,9 @@ __global__ void layernorm_backward_wb_kernel(float* __restrict__ part_w, float* 
 // dinp = dout * GELU'(inp), GELU in the tanh form
 __global__ void gelu_backward_kernel(float* __restrict__ dinp, const float* __restrict__ inp,
                                      const float* __restrict__ dout, long long n) {
-  const float k = 0.7978845608028654f;  // sqrt(2/pi)
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float x = inp[i];
-    const float th = tanhf(k * (x + 0.044715f * x * x * x));
-    const float d = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * k * (1.f + 3.f * 0.044715f * x * x);
-    dinp[i] = dout[i] * d;
-  }
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    dinp[i] = dout[i] * gelu_grad(inp[i]);
 }
 
 // dwpe[t][c] = sum over sequences of dx[b][t][c] (positions < T)
