@@ -933,9 +933,14 @@ int gpt2_forward_backward(const GPT2Config* cfg, const float* params, float* gra
     TRY(gemm_residual(xmid + l * NC, x, att + l * NC, P(po.attprojw) + l * CC, P(po.attprojb) + l * C, C, C));
     launch_layernorm_f32(ln2 + l * NC, ln2m + static_cast<size_t>(l) * N, ln2r + static_cast<size_t>(l) * N,
                          xmid + l * NC, P(po.ln2w) + l * C, P(po.ln2b) + l * C, N, C, s);
-    TRY(gemm(precision, fc + l * 4 * NC, ln2 + l * NC, P(po.fcw) + l * 4 * CC, P(po.fcb) + l * 4 * C, N, 4 * C, C,
-             kEpiF32, s));
-    launch_gelu(fcg + l * 4 * NC, fc + l * 4 * NC, static_cast<int>(4 * NC), s);
+    if (precision == GPT2_TF32 && N > kSkinnyMaxRows) {  // pre-activation and GELU from one epilogue
+      TRY(launch_gemm_tc(fc + l * 4 * NC, ln2 + l * NC, P(po.fcw) + l * 4 * CC, P(po.fcb) + l * 4 * C, N, 4 * C, C,
+                         kEpiGeluDualF32, kOpTF32, s, fcg + l * 4 * NC));
+    } else {
+      TRY(gemm(precision, fc + l * 4 * NC, ln2 + l * NC, P(po.fcw) + l * 4 * CC, P(po.fcb) + l * 4 * C, N, 4 * C, C,
+               kEpiF32, s));
+      launch_gelu(fcg + l * 4 * NC, fc + l * 4 * NC, static_cast<int>(4 * NC), s);
+    }
     TRY(gemm_residual(xin + (l + 1) * NC, xmid + l * NC, fcg + l * 4 * NC, P(po.fcprojw) + l * 4 * CC,
                       P(po.fcprojb) + l * C, C, 4 * C));
   }

@@ -148,7 +148,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmap_a);
     tma_prefetch_desc(&tmap_b);
     tma_prefetch_desc(&tmap_out);
-    if constexpr (kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32) tma_prefetch_desc(&tmap_res);
+    if constexpr (kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32 || kEpi == kEpiGeluDualF32)
+      tma_prefetch_desc(&tmap_res);
   }
   if (warp == 1) {
     if constexpr (kPair) {
@@ -324,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m0 = m_blk * kTileM + static_cast<int>(rank) * kBM + row_in_tile;
       const int n0 = n_blk * kBN;
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(row_in_tile) << 16) + static_cast<uint32_t>(acc * kBN);
-      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits || kEpi == kEpiGeluBwdF32);
+      constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits ||
+                                kEpi == kEpiGeluBwdF32 || kEpi == kEpiGeluDualF32);
       constexpr bool kAux = (kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32);  // reads a tile of tmap_res
       constexpr int kChunkCols = kOutF32 ? 32 : 64;  // 128 bytes of output per row
       // logits epilogue: this row's running max and sum of exp over the
@@ -442,6 +444,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_store_3d(&tmap_out, stg, col0, m0, tile / tiles_mn);  // the split's slice of the output
           bulk_commit_group();
         }
+        if constexpr (kEpi == kEpiGeluDualF32) {
+          // the chunk's GELU, the second output, through the same buffer
+          // once the store above has read it
+          if (lane == 0) bulk_wait_group_read<0>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(my_row + ((j ^ sw) << 4)) =
+                make_float4(gelu_exact(v[4 * j]), gelu_exact(v[4 * j + 1]), gelu_exact(v[4 * j + 2]),
+                            gelu_exact(v[4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmap_res, stg, col0, m0, 0);
+            bulk_commit_group();
+          }
+        }
         if (!ok) {
           *abort_flag = 1;
           break;
@@ -558,7 +577,8 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   const CUtensorMapDataType dt_in = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : dt16;
   const int eb = kTF32 ? 4 : 2;
   const int bk = kRowBytes / eb;
-  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits || kEpi == kEpiGeluBwdF32);
+  constexpr bool kOutF32 = (kEpi == kEpiF32 || kEpi == kEpiResidF32 || kEpi == kEpiLogits ||
+                            kEpi == kEpiGeluBwdF32 || kEpi == kEpiGeluDualF32);
   if (!make_map(&ta, A, dt_in, eb, M, K, bk, kBM)) return GPT2_ERR_CUDA;
   if (!make_map(&tb, B, dt_in, eb, N, K, bk, L::kBRows)) return GPT2_ERR_CUDA;
   const int num_kb = (K + bk - 1) / bk;
@@ -572,7 +592,8 @@ int launch_impl(void* out, const void* A, const void* B, const float* bias, int 
   // the tile source of the epilogues that read one: `resid` when given,
   // else the output itself (the residual epilogue's out += ...)
   tr = to;
-  if ((kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32) && resid != nullptr && resid != out)
+  if ((kEpi == kEpiResidF32 || kEpi == kEpiGeluBwdF32 || kEpi == kEpiGeluDualF32) && resid != nullptr &&
+      resid != out)
     if (!make_out_map(&tr, resid, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, M, N, 1, 32, 32)) return GPT2_ERR_CUDA;
   constexpr int kTileM = kPair ? 2 * kBM : kBM;
   const int tiles_m = (M + kTileM - 1) / kTileM;
@@ -660,9 +681,10 @@ int launch_typed(void* out, const void* A, const void* B, const float* bias, int
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s, const float* resid) {
   if (M <= 0 || N <= 0 || K <= 0) return GPT2_OK;
-  if (resid != nullptr && resid != out && (epi != kEpiResidF32 || M <= kSkinnyMaxRows) && epi != kEpiGeluBwdF32)
+  const bool two_tensor = epi == kEpiGeluBwdF32 || epi == kEpiGeluDualF32;  // resid required
+  if (resid != nullptr && resid != out && (epi != kEpiResidF32 || M <= kSkinnyMaxRows) && !two_tensor)
     return GPT2_ERR_UNSUPPORTED;
-  if (epi == kEpiGeluBwdF32 && (resid == nullptr || resid == out || M <= kSkinnyMaxRows || op != kOpTF32))
+  if (two_tensor && (resid == nullptr || resid == out || M <= kSkinnyMaxRows || op != kOpTF32))
     return GPT2_ERR_UNSUPPORTED;
   if (M <= kSkinnyMaxRows) return launch_gemm_skinny(out, A, B, bias, M, N, K, epi, op, s);
   switch (op) {
@@ -688,6 +710,8 @@ int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, i
         case kEpiResidF32: return launch_typed<kEpiResidF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
         case kEpiGeluBwdF32:
           return launch_typed<kEpiGeluBwdF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
+        case kEpiGeluDualF32:
+          return launch_typed<kEpiGeluDualF32, kOpTF32>(out, A, B, bias, M, N, K, s, nullptr, 0, resid);
       }
       break;
   }

@@ -111,15 +111,16 @@ enum GemmEpilogue {
   kEpiGelu16 = 2,    // out 16-bit = GELU(acc + bias)
   kEpiResidF32 = 3,  // out fp32 = resid + acc (+ bias): resid is out (in place) unless given
   kEpiLogits = 4,    // out fp32 = acc, plus per-(row, 256-column tile) softmax statistics
-  kEpiGeluBwdF32 = 5 // out fp32 = acc * GELU'(aux), aux the fp32 [M,N] GELU input (tf32 operands only)
+  kEpiGeluBwdF32 = 5, // out fp32 = acc * GELU'(aux), aux the fp32 [M,N] GELU input (tf32 operands only)
+  kEpiGeluDualF32 = 6 // out fp32 = acc (+ bias), and aux fp32 = GELU(out) (tf32 operands only)
 };
 // Operand types of the tensor-core kernels.
 enum OperandType { kOpBF16 = 0, kOpF16 = 1, kOpTF32 = 2 };
 // Returns a GPT2_ERR_* code (tensor-map encoding can fail on bad strides).
 // The 16-bit epilogues exist for the bf16 and fp16 operand types.  resid:
-// the fp32 [M,N] tile source of the epilogues that read one while out is
-// written, M > kSkinnyMaxRows: the residual epilogue's addend (out itself,
-// in place, when null) or kEpiGeluBwdF32's GELU input (required).
+// a second fp32 [M,N] tensor of the epilogue, M > kSkinnyMaxRows: the
+// residual epilogue's addend (out itself, in place, when null),
+// kEpiGeluBwdF32's GELU input or kEpiGeluDualF32's GELU output (required).
 int launch_gemm_tc(void* out, const void* A, const void* B, const float* bias, int M, int N, int K, int epi, int op,
                    cudaStream_t s, const float* resid = nullptr);
 
