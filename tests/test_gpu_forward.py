@@ -141,6 +141,23 @@ def test_gpt2_124m_sampled(name):
     check_sampled(w, ab.GPT2_FP16, logits, probs, params, tok, 64, w.B - 1)
 
 
+@pytest.mark.parametrize("precision", [ab.GPT2_FP16, ab.GPT2_TF32])
+def test_gpt2_124m_ragged_several_attention_units_per_cta(precision):
+    # GPT-2 124M, B=8 sequences of T=600 tokens: 5 query tiles per sequence
+    # (the last ragged), so 3 attention units per (sequence, head), the last
+    # with one query tile; 288 units on 152 CTAs, several per CTA.  Every row
+    # of sequence 7 and the first 64 rows of sequence 0 against the oracle.
+    w = inputs.Workload("gpt2-124m-b8-t600", inputs.GPT2_124M, B=8, T=600, index=1)
+    params = inputs.make_params(w.cfg, 1001, "gpt2")
+    tok = inputs.make_tokens(2601, w.B, w.T, w.cfg.vocab_size)
+    m = GPT2Model(w.cfg, params, w.B, w.T, precision)
+    logits, probs = m.new_outputs(w.B, w.T)
+    m.forward(dev(tok), logits, probs)
+    no_device_error()
+    check_properties(w.cfg, logits, probs)
+    check_sampled(w, precision, logits, probs, params, tok, 64, w.B - 1)
+
+
 def test_gpt2_medium_sampled():
     w = inputs.WORKLOADS["gpt2-medium-b8"]
     params, tok = inputs.workload_inputs(w)
