@@ -81,6 +81,19 @@ def test_head_size_64_ragged_tiles(precision, T):
     check(cfg, params, tok, tgt, precision, f"hs64 T={T}")
 
 
+def test_several_attention_units_per_cta_ragged():
+    # head size 64 in tf32 mode, B=16 sequences of T=600: 3 attention units
+    # per (sequence, head), the last with one query tile, 192 units on 152
+    # CTAs (several per CTA), the backward's items likewise; 9600 rows, not
+    # a multiple of the GEMM tiles (the residual and GELU epilogues)
+    cfg = inputs.GPT2Config(max_seq_len=640, vocab_size=512, padded_vocab_size=512, num_layers=2, num_heads=4,
+                            channels=256)
+    params = inputs.make_params(cfg, 39, "perturbed")
+    tok = inputs.make_tokens(40, 16, 600, cfg.vocab_size)
+    tgt = inputs.make_tokens(41, 16, 600, cfg.vocab_size)
+    check(cfg, params, tok, tgt, ab.GPT2_TF32, "B=16 T=600")
+
+
 @pytest.mark.parametrize("precision", [ab.GPT2_FP32, ab.GPT2_TF32])
 def test_124m_width_one_layer(precision):
     cfg = dataclasses.replace(inputs.GPT2_124M, num_layers=1)
