@@ -14,12 +14,14 @@
 // one runs, and its steps continue the same rings, so the first loads and
 // the epilogue of a unit overlap the work of its neighbours (measured: a
 // CTA per unit spent about 5700 cycles before its first S and 1800 in its
-// last epilogue, a quarter of the longest unit's time).  The score tiles of both form one sequence of steps (A and B
-// take turns on each key tile while both have one; B's last tile follows
-// alone) that rotates through three S accumulators in TMEM; P of a step is
-// written over the first half of its S buffer (16-bit, two per column) and
-// read from there by the P V instruction, so S of step s + 3 is issued into
-// that buffer right after P V of step s.
+// last epilogue, a quarter of the longest unit's time).  The score tiles of
+// both form one sequence of steps (A and B take turns on each key tile while
+// both have one; B's last tile follows alone) that rotates through three S
+// accumulators in TMEM; P of a step is written over the first half of its S
+// buffer (16-bit, two per column) and read from there by the P V
+// instruction, so S of step s + 3 is issued into that buffer right after P V
+// of step s.  S is signalled to each group on a barrier of its own per
+// buffer: a group walks only its own steps.
 //   warp 0      TMA: per unit its two Q tiles (two buffers), then K and V
 //               tiles (128 keys x 64 dimensions each, 128-byte swizzle; one
 //               barrier for both) through a ring of three stages, from the
@@ -35,12 +37,11 @@
 //               issuing warps, not one: measured, a single warp spent about
 //               1800 cycles per step issuing 12 instructions and waiting on
 //               barriers, three times the tensor work.  Each runs its loop as
-//               a whole warp
-//               and one elected lane issues.  It waits once per key tile
-//               (K and V land together) and frees the stage with one commit
-//               after the tile's last P V: measured, each wait and commit
-//               of this warp costs a few hundred cycles in a busy SM, and
-//               this warp paces the kernel;
+//               a whole warp and one elected lane issues.  It waits once per
+//               key tile (K and V land together) and frees the stage with
+//               one commit after the tile's last P V: measured, each wait
+//               and commit of this warp costs a few hundred cycles in a busy
+//               SM;
 //   warps 2-5   softmax of group A, warps 6-9 softmax of group B, one thread
 //               per query row.  One pass over the S row from TMEM in chunks
 //               of 32 keys (the next chunk's load in flight): p = exp2(s *
