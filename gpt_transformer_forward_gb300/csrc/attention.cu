@@ -324,10 +324,13 @@ __global__ void __launch_bounds__(64) attn_f32_kernel(float* __restrict__ out, c
 // block of position p of sequence b is table[b][p / block] (the block-table
 // layout of a paged KV cache).  Positions come from `pos` (all sequences
 // at one position) or, when pos_arr is given, per sequence from it.
-constexpr int kDecWarps = 4;
+constexpr int kDecWarps = 4;       // warps computing; one more issues the copies
+constexpr int kDecStages = 8;      // chunks of the cache in shared memory
+constexpr int kDecStageBytes = 8192;  // a chunk's K rows, then its V rows (4 KB each)
+constexpr int kDecSmem = kDecStages * kDecStageBytes + 2 * kDecStages * 8;
 
 template <typename E, typename OutT, int HS>
-__global__ void __launch_bounds__(32 * kDecWarps)
+__global__ void __launch_bounds__(32 * (kDecWarps + 1))
     decode_attn_kernel(OutT* __restrict__ out, const E* __restrict__ qkv, E* __restrict__ kcache,
                        E* __restrict__ vcache, int C, int NH, int pos_all, const int* __restrict__ pos_arr,
                        KVRows rows, float scale_log2) {
@@ -336,7 +339,12 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   constexpr int kRPI = 32 / kLPR;                          // rows per warp instruction
   constexpr int kIt = 8;                                   // instructions per chunk (each of K, V)
   constexpr int kChunk = kIt * kRPI;                       // positions per chunk
+  constexpr int kRowBytes = HS * static_cast<int>(sizeof(E));
   static_assert(kLPR >= 1 && kLPR <= 32 && 32 % kLPR == 0, "head size and element type");
+  static_assert(kChunk * kRowBytes * 2 == kDecStageBytes, "a chunk's K and V fill a stage");
+  extern __shared__ __align__(16) uint8_t dec_smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(dec_smem + kDecStages * kDecStageBytes);
+  uint64_t* empty = full + kDecStages;
   __shared__ float m_s[kDecWarps], l_s[kDecWarps];
   __shared__ float o_s[kDecWarps][HS];
   __shared__ int tbl_s[kMaxBlocksPerSeq];  // this sequence's block table (paged layout)
@@ -348,6 +356,13 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   // before its first kernel: they may be read before the wait below
   const int pos = pos_arr != nullptr ? __ldg(pos_arr + b) : pos_all;
   const bool pos_ok = pos >= 0 && pos < rows.capacity;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kDecStages; ++i) {
+      mbar_init(&full[i], 1u);
+      mbar_init(&empty[i], 1u);
+    }
+    fence_barrier_init();
+  }
   if (rows.table != nullptr && pos_ok) {
     for (int i = threadIdx.x; i <= (pos >> rows.lbs); i += blockDim.x) {
       int blk = __ldg(rows.table + static_cast<size_t>(b) * rows.max_blocks + i);
@@ -364,112 +379,144 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     if (rows.table == nullptr) return (static_cast<size_t>(b) * NH + h) * rows.maxT + j;
     return ((static_cast<size_t>(tbl_s[j >> rows.lbs]) * NH + h) << rows.lbs) + (j & ((1 << rows.lbs) - 1));
   };
-  if (pos_ok) {
-    // The cache rows before pos were written by earlier steps: all of them
-    // (one layer's cache at a few hundred positions is tens of MB, well
-    // within L2) are requested into L2 while the QKV projection before this
-    // kernel finishes and leaves HBM mostly idle (a prefetch has no other
-    // effect; measured in a decode step against prefetching each warp's
-    // first chunk only, 1 % faster).  A row of 64 16-bit elements is one
-    // 128-byte line.
-    for (int j = threadIdx.x; j < pos; j += blockDim.x) {
+  // Cache rows [0, pos) (written by earlier steps) come through a ring of
+  // kDecStages chunks in shared memory, copied by the last warp with bulk
+  // copies (one per run of consecutive rows: the whole chunk in the dense
+  // layout, up to a block boundary in the paged one); the first kDecStages
+  // chunks are requested before the wait for the QKV projection, which
+  // leaves HBM mostly idle.  (With each warp loading its chunk into
+  // registers and waiting for it in turn, the kernel kept one chunk per warp
+  // in flight: measured, about 12 us per layer inside a decode step.)
+  const int n_cached = pos_ok ? (pos + kChunk - 1) / kChunk : 0;  // chunks with cache rows
+  uint32_t filled = 0, fill_par = 0;  // producer: stages ever filled, parity of their last fill
+  int issued = 0;
+  auto issue = [&](int c) -> bool {  // producer lane: chunk c into stage c % kDecStages
+    const int st = c % kDecStages;
+    if (c >= kDecStages && !mbar_wait(&empty[st], ((c / kDecStages) - 1) & 1)) return false;
+    const int j0 = c * kChunk, j1 = min(j0 + kChunk, pos);
+    uint8_t* kdst = dec_smem + st * kDecStageBytes;
+    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>((j1 - j0) * kRowBytes * 2));
+    for (int j = j0; j < j1;) {
+      const int run_end = rows.table == nullptr ? j1 : min(j1, ((j >> rows.lbs) + 1) << rows.lbs);
+      const uint32_t bytes = static_cast<uint32_t>((run_end - j) * kRowBytes);
       const size_t rj = row(j) * HS;
-      for (int off = 0; off < HS * static_cast<int>(sizeof(E)); off += 128) {
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(kcache + rj) + off));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(vcache + rj) + off));
-      }
+      bulk_load(kdst + (j - j0) * kRowBytes, kcache + rj, bytes, &full[st]);
+      bulk_load(kdst + kDecStageBytes / 2 + (j - j0) * kRowBytes, vcache + rj, bytes, &full[st]);
+      j = run_end;
     }
-  }
+    filled |= 1u << st;
+    fill_par = (fill_par & ~(1u << st)) | ((static_cast<uint32_t>(c / kDecStages) & 1u) << st);
+    ++issued;
+    return true;
+  };
+  const bool producer = warp == kDecWarps;
+  bool prod_ok = true;
+  if (producer && lane == 0)
+    for (int c = 0; c < min(n_cached, kDecStages) && prod_ok; ++c) prod_ok = issue(c);
   pdl_wait();  // q and this token's key and value come from the QKV projection
   pdl_trigger();
-  if (!pos_ok) {  // a position outside the cache: flagged, the row's output is zero
-    if (threadIdx.x == 0) set_error(GPT2_DEVERR_POSITION);
-    for (int d = threadIdx.x; d < HS; d += blockDim.x) out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(0.f);
-    return;
-  }
-  // the query's dimensions of this lane, scaled by log2(e) / sqrt(hs)
-  float q[kPer];
-  {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + h * HS) + dg);
-    const E* e = reinterpret_cast<const E*>(&raw);
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) q[k] = to_f32(e[k]) * scale_log2;
-  }
-  // this token's key and value: used for position pos, and appended
-  const uint4* kq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + C + h * HS) + dg;
-  const uint4* vq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + 2 * C + h * HS) + dg;
-  if (threadIdx.x < kLPR) {
-    reinterpret_cast<uint4*>(kcache + row(pos) * HS)[dg] = __ldg(kq);
-    reinterpret_cast<uint4*>(vcache + row(pos) * HS)[dg] = __ldg(vq);
-  }
   float m = -INFINITY, l = 0.f, acc[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-  const int nchunk = pos / kChunk + 1;  // chunks covering positions 0 .. pos
-  // K and V rows of chunk c into registers (zero past pos; row pos from the
-  // QKV row)
-  auto load = [&](int c, uint4(&kr)[kIt], uint4(&vr)[kIt]) {
-    const int j0 = c * kChunk + g;
+  if (producer) {
+    if (lane == 0) {
+      for (int c = issued; c < n_cached && prod_ok; ++c) prod_ok = issue(c);
+      // the copies issued here land before the CTA may exit
+      for (int st = 0; st < kDecStages; ++st)
+        if ((filled >> st) & 1u) mbar_wait(&full[st], (fill_par >> st) & 1u);
+    }
+    __syncwarp();
+  } else if (!pos_ok) {  // a position outside the cache: flagged, the row's output is zero
+    if (threadIdx.x == 0) set_error(GPT2_DEVERR_POSITION);
+    for (int d = threadIdx.x; d < HS; d += 32 * kDecWarps) out[static_cast<size_t>(b) * C + h * HS + d] = from_f32<OutT>(0.f);
+  } else {
+    // the query's dimensions of this lane, scaled by log2(e) / sqrt(hs)
+    float q[kPer];
+    {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + h * HS) + dg);
+      const E* e = reinterpret_cast<const E*>(&raw);
 #pragma unroll
-    for (int i = 0; i < kIt; ++i) {
-      const int j = j0 + i * kRPI;
-      if (j < pos) {
-        const size_t rj = row(j) * HS;
-        kr[i] = __ldg(reinterpret_cast<const uint4*>(kcache + rj) + dg);
-        vr[i] = __ldg(reinterpret_cast<const uint4*>(vcache + rj) + dg);
-      } else if (j == pos) {
-        kr[i] = __ldg(kq);
-        vr[i] = __ldg(vq);
-      } else {
-        kr[i] = make_uint4(0u, 0u, 0u, 0u);
-        vr[i] = make_uint4(0u, 0u, 0u, 0u);
+      for (int k = 0; k < kPer; ++k) q[k] = to_f32(e[k]) * scale_log2;
+    }
+    // this token's key and value: used for position pos, and appended
+    const uint4* kq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + C + h * HS) + dg;
+    const uint4* vq = reinterpret_cast<const uint4*>(qkv + static_cast<size_t>(b) * 3 * C + 2 * C + h * HS) + dg;
+    if (threadIdx.x < kLPR) {
+      reinterpret_cast<uint4*>(kcache + row(pos) * HS)[dg] = __ldg(kq);
+      reinterpret_cast<uint4*>(vcache + row(pos) * HS)[dg] = __ldg(vq);
+    }
+    const int nchunk = pos / kChunk + 1;  // chunks covering positions 0 .. pos
+    // K and V rows of chunk c into registers: rows before pos from the
+    // chunk's stage (its copy waited for, the stage freed once read), row pos
+    // from the QKV row, zero past pos
+    auto load = [&](int c, uint4(&kr)[kIt], uint4(&vr)[kIt]) -> bool {
+      const int j0 = c * kChunk;
+      const bool staged = c < n_cached;
+      const int st = c % kDecStages;
+      if (staged && !__all_sync(0xffffffffu, mbar_wait(&full[st], (c / kDecStages) & 1))) return false;
+      const uint8_t* kst = dec_smem + st * kDecStageBytes;
+#pragma unroll
+      for (int i = 0; i < kIt; ++i) {
+        const int r = g + i * kRPI, j = j0 + r;
+        if (j < pos) {
+          kr[i] = reinterpret_cast<const uint4*>(kst + r * kRowBytes)[dg];
+          vr[i] = reinterpret_cast<const uint4*>(kst + kDecStageBytes / 2 + r * kRowBytes)[dg];
+        } else if (j == pos) {
+          kr[i] = __ldg(kq);
+          vr[i] = __ldg(vq);
+        } else {
+          kr[i] = make_uint4(0u, 0u, 0u, 0u);
+          vr[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
+      if (staged) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      return true;
+    };
+    // the online softmax over chunk c's rows
+    auto consume = [&](int c, const uint4(&kr)[kIt], const uint4(&vr)[kIt]) {
+      const int j0 = c * kChunk + g;
+      // scores (log2 units) of this lane's kIt rows; the row's kLPR lanes
+      // each hold a partial dot product and sum it by shuffles
+      float sc[kIt];
+      float cmax = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kIt; ++i) {
+        const E* e = reinterpret_cast<const E*>(&kr[i]);
+        float d = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) d = fmaf(q[k], to_f32(e[k]), d);
+#pragma unroll
+        for (int o = kLPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        sc[i] = (j0 + i * kRPI <= pos) ? d : -INFINITY;
+        cmax = fmaxf(cmax, sc[i]);
+      }
+#pragma unroll
+      for (int o = 16; o >= kLPR; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+      // position c * kChunk <= pos is in the chunk, so cmax is finite
+      const float m_new = fmaxf(m, cmax);
+      const float alpha = exp2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
+      l *= alpha;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) acc[k] *= alpha;
+#pragma unroll
+      for (int i = 0; i < kIt; ++i) {
+        const float p = exp2_approx(sc[i] - m_new);  // 0 past pos
+        l += p;
+        const E* e = reinterpret_cast<const E*>(&vr[i]);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) acc[k] = fmaf(p, to_f32(e[k]), acc[k]);
+      }
+      m = m_new;
+    };
+    // this warp's chunks c = warp, warp + kDecWarps, ...
+    for (int c = warp; c < nchunk; c += kDecWarps) {
+      uint4 kr[kIt], vr[kIt];
+      if (!load(c, kr, vr)) break;
+      consume(c, kr, vr);
     }
-  };
-  // the online softmax over chunk c's rows
-  auto consume = [&](int c, const uint4(&kr)[kIt], const uint4(&vr)[kIt]) {
-    const int j0 = c * kChunk + g;
-    // scores (log2 units) of this lane's kIt rows; the row's kLPR lanes
-    // each hold a partial dot product and sum it by shuffles
-    float sc[kIt];
-    float cmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kIt; ++i) {
-      const E* e = reinterpret_cast<const E*>(&kr[i]);
-      float d = 0.f;
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) d = fmaf(q[k], to_f32(e[k]), d);
-#pragma unroll
-      for (int o = kLPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-      sc[i] = (j0 + i * kRPI <= pos) ? d : -INFINITY;
-      cmax = fmaxf(cmax, sc[i]);
-    }
-#pragma unroll
-    for (int o = 16; o >= kLPR; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-    // position c * kChunk <= pos is in the chunk, so cmax is finite
-    const float m_new = fmaxf(m, cmax);
-    const float alpha = exp2_approx(m - m_new);  // 0 on the first chunk (m = -inf)
-    l *= alpha;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) acc[k] *= alpha;
-#pragma unroll
-    for (int i = 0; i < kIt; ++i) {
-      const float p = exp2_approx(sc[i] - m_new);  // 0 past pos
-      l += p;
-      const E* e = reinterpret_cast<const E*>(&vr[i]);
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) acc[k] = fmaf(p, to_f32(e[k]), acc[k]);
-    }
-    m = m_new;
-  };
-  // this warp's chunks c = warp, warp + kDecWarps, ...  (measured in a
-  // decode step: a second register buffer, loading the next chunk while one
-  // is used, with chunks half as long to keep three CTAs per SM, made the
-  // step no faster)
-  for (int c = warp; c < nchunk; c += kDecWarps) {
-    uint4 kr[kIt], vr[kIt];
-    load(c, kr, vr);
-    consume(c, kr, vr);
   }
   // sum over the rows of an instruction: every lane then holds the warp's
   // sum and its dimensions' output
@@ -479,15 +526,18 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 #pragma unroll
     for (int k = 0; k < kPer; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
   }
-  if (lane == 0) {
-    m_s[warp] = m;
-    l_s[warp] = l;
-  }
-  if (g == 0) {
+  if (!producer) {
+    if (lane == 0) {
+      m_s[warp] = m;
+      l_s[warp] = l;
+    }
+    if (g == 0) {
 #pragma unroll
-    for (int k = 0; k < kPer; ++k) o_s[warp][dg * kPer + k] = acc[k];
+      for (int k = 0; k < kPer; ++k) o_s[warp][dg * kPer + k] = acc[k];
+    }
   }
   __syncthreads();
+  if (!pos_ok) return;
   for (int d = threadIdx.x; d < HS; d += blockDim.x) {
     float M = -INFINITY;
 #pragma unroll
@@ -549,8 +599,17 @@ template <typename E, typename OutT, int HS>
 static void decode_typed(OutT* out, const E* qkv, E* kc, E* vc, int B, int C, int NH, int pos, const int* pos_arr,
                          const KVRows& rows, cudaStream_t s) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(HS));
-  launch_pdl(decode_attn_kernel<E, OutT, HS>, dim3(NH, B), dim3(32 * kDecWarps), 0, s, out, qkv, kc, vc, C, NH, pos,
-             pos_arr, rows, scale_log2);
+  // the ring of cache chunks is dynamic shared memory beyond the 48 KB a
+  // launch gets without asking (set once per instantiation and device)
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(decode_attn_kernel<E, OutT, HS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kDecSmem) == cudaSuccess)
+      attr_set[dev] = true;
+  }
+  launch_pdl(decode_attn_kernel<E, OutT, HS>, dim3(NH, B), dim3(32 * (kDecWarps + 1)), kDecSmem, s, out, qkv, kc, vc,
+             C, NH, pos, pos_arr, rows, scale_log2);
 }
 
 template <typename E>
