@@ -328,6 +328,11 @@ constexpr int kDecWarps = 4;       // warps computing; one more issues the copie
 constexpr int kDecStages = 8;      // chunks of the cache in shared memory
 constexpr int kDecStageBytes = 8192;  // a chunk's K rows, then its V rows (4 KB each)
 constexpr int kDecSmem = kDecStages * kDecStageBytes + 2 * kDecStages * 8;
+// chunk c goes to warp c % kDecWarps and stage c % kDecStages: with the
+// stages a multiple of the warps, the chunks that share a stage share a
+// warp too, so no warp waits on a stage's barrier more than one phase ahead
+// of the fill it needs (a waiter two phases ahead would pass at once)
+static_assert(kDecStages % kDecWarps == 0, "stages per warp");
 
 template <typename E, typename OutT, int HS>
 __global__ void __launch_bounds__(32 * (kDecWarps + 1))
