@@ -71,6 +71,11 @@
 // drains its copies and MMAs, frees TMEM and returns.
 #include "kernels.cuh"
 
+#include <functional>
+#include <queue>
+#include <utility>
+#include <vector>
+
 namespace gpt2 {
 namespace {
 
@@ -130,16 +135,34 @@ struct Schedule {
 };
 
 // A unit: query tiles 2u and 2u + 1 of one (sequence b, head h).  Units are
-// numbered by decreasing length (u from the last), then b, then h; CTA c of
-// G takes units c, 2G - 1 - c, 2G + c, 4G - 1 - c, ... (alternate rounds
-// run backwards, which evens out the sum of lengths over the CTAs).
+// numbered by decreasing length (u from the last), then b, then h.  Which
+// CTA takes which units comes from a table made on the host: longest
+// first, each unit to the CTA with the least work so far (for B = 16, T =
+// 1024, 12 heads on 152 CTAs the busiest CTA has 47 steps, against 50 with
+// the rule below; measured, the launch about 1 % shorter).  Past the
+// table's size CTA c of G takes units c, 2G - 1 - c, 2G + c, 4G - 1 - c,
+// ... (alternate rounds run backwards).
+constexpr int kSchedMaxCtas = 160;
+constexpr int kSchedMaxUnits = 1600;
+struct UnitSchedule {
+  int n;                                 // units in the table; 0: no table
+  uint16_t first[kSchedMaxCtas + 1];     // CTA c's units are unit[first[c] .. first[c + 1])
+  uint16_t unit[kSchedMaxUnits];         // unit numbers, each CTA's in increasing order
+};
+// a kernel's parameters are at most 4 KB: the table beside two tensor maps
+static_assert(sizeof(UnitSchedule) <= 3584, "kernel parameter space");
 struct Unit {
   int b, h, u, n_kv;
   Schedule sch;
 };
 struct UnitList {
   int c, G, n_units, per_u, NH, T, U;
+  const UnitSchedule* tab;
   __device__ int id(int i) const {  // the CTA's i-th unit, or -1
+    if (tab->n > 0) {
+      const int e = tab->first[c] + i;
+      return e < tab->first[c + 1] ? static_cast<int>(tab->unit[e]) : -1;
+    }
     const int k = i * G + ((i & 1) ? G - 1 - c : c);
     return k < n_units ? k : -1;
   }
@@ -188,7 +211,8 @@ struct Cursor {
 template <typename T16, typename OutT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc05_kernel(const __grid_constant__ CUtensorMap tmap_qkv, const __grid_constant__ CUtensorMap tmap_out,
-                     float* __restrict__ lse, int B, int T, int NH, int Tp, float scale_log2) {
+                     float* __restrict__ lse, int B, int T, int NH, int Tp, float scale_log2,
+                     const __grid_constant__ UnitSchedule sched) {
   using L = Smem;
   constexpr int kKV = L::kKV;
   extern __shared__ uint8_t smem_raw[];
@@ -229,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ul.NH = NH;
   ul.T = T;
   ul.U = U;
+  ul.tab = &sched;
   constexpr uint32_t kFmt = std::is_same<T16, __half>::value ? 0u : 1u;
   constexpr uint32_t kIdescS = make_idesc(kFmt, kTQ, kTK);
   constexpr uint32_t kIdescPV = make_idesc(kFmt, kTQ, kHS) | (1u << 16);  // B (V) MN-major
@@ -676,6 +701,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The units' table for G CTAs: units in their numbering (non-increasing
+// length), each to the CTA with the least work so far, ties to the lowest
+// CTA; a unit's work is its steps plus one (its first loads and its
+// epilogue cost about a step).  No table (n = 0) past the table's size.
+// Kept per thread for the last shape asked.
+const UnitSchedule& unit_schedule(int B, int T, int NH, int G) {
+  thread_local UnitSchedule sc{};
+  thread_local int key[4] = {-1, -1, -1, -1};
+  if (key[0] == B && key[1] == T && key[2] == NH && key[3] == G) return sc;
+  key[0] = B;
+  key[1] = T;
+  key[2] = NH;
+  key[3] = G;
+  sc = UnitSchedule{};
+  const int U = (T + 2 * kTQ - 1) / (2 * kTQ), per_u = B * NH, kv_tiles = (T + kTK - 1) / kTK;
+  const long long n_units = static_cast<long long>(U) * per_u;
+  if (G <= 0 || G > kSchedMaxCtas || n_units > kSchedMaxUnits) return sc;
+  std::vector<std::vector<int>> lists(G);
+  using Load = std::pair<long long, int>;  // (work so far, CTA)
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+  for (int c = 0; c < G; ++c) least.push({0, c});
+  for (int k = 0; k < n_units; ++k) {
+    const int u = U - 1 - k / per_u;
+    const int n_a = std::min(2 * u + 1, kv_tiles);
+    const int n_b = (2 * u + 1) * kTQ < T ? std::min(2 * u + 2, kv_tiles) : 0;
+    const Load top = least.top();
+    least.pop();
+    lists[top.second].push_back(k);
+    least.push({top.first + n_a + n_b + 1, top.second});
+  }
+  int e = 0;
+  for (int c = 0; c < G; ++c) {
+    sc.first[c] = static_cast<uint16_t>(e);
+    for (int k : lists[c]) sc.unit[e++] = static_cast<uint16_t>(k);
+  }
+  sc.first[G] = static_cast<uint16_t>(e);
+  sc.n = e;
+  return sc;
+}
+
 template <typename T16, typename OutT>
 int launch_typed(void* out, float* lse, const CUtensorMap& map, int B, int T, int C, int NH, cudaStream_t s) {
   // the output [B][T][C] as boxes of 128 bytes x 32 rows (one warp's rows),
@@ -719,7 +784,8 @@ int launch_typed(void* out, float* lse, const CUtensorMap& map, int B, int T, in
   cfg.attrs = attr;
   cfg.numAttrs = pdl_on() ? 1 : 0;
   const int Tp = (T + kTQ - 1) / kTQ * kTQ;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, map_out, lse, B, T, NH, Tp, scale_log2);
+  const UnitSchedule& sched = unit_schedule(B, T, NH, static_cast<int>(cfg.gridDim.x));
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, map_out, lse, B, T, NH, Tp, scale_log2, sched);
   return e == cudaSuccess ? GPT2_OK : note_cuda_error(e);
 }
 }  // namespace
