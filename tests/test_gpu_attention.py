@@ -125,6 +125,25 @@ def test_attention_ragged_launch_with_several_units_per_cta(precision):
         assert_close(got[b:b + 1], oracle.attention(qkv[b:b + 1], NH), atol=TOL[precision], what=f"sequence {b}")
 
 
+def test_attention_launch_past_the_unit_table():
+    # B=136, T=250, 12 heads of 64: one unit per (sequence, head), the
+    # second query tile ragged (122 rows); 1632 units, more than the
+    # host-made table holds (1600), so the CTAs take units round-robin,
+    # alternate rounds backwards.  Sequences 0, 67 and 135 against the
+    # oracle.
+    B, T, C, NH = 136, 250, 768, 12
+    qkv = inputs.make_normal(421, (B, T, 3 * C), 0.55)
+    out = torch.full((B, T, C), float("nan"), dtype=torch.float32, device="cuda")
+    wsz = ab.attention_workspace_size(B, T, C, ab.GPT2_FP16)
+    ws = torch.empty(max(wsz, 1), dtype=torch.uint8, device="cuda")
+    ab.attention_forward(out, dev(qkv), B, T, C, NH, ab.GPT2_FP16, ws, wsz)
+    no_device_error()
+    got = host(out)
+    assert np.isfinite(got).all()
+    for b in (0, 67, B - 1):
+        assert_close(got[b:b + 1], oracle.attention(qkv[b:b + 1], NH), atol=TOL[ab.GPT2_FP16], what=f"sequence {b}")
+
+
 def test_attention_causal_bitwise():
     B, T, C, NH = 1, 150, 768, 12
     qkv = inputs.make_normal(9, (B, T, 3 * C), 0.55)
