@@ -332,8 +332,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // logits epilogue: this row's running max and sum of exp over the
       // tile's columns below V
       float run_m = -INFINITY, run_s = 0.f;
+      // a warp whose 32 rows all lie past M (a few activation rows, as the
+      // decode step's LM head has) has nothing to write: it only frees the
+      // accumulator
+      const bool live = m0 < M;
 #pragma unroll 1
-      for (int ch = col_half * (kBN / kChunkCols / 2); ch < (col_half + 1) * (kBN / kChunkCols / 2); ++ch) {
+      for (int ch = col_half * (kBN / kChunkCols / 2); live && ch < (col_half + 1) * (kBN / kChunkCols / 2); ++ch) {
         const int col0 = n0 + ch * kChunkCols;
         bool ok = true;
         if constexpr (kAux) {  // the residual (or GELU input) tile into the staging buffer
