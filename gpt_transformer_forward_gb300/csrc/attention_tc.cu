@@ -537,13 +537,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // instructions per chunk); a chunk caught without such a key is
         // recomputed with the same m below.  Four independent chains for the
         // sum keep the SFU fed.
-        auto softmax_chunk = [&](int c, const uint32_t(&cur)[32], bool check) -> bool {
+        // kFull: every key of the tile visible to every row of the warp,
+        // known at compile time (no masking code)
+        auto softmax_chunk = [&](int c, const uint32_t(&cur)[32], bool check, auto full) -> bool {
+          constexpr bool kFull = decltype(full)::value;
           const float2 sc = make_float2(scale_log2, scale_log2), nm = make_float2(-m_run, -m_run);
           float2 xv[16];
   #pragma unroll
           for (int i = 0; i < 16; ++i)
             xv[i] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sc, nm);
-          if (!all_full) {
+          if (!kFull && !all_full) {
   #pragma unroll
             for (int i = 0; i < 16; ++i) {
               if (c * 32 + 2 * i >= valid) xv[i].x = -INFINITY;
@@ -593,23 +596,43 @@ __global__ void __launch_bounds__(kThreads, 1)
               m_run = mx * scale_log2;
             }
           }
-          auto chunk = [&](auto cc, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
+          // a full tile (all its keys visible to every row of the warp: n_live
+          // is 4) runs a copy without the masking and live-chunk tests: the
+          // pass 0.621 -> 0.610 ms (measured); the chunks' indices stay
+          // compile-time constants (a loop over chunk pairs, half the code,
+          // took 0.665)
+          auto chunk = [&](auto cc, auto full, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
             constexpr int c = decltype(cc)::value;
+            constexpr bool kFull = decltype(full)::value;
             if (!go) return;
-            if (c >= n_live) {
+            if (!kFull && c >= n_live) {
               zero_chunk(c);
               return;
             }
-            if (c + 1 < n_live) tmem_ld_32x32b_x32(lane_base + s_col + (c + 1) * 32, nxt);
-            go = softmax_chunk(c, cur, true);
+            const bool next_live = kFull ? (c + 1 < kTK / 32) : (c + 1 < n_live);
+            if (next_live) tmem_ld_32x32b_x32(lane_base + s_col + (c + 1) * 32, nxt);
+            go = softmax_chunk(c, cur, true, full);
             if (!go) fail = c;
-            if (c + 1 < n_live) tmem_ld_wait_regs(nxt);
+            if (next_live) tmem_ld_wait_regs(nxt);
           };
           static_assert(kTK == 128, "four chunks of 32 keys");
-          chunk(std::integral_constant<int, 0>(), ra, rb);
-          chunk(std::integral_constant<int, 1>(), rb, ra);
-          chunk(std::integral_constant<int, 2>(), ra, rb);
-          chunk(std::integral_constant<int, 3>(), rb, ra);
+          using I0 = std::integral_constant<int, 0>;
+          using I1 = std::integral_constant<int, 1>;
+          using I2 = std::integral_constant<int, 2>;
+          using I3 = std::integral_constant<int, 3>;
+          if (all_full) {
+            const std::true_type f;
+            chunk(I0(), f, ra, rb);
+            chunk(I1(), f, rb, ra);
+            chunk(I2(), f, ra, rb);
+            chunk(I3(), f, rb, ra);
+          } else {
+            const std::false_type f;
+            chunk(I0(), f, ra, rb);
+            chunk(I1(), f, rb, ra);
+            chunk(I2(), f, ra, rb);
+            chunk(I3(), f, rb, ra);
+          }
           done = go;
         }
         if (!done) {
@@ -669,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t rr[32];
             tmem_ld_32x32b_x32(lane_base + s_col + c * 32, rr);
             tmem_ld_wait_regs(rr);
-            softmax_chunk(c, rr, false);
+            softmax_chunk(c, rr, false, std::false_type());
           }
         }
         l_run += sum2.x + sum2.y;
