@@ -597,10 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // a full tile (all its keys visible to every row of the warp: n_live
-          // is 4) runs a copy without the masking and live-chunk tests: the
-          // pass 0.621 -> 0.610 ms (measured); the chunks' indices stay
-          // compile-time constants (a loop over chunk pairs, half the code,
-          // took 0.665)
+          // is 4) runs a copy without the masking and live-chunk tests
+          // (measured: 12 layers at B = 16, T = 1024 went 0.621 -> 0.610
+          // ms); the chunks' indices stay compile-time constants (a loop
+          // over chunk pairs, half the code, took 0.665 ms)
           auto chunk = [&](auto cc, auto full, uint32_t(&cur)[32], uint32_t(&nxt)[32]) {
             constexpr int c = decltype(cc)::value;
             constexpr bool kFull = decltype(full)::value;
