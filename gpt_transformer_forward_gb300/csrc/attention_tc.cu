@@ -516,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // exponentials are not computed
         const int n_live = (__reduce_max_sync(0xffffffffu, valid) + 31) >> 5;
         const bool all_full = __all_sync(0xffffffffu, valid == kTK);
+        // keys below min_valid are visible to every row of the warp: a chunk
+        // below it needs no masking
+        const int min_valid = __reduce_min_sync(0xffffffffu, static_cast<unsigned>(valid));
         // P V of this group's previous step s_prev (tile j - 1) must be done
         // before O is rescaled.  Its ring slot's barrier is unambiguous then:
         // P V of step s_prev - 3 finished before S of step s (issued after
@@ -546,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   #pragma unroll
           for (int i = 0; i < 16; ++i)
             xv[i] = __ffma2_rn(make_float2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])), sc, nm);
-          if (!kFull && !all_full) {
+          if (!kFull && c * 32 + 32 > min_valid) {
   #pragma unroll
             for (int i = 0; i < 16; ++i) {
               if (c * 32 + 2 * i >= valid) xv[i].x = -INFINITY;
