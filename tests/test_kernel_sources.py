@@ -5,7 +5,10 @@ start while the kernel ahead of it on the stream still runs; it is correct
 only if its body waits (griddepcontrol.wait, pdl_wait()) before it touches
 what that kernel writes.  Every kernel that can get the attribute must
 therefore contain pdl_wait(): the kernels passed to launch_pdl, and the two
-GEMM kernels that set the attribute in their own launch configuration."""
+GEMM kernels that set the attribute in their own launch configuration.
+
+Every barrier wait is bounded in time and no kernel traps: the checks below
+keep a lost arrival or a failed check from hanging or faulting the GPU."""
 import os
 import re
 
@@ -84,3 +87,54 @@ def test_the_check_sees_a_missing_wait():
     assert _pdl_kernels({"planted.cu": src}) == ["bad_kernel", "good_kernel"]
     assert "pdl_wait()" in _kernel_body(src, "good_kernel")
     assert "pdl_wait()" not in _kernel_body(src, "bad_kernel")
+
+
+# Every wait on an mbarrier gives up after a time limit (about a second),
+# records GPT2_DEVERR_TIMEOUT and returns, so that a lost arrival cannot
+# hang the GPU.  The waiting instructions therefore appear only inside the
+# bounded helpers of common.cuh, and every endless loop there checks the
+# clock.
+
+def _loops(text):
+    """Bodies of the `for (;;)` and `while (true)` loops of a source."""
+    out = []
+    for m in re.finditer(r"for\s*\(\s*;\s*;\s*\)|while\s*\(\s*(true|1)\s*\)", text):
+        i = text.index("{", m.end())
+        depth = 0
+        for j in range(i, len(text)):
+            if text[j] == "{":
+                depth += 1
+            elif text[j] == "}":
+                depth -= 1
+                if depth == 0:
+                    out.append(text[i:j + 1])
+                    break
+    return out
+
+
+def test_barrier_waits_only_in_the_bounded_helpers():
+    srcs = _sources()
+    for f, text in srcs.items():
+        if f == "common.cuh":
+            continue
+        for word in ("mbarrier.try_wait", "mbarrier.test_wait"):
+            assert word not in text, f"{f} waits on a barrier outside the bounded helpers ({word})"
+
+
+def test_every_endless_loop_has_a_time_limit():
+    for f, text in _sources().items():
+        for body in _loops(text):
+            assert re.search(r"globaltimer_ns\(\)\s*-\s*t0\s*>", body), f"{f}: an endless loop without a time limit"
+
+
+def test_the_loop_check_sees_an_unbounded_spin():
+    bad = "__device__ void f(volatile int* p) { for (;;) { if (*p) return; } }"
+    assert _loops(bad) and not re.search(r"globaltimer_ns\(\)\s*-\s*t0\s*>", _loops(bad)[0])
+
+
+def test_no_device_traps():
+    # no trap instruction and no device assert (a failed one traps): errors
+    # are reported through the device error word
+    for f, text in _sources().items():
+        assert "__trap" not in text and "trap;" not in text, f"{f} traps"
+        assert not re.search(r"(?<![A-Za-z_])assert\s*\(", text), f"{f} has a device assert"
